@@ -1,0 +1,263 @@
+/*
+ * CPU oracle for the GEMV library -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg use
+ * this file.  The library's product path never links, loads or calls it, and
+ * it shares no code, header or table with the CUDA sources.
+ *
+ * What it computes (double precision, plain loops, column index ascending):
+ *
+ *   y[i] = sum_{j=0}^{N-1} w(i,j) * x(j)
+ *
+ *   "Making GEMV Fast", section "Algorithm": every output is the dot product of
+ *   one row of A with x; "Row-major indexing refresher": A(r,c) = A[r*N + c].
+ *   "llama.cpp GEMV CUDA": y_i = sum_j W_ij x_j with W [M, d] row-major.
+ *
+ *   f32: w = A[i*N+j],                 x = x[j]           (FP32 storage)
+ *   f16: w = dec16(A[i*N+j]),          x = dec16(x[j])    (binary16 storage)
+ *   q8 : w = dec16(S[i*g + j/128]) * (int8)A[i*N+j]
+ *   q4 : byte b = A[i*(N/2) + j/2]; nibble = low 4 bits for even j, high 4
+ *        bits for odd j, read as 4-bit two's complement in [-8, 7];
+ *        w = dec16(S[i*g + j/128]) * nibble
+ *        with g = ceil(N/128) FP16 scales per row ("membound", section
+ *        "dequant GEMV": weights dequantised in register as q times the
+ *        group scale; the reference there is computed on q*s exactly).
+ *
+ * Alongside y it returns den[i] = sum_j |w(i,j)| * |x(j)|, the normaliser of
+ * the parity metric |y_gpu - y_ref| / den.
+ *
+ * dec16 is written from the IEEE 754 binary16 definition: 1 sign bit, 5
+ * exponent bits with bias 15, 10 fraction bits; exponent 0 encodes zero and
+ * subnormals (fraction * 2^-24), exponent 31 encodes inf / NaN.
+ *
+ * Rows may be requested one by one (a list of row indices) so that a parity
+ * check at full size can sample outputs.  Rows are split across threads with
+ * OpenMP; each row is still summed by one thread in column order, so the
+ * result does not depend on the thread count.
+ *
+ * Counting model ("Making GEMV Fast", sections "Memory Access" and
+ * "Computation"): FLOPs = M(2N-1) = 2MN - M; FP32 bytes = 4(MN + N + M),
+ * generalised per storage type as bytes(A) + bytes(scales) + bytes(x) + 4M.
+ *
+ * Built with ORACLE_MUTANT=k (k > 0) it contains one deliberate mistake; the
+ * test-suite builds those variants to show that its pins catch each one.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#define ORACLE_GROUP 128
+
+/* ---- IEEE 754 binary16 -> double ---------------------------------------- */
+
+double oracle_dec16(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1F;
+    const int frac = h & 0x3FF;
+    double mag;
+    if (expo == 0) {
+#if ORACLE_MUTANT == 5
+        mag = ldexp(1.0 + frac / 1024.0, -15); /* subnormals treated as normals */
+#else
+        mag = ldexp((double)frac, -24);        /* zero and subnormals */
+#endif
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp(1024.0 + frac, expo - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+void oracle_dec16_array(const uint16_t *h, double *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_dec16(h[k]);
+}
+
+/* ---- weight of element (i, j) per storage type ---------------------------- */
+
+static int64_t n_groups(int64_t N) { return (N + ORACLE_GROUP - 1) / ORACLE_GROUP; }
+
+static double w_f32(const float *A, int64_t M, int64_t N, int64_t i, int64_t j)
+{
+#if ORACLE_MUTANT == 4
+    (void)N;
+    return (double)A[j * M + i]; /* transposed operand (column-major read) */
+#else
+    (void)M;
+    return (double)A[i * N + j];
+#endif
+}
+
+static double w_f16(const uint16_t *A, int64_t N, int64_t i, int64_t j)
+{
+    return oracle_dec16(A[i * N + j]);
+}
+
+static double scale_of(const uint16_t *S, int64_t N, int64_t i, int64_t j)
+{
+#if ORACLE_MUTANT == 3
+    return oracle_dec16(S[i * n_groups(N) + j / 64]); /* wrong group width */
+#elif ORACLE_MUTANT == 7
+    return oracle_dec16(S[i * (N / ORACLE_GROUP) + j / ORACLE_GROUP]); /* floor(N/128) pitch */
+#else
+    return oracle_dec16(S[i * n_groups(N) + j / ORACLE_GROUP]);
+#endif
+}
+
+static double w_q8(const int8_t *A, const uint16_t *S, int64_t N, int64_t i, int64_t j)
+{
+    return scale_of(S, N, i, j) * (double)A[i * N + j];
+}
+
+static int q4_code(const uint8_t *A, int64_t N, int64_t i, int64_t j)
+{
+    const uint8_t b = A[i * (N / 2) + j / 2];
+#if ORACLE_MUTANT == 1
+    const int nib = (j & 1) ? (b & 0xF) : (b >> 4); /* nibble order swapped */
+#else
+    const int nib = (j & 1) ? (b >> 4) : (b & 0xF);
+#endif
+#if ORACLE_MUTANT == 2
+    return nib - 8; /* offset-8 instead of two's complement */
+#else
+    return nib >= 8 ? nib - 16 : nib;
+#endif
+}
+
+static double w_q4(const uint8_t *A, const uint16_t *S, int64_t N, int64_t i, int64_t j)
+{
+    return scale_of(S, N, i, j) * (double)q4_code(A, N, i, j);
+}
+
+/* ---- one row ------------------------------------------------------------- */
+
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_Q8 = 2, ORACLE_Q4 = 3 };
+
+static double x_of(int kind, const void *x, int64_t j)
+{
+    if (kind == ORACLE_F32) return (double)((const float *)x)[j];
+    return oracle_dec16(((const uint16_t *)x)[j]);
+}
+
+static double w_of(int kind, const void *A, const uint16_t *S, int64_t M, int64_t N, int64_t i,
+                   int64_t j)
+{
+    switch (kind) {
+    case ORACLE_F32: return w_f32((const float *)A, M, N, i, j);
+    case ORACLE_F16: return w_f16((const uint16_t *)A, N, i, j);
+    case ORACLE_Q8: return w_q8((const int8_t *)A, S, N, i, j);
+    default: return w_q4((const uint8_t *)A, S, N, i, j);
+    }
+}
+
+static void one_row(int kind, const void *A, const void *x, const uint16_t *S, int64_t M,
+                    int64_t N, int64_t i, double *y, double *den)
+{
+    double acc = 0.0, mag = 0.0;
+#if ORACLE_MUTANT == 6
+    const int64_t jend = N > 0 ? N - 1 : 0; /* last column dropped */
+#else
+    const int64_t jend = N;
+#endif
+    for (int64_t j = 0; j < jend; ++j) {
+        const double w = w_of(kind, A, S, M, N, i, j);
+        const double v = x_of(kind, x, j);
+        acc += w * v;
+        mag += fabs(w) * fabs(v);
+    }
+    *y = acc;
+    *den = mag;
+}
+
+static int run_rows(int kind, const void *A, const void *x, const uint16_t *S, int64_t M,
+                    int64_t N, const int64_t *rows, int64_t nrows, double *y, double *den,
+                    int threads)
+{
+    if (M < 0 || N < 0 || nrows < 0 || !y || !den) return -1;
+    if ((M > 0 && N > 0) && (!A || !x)) return -1;
+    if ((kind == ORACLE_Q8 || kind == ORACLE_Q4) && M > 0 && N > 0 && !S) return -1;
+    if (kind == ORACLE_Q4 && (N % 2)) return -1;
+    if (!rows) nrows = M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) return -1;
+    }
+    if (threads < 1) threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 16)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        one_row(kind, A, x, S, M, N, i, &y[r], &den[r]);
+    }
+    return 0;
+}
+
+int oracle_gemv_f32(const float *A, const float *x, int64_t M, int64_t N, const int64_t *rows,
+                    int64_t nrows, double *y, double *den, int threads)
+{
+    return run_rows(ORACLE_F32, A, x, NULL, M, N, rows, nrows, y, den, threads);
+}
+
+int oracle_gemv_f16(const uint16_t *A, const uint16_t *x, int64_t M, int64_t N,
+                    const int64_t *rows, int64_t nrows, double *y, double *den, int threads)
+{
+    return run_rows(ORACLE_F16, A, x, NULL, M, N, rows, nrows, y, den, threads);
+}
+
+int oracle_gemv_q8(const int8_t *A, const uint16_t *x, const uint16_t *S, int64_t M, int64_t N,
+                   const int64_t *rows, int64_t nrows, double *y, double *den, int threads)
+{
+    return run_rows(ORACLE_Q8, A, x, S, M, N, rows, nrows, y, den, threads);
+}
+
+int oracle_gemv_q4(const uint8_t *A, const uint16_t *x, const uint16_t *S, int64_t M, int64_t N,
+                   const int64_t *rows, int64_t nrows, double *y, double *den, int threads)
+{
+    return run_rows(ORACLE_Q4, A, x, S, M, N, rows, nrows, y, den, threads);
+}
+
+/* ---- dequantised weights (the q*s the reference is computed on) --------- */
+
+int oracle_dequant_q8(const int8_t *A, const uint16_t *S, int64_t M, int64_t N, double *W)
+{
+    if (M < 0 || N < 0 || ((M > 0 && N > 0) && (!A || !S || !W))) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) W[i * N + j] = w_q8(A, S, N, i, j);
+    return 0;
+}
+
+int oracle_dequant_q4(const uint8_t *A, const uint16_t *S, int64_t M, int64_t N, double *W)
+{
+    if (M < 0 || N < 0 || (N % 2) || ((M > 0 && N > 0) && (!A || !S || !W))) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) W[i * N + j] = w_q4(A, S, N, i, j);
+    return 0;
+}
+
+/* ---- counting model ------------------------------------------------------ */
+
+double oracle_flops(int64_t M, int64_t N)
+{
+    if (M <= 0 || N <= 0) return 0.0;
+    return (double)M * (double)(2 * N - 1);
+}
+
+/* bytes read (A, scales, x) plus bytes written (y, FP32) for one call */
+double oracle_bytes(int kind, int64_t M, int64_t N)
+{
+    const double m = (double)M, n = (double)N;
+    switch (kind) {
+    case ORACLE_F32: return 4.0 * (m * n + n + m);
+    case ORACLE_F16: return 2.0 * m * n + 2.0 * n + 4.0 * m;
+    case ORACLE_Q8: return m * n + 2.0 * m * (double)n_groups(N) + 2.0 * n + 4.0 * m;
+    case ORACLE_Q4: return m * n / 2.0 + 2.0 * m * (double)n_groups(N) + 2.0 * n + 4.0 * m;
+    default: return -1.0;
+    }
+}
+
+int oracle_mutant_id(void) { return ORACLE_MUTANT; }

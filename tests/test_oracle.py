@@ -1,0 +1,299 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each ``pin_*`` function checks the oracle against something other than
+itself: values the pages print (``tests/golden``), closed forms, exact
+rational brute force, numpy's own binary16 decoding, and hand-built int4
+byte tables.  ``test_mutants_are_caught`` builds the oracle with one planted
+mistake at a time and requires at least one pin to fail for each.
+"""
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ONE_F16 = 0x3C00
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _f16_value(bits):
+    """Independent FP16 decode (numpy's), used only as a check on the oracle."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _scales_ones(M, N):
+    return np.full((M, synth.n_groups(N)), ONE_F16, dtype=np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# pins
+# ---------------------------------------------------------------------------
+
+def pin_dec16_all_patterns(orc):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = orc.dec16(bits)
+    ref = _f16_value(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+    named = {0x3C00: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24,
+             0x0400: 2.0 ** -14, 0x7BFF: 65504.0, 0x7C00: np.inf, 0xFC00: -np.inf}
+    for b, v in named.items():
+        assert orc.dec16([b])[0] == v, hex(b)
+
+
+def pin_rowmajor_worked_example(orc):
+    g = _golden("rowmajor_worked_example.json")
+    M, N = g["M"], g["N"]
+    flat = np.arange(M * N)
+    assert flat.reshape(M, N)[g["probe_row"], g["probe_col"]] == flat[g["probe_offset"]]
+    expect = np.array([flat[i * N + g["probe_col"]] for i in range(M)], dtype=np.float64)
+    assert list(expect) == [2.0, 6.0, 10.0]
+    e = np.zeros(N)
+    e[g["probe_col"]] = 1.0
+    cases = {
+        "f32": (flat.astype(np.float32), e.astype(np.float32), None),
+        "f16": (synth.to_f16_bits(flat.astype(np.float64)), synth.to_f16_bits(e), None),
+        "q8": (flat.astype(np.int8), synth.to_f16_bits(e), _scales_ones(M, N)),
+    }
+    for dt, (A, x, s) in cases.items():
+        y, den = orc.gemv(dt, A.reshape(M, N), x, M, N, scales=s)
+        assert np.array_equal(y, expect), dt
+        assert y[g["probe_row"]] == flat[g["probe_offset"]], dt
+        assert np.array_equal(den, np.abs(expect)), dt
+
+
+def pin_identity(orc):
+    for n in (1, 6, 130):
+        eye = np.eye(n)
+        xf = synth.uniform(7, 2, 0, n, -1, 1).astype(np.float32)
+        y, _ = orc.gemv("f32", eye.astype(np.float32), xf, n, n)
+        assert np.array_equal(y, xf.astype(np.float64))
+        xb = synth.to_f16_bits(synth.normal(7, 2, 0, n, 1.0))
+        xv = _f16_value(xb)
+        y, _ = orc.gemv("f16", synth.to_f16_bits(eye), xb, n, n)
+        assert np.array_equal(y, xv)
+        y, _ = orc.gemv("q8", eye.astype(np.int8), xb, n, n, scales=_scales_ones(n, n))
+        assert np.array_equal(y, xv)
+        if n % 2 == 0:
+            Aq = synth.pack_int4(eye.astype(np.int64))
+            y, _ = orc.gemv("q4", Aq, xb, n, n, scales=_scales_ones(n, n))
+            assert np.array_equal(y, xv)
+
+
+def _grouped_quant_case(dtype, M=3, N=300):
+    """Random codes and per-(row, group) power-of-two scales, all exact in FP16."""
+    lo, hi = (-127, 127) if dtype == "q8" else (-8, 7)
+    q = synth.integers(11, 1, 0, M * N, lo, hi).reshape(M, N)
+    g = synth.n_groups(N)
+    expo = np.arange(M * g).reshape(M, g) - 6
+    s_val = np.ldexp(1.0, expo)
+    s_bits = synth.to_f16_bits(s_val)
+    A = q.astype(np.int8) if dtype == "q8" else synth.pack_int4(q)
+    return q, A, s_val, s_bits
+
+
+def pin_unit_vectors(orc):
+    M, N = 3, 300
+    for dt in ("f32", "f16"):
+        w = synth.random_case(dt, M, N, 5)
+        A = synth.weight_rows(w, 0, M)
+        Av = A.astype(np.float64) if dt == "f32" else _f16_value(A)
+        for k in (0, 1, 127, 128, 299):
+            e = np.zeros(N)
+            e[k] = 1.0
+            x = e.astype(np.float32) if dt == "f32" else synth.to_f16_bits(e)
+            y, _ = orc.gemv(dt, A, x, M, N)
+            assert np.array_equal(y, Av[:, k]), (dt, k)
+    for dt in ("q8", "q4"):
+        q, A, s_val, s_bits = _grouped_quant_case(dt, M, N)
+        expect_w = s_val[:, np.arange(N) // 128] * q
+        assert np.array_equal(orc.dequant(dt, A, s_bits, M, N), expect_w), dt
+        for k in (0, 1, 63, 64, 127, 128, 255, 256, 299):
+            e = np.zeros(N)
+            e[k] = 1.0
+            y, _ = orc.gemv(dt, A, synth.to_f16_bits(e), M, N, scales=s_bits)
+            assert np.array_equal(y, expect_w[:, k]), (dt, k)
+
+
+def pin_int4_byte_table(orc):
+    # one row, hand-built bytes: low nibble = even column, two's complement
+    row = np.array([[0x21, 0x43, 0x8F, 0x7E, 0x09]], dtype=np.uint8)
+    codes = [1, 2, 3, 4, -1, -8, -2, 7, -7, 0]
+    N = 10
+    s = _scales_ones(1, N)
+    W = orc.dequant("q4", row, s, 1, N)
+    assert list(W[0]) == codes
+    for k in range(N):
+        e = np.zeros(N)
+        e[k] = 1.0
+        y, _ = orc.gemv("q4", row, synth.to_f16_bits(e), 1, N, scales=s)
+        assert y[0] == codes[k], k
+
+
+def pin_all_ones(orc):
+    for (M, N) in ((1, 1), (4, 37), (3, 258)):
+        x = synth.integers(13, 2, 0, N, -4, 4).astype(np.float64)
+        total = float(x.sum())
+        ones = np.ones((M, N))
+        y, den = orc.gemv("f32", ones.astype(np.float32), x.astype(np.float32), M, N)
+        assert np.all(y == total) and np.all(den == np.abs(x).sum())
+        xb = synth.to_f16_bits(x)
+        y, _ = orc.gemv("f16", synth.to_f16_bits(ones), xb, M, N)
+        assert np.all(y == total)
+        y, _ = orc.gemv("q8", ones.astype(np.int8), xb, M, N, scales=_scales_ones(M, N))
+        assert np.all(y == total)
+        if N % 2 == 0:
+            y, _ = orc.gemv("q4", synth.pack_int4(ones.astype(np.int64)), xb, M, N,
+                            scales=_scales_ones(M, N))
+            assert np.all(y == total)
+
+
+def _exact_weights(dt, A, s_bits, M, N):
+    """Exact rational weights, decoded independently of the oracle."""
+    W = [[None] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            if dt == "f32":
+                W[i][j] = Fraction(float(A[i, j]))
+            elif dt == "f16":
+                W[i][j] = Fraction(float(np.uint16(A[i, j]).view(np.float16)))
+            else:
+                sc = Fraction(float(np.uint16(s_bits[i, j // 128]).view(np.float16)))
+                if dt == "q8":
+                    code = int(A[i, j])
+                else:
+                    byte = int(A[i, j // 2])
+                    nib = (byte >> (4 * (j % 2))) & 0xF
+                    code = nib - 16 if nib > 7 else nib
+                W[i][j] = sc * code
+    return W
+
+
+def pin_bruteforce_exact(orc):
+    shapes = [(1, 1), (2, 3), (4, 8), (9, 33), (5, 130), (3, 257), (2, 64)]
+    for dt in ("f32", "f16", "q8", "q4"):
+        for (M, N) in shapes:
+            if dt == "q4" and N % 2:
+                continue
+            w = synth.random_case(dt, M, N, 1000 + M * 7 + N)
+            inp = synth.make(w)
+            A, x, s = inp["A"], inp["x"], inp.get("scales")
+            W = _exact_weights(dt, A, s, M, N)
+            xv = [Fraction(float(v)) for v in (x if dt == "f32" else x.view(np.float16))]
+            y, den = orc.gemv(dt, A, x, M, N, scales=s)
+            for i in range(M):
+                ex = sum((W[i][j] * xv[j] for j in range(N)), Fraction(0))
+                ed = sum((abs(W[i][j]) * abs(xv[j]) for j in range(N)), Fraction(0))
+                # double accumulation over N terms: |error| <= N * 2^-53 * den
+                bound = float(ed) * N * 2.0 ** -52
+                assert abs(y[i] - float(ex)) <= bound, (dt, M, N, i)
+                assert abs(den[i] - float(ed)) <= bound, (dt, M, N, i)
+
+
+def pin_counts(orc):
+    M = N = 1024
+    assert orc.flops(M, N) == 2 * M * N - M == 2096128
+    assert orc.bytes("f32", M, N) == 4 * (M * N + N + M) == 4202496
+    g = _golden("published_bandwidth.json")
+    # both printed numbers are rounded (ms to 4 places, GB/s to 1): the byte
+    # count must make the two intervals overlap
+    b = orc.bytes("f16", g["fp16_M"], g["fp16_N"])
+    lo = b / ((g["fp16_ms"] + 0.00005) * 1e-3) / 1e9
+    hi = b / ((g["fp16_ms"] - 0.00005) * 1e-3) / 1e9
+    assert lo <= g["fp16_gbs"] + 0.05 and hi >= g["fp16_gbs"] - 0.05
+    # FP16 : INT4 byte ratio at the decode shape approaches 2 / (0.5 + 2/128)
+    ratio = orc.bytes("f16", 4096, 14336) / orc.bytes("q4", 4096, 14336)
+    assert abs(ratio - g["int4_cap_printed"]) < 0.01
+    assert int(2 / (0.5 + 2 / 128) * 100) / 100 == g["int4_cap_printed"]
+    assert orc.bytes("q8", 4096, 14336) == 4096 * 14336 + 2 * 4096 * 112 + 2 * 14336 + 4 * 4096
+    assert orc.flops(0, 5) == 0 and orc.flops(5, 0) == 0
+
+
+PINS = [pin_dec16_all_patterns, pin_rowmajor_worked_example, pin_identity, pin_unit_vectors,
+        pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts]
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(orc, pin):
+    pin(orc)
+
+
+def test_threads_do_not_change_results(orc):
+    w = synth.random_case("f16", 257, 1000, 77)
+    inp = synth.make(w)
+    y1, d1 = orc.gemv("f16", inp["A"], inp["x"], w.M, w.N, threads=1)
+    y4, d4 = orc.gemv("f16", inp["A"], inp["x"], w.M, w.N, threads=4)
+    assert y1.tobytes() == y4.tobytes() and d1.tobytes() == d4.tobytes()
+
+
+def test_row_subset_matches_full(orc):
+    w = synth.random_case("q4", 50, 260, 78)
+    inp = synth.make(w)
+    y, d = orc.gemv("q4", inp["A"], inp["x"], w.M, w.N, scales=inp["scales"])
+    rows = [49, 0, 17, 17, 3]
+    ys, ds = orc.gemv("q4", inp["A"], inp["x"], w.M, w.N, scales=inp["scales"], rows=rows)
+    assert np.array_equal(ys, y[rows]) and np.array_equal(ds, d[rows])
+
+
+def test_zero_rows_and_empty(orc):
+    A = np.zeros((2, 5), dtype=np.float32)
+    A[1, 2] = 3.0
+    y, d = orc.gemv("f32", A, np.ones(5, dtype=np.float32), 2, 5)
+    assert y[0] == 0.0 and d[0] == 0.0 and y[1] == 3.0
+    y, d = orc.gemv("f32", np.zeros((3, 0), np.float32), np.zeros(0, np.float32), 3, 0)
+    assert np.array_equal(y, np.zeros(3)) and np.array_equal(d, np.zeros(3))
+    y, d = orc.gemv("f16", np.zeros((0, 4), np.uint16), np.zeros(4, np.uint16), 0, 4)
+    assert y.size == 0
+
+
+def test_rejects_bad_arguments(orc):
+    with pytest.raises(ValueError):
+        orc.gemv("q4", np.zeros((1, 2), np.uint8), np.zeros(3, np.uint16), 1, 3,
+                 scales=np.zeros((1, 1), np.uint16))
+    with pytest.raises(ValueError):
+        orc.gemv("f32", np.zeros((2, 2), np.float32), np.zeros(2, np.float32), 2, 2, rows=[2])
+
+
+def test_error_metric():
+    y_ref = np.array([1.0, 0.0, -2.0])
+    den = np.array([2.0, 0.0, 4.0])
+    assert oracle.max_normalised_error([1.0, 0.0, -2.0], y_ref, den) == 0.0
+    assert oracle.max_normalised_error([1.5, 0.0, -2.0], y_ref, den) == 0.25
+    assert oracle.max_normalised_error([1.0, 1e-30, -2.0], y_ref, den) == np.inf
+    assert oracle.max_normalised_error([np.nan, 0.0, -2.0], y_ref, den) == np.inf
+
+
+MUTANTS = {1: "int4 nibble order swapped", 2: "int4 read as offset-8",
+           3: "scale group width 64", 4: "A read column-major",
+           5: "binary16 subnormals decoded as normals", 6: "last column dropped",
+           7: "scale row pitch floor(N/128)"}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[k] for k in sorted(MUTANTS)])
+def test_mutants_are_caught(tmp_path, mutant):
+    bad = oracle.Oracle(oracle.build(mutant, build_dir=str(tmp_path)))
+    assert bad.mutant == mutant
+    failed = []
+    for pin in PINS:
+        try:
+            pin(bad)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches mutant {mutant} ({MUTANTS[mutant]})"
