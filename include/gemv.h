@@ -1,0 +1,181 @@
+/*
+ * gemv.h -- C ABI of the GB300 (sm_103a) GEMV library.
+ *
+ * Computes the row-major matrix-vector product
+ *
+ *     y[i] = sum_{j=0}^{N-1} A[i,j] * x[j],   0 <= i < M,   A[i,j] = A[i*N + j]
+ *
+ * ("Making GEMV Fast", sections "Row-major indexing refresher" and
+ * "Algorithm"; "llama.cpp GEMV CUDA", the kernel-equation paragraph).
+ * Weights may be FP32, FP16, or weight-only quantised INT8 / INT4 with one
+ * FP16 scale per row per 128 contiguous columns ("membound", section "The
+ * kernel decode actually runs: dequant GEMV").  Accumulation and y are FP32.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named A, x, y, scales, W, buf and sink are DEVICE pointers on the
+ *   current CUDA device.  The caller allocates and owns them.  The library
+ *   never allocates device or host memory; its only device state is one
+ *   status word per device, a static variable inside the library.
+ * - FP16 data is passed as IEEE 754 binary16 bit patterns (uint16_t).
+ * - `stream` is a cudaStream_t (CUstream) passed as void*; NULL selects the
+ *   legacy default stream.  Every call only enqueues work and returns: a
+ *   status of GEMV_OK means "validated and launched", not "finished".
+ * - Sizes are element counts (int64_t).  M == 0 is a no-op.  N == 0 writes
+ *   y[0..M) = 0 (A and x may then be NULL).  Negative sizes are rejected.
+ * - Alignment: each pointer must be aligned to its element size, else
+ *   GEMV_ERR_MISALIGNED.  16-byte aligned A and x with a row pitch that is a
+ *   multiple of 16 bytes take the vectorised kernels; any other legal layout
+ *   takes an element-wise kernel that gives the same results more slowly.
+ * - y must not overlap A, x or scales (not checked).
+ * - Errors are returned, never raised: the library does not exit, abort or
+ *   trap.  Launch failures return GEMV_ERR_LAUNCH (gemv_last_cuda_error()
+ *   gives the CUDA code).  A device-side wait that gives up sets the device
+ *   status word, which gemv_get_device_error() reports as GEMV_ERR_TIMEOUT.
+ * - Calls on different streams may run concurrently; the entry points keep
+ *   no per-call host state and are safe to call from several threads.
+ */
+#ifndef MEMORY_BOUND_GEMV_GB300_GEMV_H
+#define MEMORY_BOUND_GEMV_GB300_GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMV_OK = 0,
+    GEMV_ERR_INVALID_VALUE = 1, /* NULL pointer, negative size, bad variant id */
+    GEMV_ERR_MISALIGNED = 2,    /* a pointer not aligned to its element size */
+    GEMV_ERR_UNSUPPORTED = 3,   /* e.g. INT4 with odd N, size beyond the index range */
+    GEMV_ERR_LAUNCH = 4,        /* the CUDA launch failed */
+    GEMV_ERR_TIMEOUT = 5,       /* a device-side wait gave up (see gemv_get_device_error) */
+    GEMV_ERR_CUDA = 6           /* another CUDA runtime call failed */
+} gemv_status_t;
+
+/* Storage types, used by the variant-introspection calls. */
+typedef enum { GEMV_F32 = 0, GEMV_F16 = 1, GEMV_Q8 = 2, GEMV_Q4 = 3 } gemv_dtype_t;
+
+/*
+ * FP32 GEMV.  A: float [M][N] row-major, x: float [N], y: float [M].
+ * "cuda-gemv-optimization", kernel 4 "Warp-level reduction"; "Making GEMV
+ * Fast", section "Turning that access pattern into code".
+ */
+gemv_status_t gemv_f32(const float *A, const float *x, float *y, int64_t M, int64_t N,
+                       void *stream);
+
+/*
+ * FP16 weights and x, FP32 accumulate and output.  A: binary16 [M][N],
+ * x: binary16 [N], y: float [M].
+ * "membound", section "The stages": kernel "vec" (128-bit loads, FP32
+ * accumulation of converted halves); "llama.cpp GEMV CUDA" (FP16 weights and
+ * hidden state, FP32 accumulate and output).
+ */
+gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                       void *stream);
+
+/*
+ * INT8 weight-only GEMV: y[i] = sum_j s[i, j/128] * q[i,j] * x[j].
+ * A: int8 [M][N] (q in [-128, 127]); scales: binary16 [M][ceil(N/128)]
+ * row-major; x: binary16 [N]; y: float [M].  The dequantised weight
+ * FP32(s) * q is exact in FP32.
+ * "membound", section "The kernel decode actually runs: dequant GEMV" (the
+ * page uses one scale per row; a row whose group scales are all equal is that
+ * case).
+ */
+gemv_status_t gemv_q8(const int8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, void *stream);
+
+/*
+ * INT4 weight-only GEMV, same formula as gemv_q8.  A: uint8 [M][N/2]; column
+ * j of a row is byte j/2, low nibble for even j and high nibble for odd j,
+ * read as 4-bit two's complement in [-8, 7].  N must be even, else
+ * GEMV_ERR_UNSUPPORTED.  scales, x, y as for gemv_q8.
+ * "membound", section "The kernel decode actually runs: dequant GEMV"
+ * (two weights per byte, symmetric per-group-of-128 FP16 scales).
+ */
+gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, void *stream);
+
+/*
+ * Pure-read bandwidth probe: streams buf[0..bytes) once with the same
+ * 16-byte read-only loads the GEMV kernels use and folds every word into
+ * *sink with XOR (so no load is dead code).  bytes must be a multiple of 16
+ * and buf 16-byte aligned.  `variant` selects the read pattern
+ * (0 .. gemv_probe_variant_count()-1).  Achieved bytes / time is the
+ * measured read ceiling that memory-bandwidth utilisation is quoted against.
+ * "membound", section "Why GEMV, and why MBU" (pure-read probe as the
+ * denominator for a read-dominated kernel).
+ */
+gemv_status_t gemv_probe_read(const void *buf, size_t bytes, unsigned long long *sink,
+                              int variant, void *stream);
+int gemv_probe_variant_count(void);
+const char *gemv_probe_variant_name(int variant);
+
+/*
+ * Dequantise to FP32: W[i*N + j] = FP32(s[i, j/128]) * q[i,j], using the
+ * same unpacking code as the GEMV kernels.  The product is exact, so W must
+ * equal the oracle's dequantised weights bit for bit.  Test helper:
+ * "membound", section "dequant GEMV" (reference computed on q*s exactly).
+ */
+gemv_status_t gemv_dequant_q8(const int8_t *A, const uint16_t *scales, float *W, int64_t M,
+                              int64_t N, void *stream);
+gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W, int64_t M,
+                              int64_t N, void *stream);
+
+/*
+ * Kernel variants.  Every dtype has a table of compiled variants (kernel
+ * family, threads per row, loads in flight, warps per block, how x is
+ * staged).  The plain entry points pick one by shape; these calls run a
+ * chosen one so that each can be checked and timed.  A variant that cannot
+ * serve the given shape or alignment returns GEMV_ERR_UNSUPPORTED.
+ *
+ * Families: 0 = rows of a warp (or of a fraction of one) streamed with a
+ * rolling buffer of loads; 1 = row tiles: a group of threads requests a whole
+ * row at once and a persistent grid walks consecutive rows in order;
+ * 2 = element-wise kernel for layouts without 16-byte alignment.
+ */
+typedef struct {
+    int dtype;           /* gemv_dtype_t */
+    int kind;            /* kernel family, see above */
+    int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1) */
+    int rows_per_group;  /* rows one lane group streams together (family 0, x reuse) */
+    int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread */
+    int warps;           /* warps per block */
+    int xmode;          /* 0: x copied to shared memory by a bulk async copy,
+                           1: x copied to shared memory by vector loads,
+                           2: x read through the L1 cache, 3: element-wise kernel */
+    char name[48];
+} gemv_variant_info_t;
+
+int gemv_variant_count(int dtype);
+gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *info);
+/* Variant the plain entry point would use for these arguments (-1 on bad args). */
+int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N);
+gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,
+                               int64_t M, int64_t N, const uint16_t *scales, void *stream);
+
+/*
+ * Synchronises `stream`, reads and clears this device's status word.
+ * Returns GEMV_ERR_TIMEOUT if any kernel gave up a bounded wait since the
+ * last call, GEMV_OK otherwise (GEMV_ERR_CUDA if the CUDA calls fail).
+ */
+gemv_status_t gemv_get_device_error(void *stream);
+
+/* Test hooks.  Limit of every device-side wait in nanoseconds (default one
+ * second), and a switch that makes the next launches skip the bulk copy of x
+ * so that their wait runs out (nothing is copied, nothing faults). */
+void gemv_debug_set_wait_limit_ns(uint64_t ns);
+void gemv_debug_skip_x_copy(int on);
+
+const char *gemv_status_string(gemv_status_t status);
+int gemv_last_cuda_error(void); /* last cudaError_t seen by this thread, 0 if none */
+const char *gemv_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

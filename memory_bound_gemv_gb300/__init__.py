@@ -1,0 +1,310 @@
+"""Python binding of the GB300 GEMV library (``include/gemv.h``).
+
+Argument marshalling only: every call checks tensor dtypes, shapes, devices
+and contiguity, then passes raw device pointers, sizes and the current CUDA
+stream to the C ABI of ``_build/libmbgemv.so``.  All arithmetic runs in that
+library's CUDA kernels.  There is no CPU fallback: if the library cannot be
+built or loaded, every call raises.
+
+Function names match the C entry points: ``gemv_f32``, ``gemv_f16``,
+``gemv_q8``, ``gemv_q4``, ``gemv_probe_read``, ``gemv_dequant_q8``,
+``gemv_dequant_q4``, ``gemv_run_variant`` ...  ``lib()`` returns the raw
+ctypes handle for callers that want to pass pointers themselves.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional
+
+F32, F16, Q8, Q4 = 0, 1, 2, 3
+DTYPES = {"f32": F32, "f16": F16, "q8": Q8, "q4": Q4}
+GROUP = 128
+
+STATUS = {0: "GEMV_OK", 1: "GEMV_ERR_INVALID_VALUE", 2: "GEMV_ERR_MISALIGNED",
+          3: "GEMV_ERR_UNSUPPORTED", 4: "GEMV_ERR_LAUNCH", 5: "GEMV_ERR_TIMEOUT",
+          6: "GEMV_ERR_CUDA"}
+OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_CUDA = range(7)
+
+XMODES = {0: "bulk", 1: "vec", 2: "l1", 3: "elem"}
+
+
+class GemvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+KINDS = {0: "vec", 1: "tile", 2: "elem"}
+
+
+class VariantInfo(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("kind", ctypes.c_int), ("threads_per_row", ctypes.c_int),
+                ("rows_per_group", ctypes.c_int), ("unroll", ctypes.c_int),
+                ("warps", ctypes.c_int), ("xmode", ctypes.c_int), ("name", ctypes.c_char * 48)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(L):
+    i64, vp, i32, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+    sig = {
+        "gemv_f32": [vp, vp, vp, i64, i64, vp],
+        "gemv_f16": [vp, vp, vp, i64, i64, vp],
+        "gemv_q8": [vp, vp, vp, i64, i64, vp, vp],
+        "gemv_q4": [vp, vp, vp, i64, i64, vp, vp],
+        "gemv_probe_read": [vp, ctypes.c_size_t, vp, i32, vp],
+        "gemv_dequant_q8": [vp, vp, vp, i64, i64, vp],
+        "gemv_dequant_q4": [vp, vp, vp, i64, i64, vp],
+        "gemv_variant_info": [i32, i32, ctypes.POINTER(VariantInfo)],
+        "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
+        "gemv_get_device_error": [vp],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = st
+    L.gemv_probe_variant_count.argtypes = []
+    L.gemv_probe_variant_count.restype = i32
+    L.gemv_probe_variant_name.argtypes = [i32]
+    L.gemv_probe_variant_name.restype = ctypes.c_char_p
+    L.gemv_variant_count.argtypes = [i32]
+    L.gemv_variant_count.restype = i32
+    L.gemv_select_variant.argtypes = [i32, vp, vp, i64, i64]
+    L.gemv_select_variant.restype = i32
+    L.gemv_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.gemv_debug_set_wait_limit_ns.restype = None
+    L.gemv_debug_skip_x_copy.argtypes = [i32]
+    L.gemv_debug_skip_x_copy.restype = None
+    L.gemv_status_string.argtypes = [st]
+    L.gemv_status_string.restype = ctypes.c_char_p
+    L.gemv_last_cuda_error.argtypes = []
+    L.gemv_last_cuda_error.restype = i32
+    L.gemv_build_info.argtypes = []
+    L.gemv_build_info.restype = ctypes.c_char_p
+    return L
+
+
+def library_path() -> str:
+    from . import build as _b
+    return _b.LIB
+
+
+def lib(build_if_stale: bool = True):
+    """The ctypes handle of libmbgemv.so (built in-tree on first use if stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _b
+            path = _b.LIB
+            if build_if_stale and not _b.up_to_date():
+                path = _b.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library missing: {path} (run memory_bound_gemv_gb300.build)")
+            _lib = _declare(ctypes.CDLL(path))
+        return _lib
+
+
+# ---------------------------------------------------------------------------
+# tensor marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(t, name, dtypes, shape, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must live on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(status, what):
+    if status != OK:
+        raise GemvError(status, what)
+
+
+def _f16_types():
+    torch = _torch()
+    return (torch.float16, torch.int16, torch.uint16)
+
+
+def _out(y, M, device):
+    torch = _torch()
+    if y is None:
+        return torch.empty(M, dtype=torch.float32, device=device)
+    _check(y, "y", (torch.float32,), (M,), device)
+    return y
+
+
+def _mn(A, dtype):
+    if A.dim() != 2:
+        raise ValueError("A must be 2-D")
+    M, W = A.shape
+    return M, (2 * W if dtype == Q4 else W)
+
+
+def gemv_f32(A, x, y=None, stream=None):
+    """y = A x with FP32 A [M, N] and x [N]; returns y (float32 [M])."""
+    torch = _torch()
+    M, N = _mn(A, F32)
+    _check(A, "A", (torch.float32,), (M, N))
+    _check(x, "x", (torch.float32,), (N,), A.device)
+    y = _out(y, M, A.device)
+    _raise(lib().gemv_f32(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, _stream_ptr(stream)), "gemv_f32")
+    return y
+
+
+def gemv_f16(A, x, y=None, stream=None):
+    """y = A x with FP16 A [M, N] and x [N], FP32 accumulation and output."""
+    M, N = _mn(A, F16)
+    _check(A, "A", _f16_types(), (M, N))
+    _check(x, "x", _f16_types(), (N,), A.device)
+    y = _out(y, M, A.device)
+    _raise(lib().gemv_f16(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, _stream_ptr(stream)), "gemv_f16")
+    return y
+
+
+def _quant(fn_name, dtype, A, x, scales, y, stream):
+    torch = _torch()
+    M, N = _mn(A, dtype)
+    _check(A, "A", (torch.int8,) if dtype == Q8 else (torch.uint8,), tuple(A.shape))
+    _check(x, "x", _f16_types(), (N,), A.device)
+    _check(scales, "scales", _f16_types(), (M, (N + GROUP - 1) // GROUP), A.device)
+    y = _out(y, M, A.device)
+    fn = getattr(lib(), fn_name)
+    _raise(fn(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, scales.data_ptr(), _stream_ptr(stream)), fn_name)
+    return y
+
+
+def gemv_q8(A, x, scales, y=None, stream=None):
+    """INT8 weights A [M, N], FP16 scales [M, ceil(N/128)], FP16 x [N]."""
+    return _quant("gemv_q8", Q8, A, x, scales, y, stream)
+
+
+def gemv_q4(A, x, scales, y=None, stream=None):
+    """Packed INT4 weights A uint8 [M, N/2] (low nibble = even column)."""
+    return _quant("gemv_q4", Q4, A, x, scales, y, stream)
+
+
+def gemv(dtype: str, A, x, scales=None, y=None, stream=None):
+    """Dispatch on the storage type name: 'f32', 'f16', 'q8', 'q4'."""
+    if dtype == "f32":
+        return gemv_f32(A, x, y, stream)
+    if dtype == "f16":
+        return gemv_f16(A, x, y, stream)
+    if dtype == "q8":
+        return gemv_q8(A, x, scales, y, stream)
+    if dtype == "q4":
+        return gemv_q4(A, x, scales, y, stream)
+    raise ValueError(dtype)
+
+
+def gemv_run_variant(dtype: str, variant: int, A, x, scales=None, y=None, stream=None):
+    """Run one compiled kernel variant (see ``variants``) on tensors."""
+    torch = _torch()
+    dt = DTYPES[dtype]
+    M, N = _mn(A, dt)
+    y = _out(y, M, A.device)
+    s_ptr = scales.data_ptr() if scales is not None else None
+    _raise(lib().gemv_run_variant(dt, variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                  s_ptr, _stream_ptr(stream)), f"gemv_run_variant({dtype}, {variant})")
+    del torch
+    return y
+
+
+def variants(dtype: str) -> List[dict]:
+    L = lib()
+    dt = DTYPES[dtype]
+    out = []
+    for k in range(L.gemv_variant_count(dt)):
+        info = VariantInfo()
+        _raise(L.gemv_variant_info(dt, k, ctypes.byref(info)), "gemv_variant_info")
+        out.append({"id": k, "name": info.name.decode(), "kind": KINDS[info.kind],
+                    "threads_per_row": info.threads_per_row,
+                    "rows_per_group": info.rows_per_group, "unroll": info.unroll,
+                    "warps": info.warps, "xmode": XMODES[info.xmode]})
+    return out
+
+
+def select_variant(dtype: str, A, x) -> int:
+    dt = DTYPES[dtype]
+    M, N = _mn(A, dt)
+    return lib().gemv_select_variant(dt, A.data_ptr(), x.data_ptr(), M, N)
+
+
+def gemv_dequant_q8(A, scales, W=None, stream=None):
+    torch = _torch()
+    M, N = _mn(A, Q8)
+    if W is None:
+        W = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _raise(lib().gemv_dequant_q8(A.data_ptr(), scales.data_ptr(), W.data_ptr(), M, N,
+                                 _stream_ptr(stream)), "gemv_dequant_q8")
+    return W
+
+
+def gemv_dequant_q4(A, scales, W=None, stream=None):
+    torch = _torch()
+    M, N = _mn(A, Q4)
+    if W is None:
+        W = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _raise(lib().gemv_dequant_q4(A.data_ptr(), scales.data_ptr(), W.data_ptr(), M, N,
+                                 _stream_ptr(stream)), "gemv_dequant_q4")
+    return W
+
+
+def probe_variants() -> List[str]:
+    L = lib()
+    return [L.gemv_probe_variant_name(k).decode() for k in range(L.gemv_probe_variant_count())]
+
+
+def gemv_probe_read(buf, sink, variant: int = 0, stream=None):
+    """Stream ``buf`` (any dtype, contiguous, 16-byte multiple) once; XOR into sink (int64 [1])."""
+    nbytes = buf.numel() * buf.element_size()
+    _raise(lib().gemv_probe_read(buf.data_ptr(), nbytes, sink.data_ptr(), variant, _stream_ptr(stream)),
+           "gemv_probe_read")
+
+
+def gemv_get_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status (OK or ERR_TIMEOUT)."""
+    return lib().gemv_get_device_error(_stream_ptr(stream))
+
+
+def debug_set_wait_limit_ns(ns: int):
+    lib().gemv_debug_set_wait_limit_ns(ns)
+
+
+def debug_skip_x_copy(on: bool):
+    lib().gemv_debug_skip_x_copy(1 if on else 0)
+
+
+def status_string(status: int) -> str:
+    return lib().gemv_status_string(status).decode()
+
+
+def build_info() -> str:
+    return lib().gemv_build_info().decode()

@@ -1,0 +1,469 @@
+// C-ABI entry points (include/gemv.h): argument validation, variant choice,
+// per-device set-up and error reporting.  All device work is in the kernels
+// of the other translation units; this file launches them and never
+// allocates memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <climits>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/gemv.h"
+#include "gemv_internal.h"
+
+#define MBG_STR2(v) #v
+#define MBG_STR(v) MBG_STR2(v)
+
+namespace mbg {
+namespace {
+
+// The device status word (bit DEVERR_TIMEOUT: a bounded wait gave up).  A
+// static device variable, so the library needs no allocation for it.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+// Largest x kept in shared memory by the automatic choice; longer x is read
+// through L1 so that several blocks still fit on an SM.
+constexpr int64_t kAutoSmemX = 64 * 1024;
+// Widest row group and chunks per thread of the compiled tile kernels.
+constexpr int kTileMaxThreads = 512;
+constexpr int kTileChunks = 8;
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    unsigned int *status = nullptr;  // device address of g_device_status
+    int sm_count = 0;
+    int max_smem = 0;                // opt-in dynamic shared memory per block
+    // resident blocks per SM of a tile variant, keyed by (dtype, variant, smem bytes)
+    std::mutex occ_mutex;
+    std::map<std::tuple<int, int, size_t>, int> occ;
+};
+DeviceState g_devices[kMaxDevices];
+
+std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
+std::atomic<int> g_skip_x_copy{0};
+thread_local int t_last_cuda_error = 0;
+
+gemv_status_t cuda_fail(cudaError_t e, gemv_status_t code)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return code;
+}
+
+const Variant *table(int dtype, int *count)
+{
+    switch (dtype) {
+    case DT_F32: return variants_f32(count);
+    case DT_F16: return variants_f16(count);
+    case DT_Q8: return variants_q8(count);
+    case DT_Q4: return variants_q4(count);
+    default: *count = 0; return nullptr;
+    }
+}
+
+void init_device(DeviceState &d, int dev)
+{
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    for (int dt = 0; e == cudaSuccess && dt < DT_COUNT; ++dt) {
+        int n = 0;
+        const Variant *v = table(dt, &n);
+        for (int k = 0; e == cudaSuccess && k < n; ++k) e = v[k].set_smem_limit(d.max_smem);
+    }
+    d.init_error = e;
+}
+
+// Set-up of the current device on its first use (symbol address of the status
+// word, SM count, shared-memory limits).  Returns nullptr on failure.
+DeviceState *current_device()
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceState &d = g_devices[dev];
+    std::call_once(d.once, init_device, std::ref(d), dev);
+    if (d.init_error != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(d.init_error);
+        return nullptr;
+    }
+    return &d;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t row_bytes_of(int dtype, int64_t N)
+{
+    switch (dtype) {
+    case DT_F32: return 4 * N;
+    case DT_F16: return 2 * N;
+    case DT_Q8: return N;
+    default: return N / 2;
+    }
+}
+
+int a_align(int dtype) { return dtype == DT_F32 ? 4 : dtype == DT_F16 ? 2 : 1; }
+int x_align(int dtype) { return dtype == DT_F32 ? 4 : 2; }
+int x_elem_bytes(int dtype) { return dtype == DT_F32 ? 4 : 2; }
+
+// Common argument checks.  Returns GEMV_OK when the call may proceed.
+gemv_status_t validate(int dtype, const void *A, const void *x, const float *y, int64_t M,
+                       int64_t N, const uint16_t *scales)
+{
+    if (dtype < 0 || dtype >= DT_COUNT) return GEMV_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0) return GEMV_ERR_INVALID_VALUE;
+    if (M == 0) return GEMV_OK;
+    if (!y) return GEMV_ERR_INVALID_VALUE;
+    if (!aligned(y, 4)) return GEMV_ERR_MISALIGNED;
+    if (N == 0) return GEMV_OK;
+    if (!A || !x) return GEMV_ERR_INVALID_VALUE;
+    const bool quant = dtype == DT_Q8 || dtype == DT_Q4;
+    if (quant && !scales) return GEMV_ERR_INVALID_VALUE;
+    if (dtype == DT_Q4 && (N % 2)) return GEMV_ERR_UNSUPPORTED;
+    if (!aligned(A, a_align(dtype)) || !aligned(x, x_align(dtype))) return GEMV_ERR_MISALIGNED;
+    if (quant && !aligned(scales, 2)) return GEMV_ERR_MISALIGNED;
+    // index range: byte offsets of A must fit in int64
+    if (M > INT64_MAX / (row_bytes_of(dtype, N) > 0 ? row_bytes_of(dtype, N) : 1))
+        return GEMV_ERR_UNSUPPORTED;
+    return GEMV_OK;
+}
+
+// Dynamic shared memory of variant v for a row of N columns.
+size_t smem_bytes(const Variant &v, int dtype, int64_t N)
+{
+    if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)
+        return static_cast<size_t>(v.x_offset) + static_cast<size_t>(N) * x_elem_bytes(dtype);
+    if (v.kind == KIND_TILE) return static_cast<size_t>(v.x_offset);
+    return 0;
+}
+
+// Can variant v serve this call?
+bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void *A, const void *x,
+                  int64_t M, int64_t N)
+{
+    if (v.xmode == XMODE_ELEM) {
+        const int64_t blocks = (M + v.warps - 1) / v.warps;
+        return blocks <= INT_MAX;
+    }
+    const int64_t rb = row_bytes_of(dtype, N);
+    if (rb % 16 || !aligned(A, 16) || !aligned(x, 16)) return false;
+    if (rb / 16 > INT_MAX / 64) return false;
+    if (static_cast<int64_t>(smem_bytes(v, dtype, N)) > d.max_smem) return false;
+    if (v.kind == KIND_TILE) {
+        // every row must be covered by one request per thread
+        if (rb / 16 > static_cast<int64_t>(v.lanes_per_row) * v.unroll) return false;
+        return true;  // persistent grid: the block count never exceeds the SM slots
+    }
+    const int64_t blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
+    return blocks <= INT_MAX;
+}
+
+// Blocks of a tile variant that fit on the GPU at once (0 on failure).
+int resident_blocks(DeviceState &d, int dtype, int vid, const Variant &v, size_t smem)
+{
+    const auto key = std::make_tuple(dtype, vid, smem);
+    {
+        std::lock_guard<std::mutex> g(d.occ_mutex);
+        auto it = d.occ.find(key);
+        if (it != d.occ.end()) return it->second;
+    }
+    int per_sm = 0;
+    const cudaError_t e = v.occupancy(&per_sm, smem);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return 0;
+    }
+    const int total = per_sm * d.sm_count;
+    std::lock_guard<std::mutex> g(d.occ_mutex);
+    d.occ[key] = total;
+    return total;
+}
+
+int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps = 0)
+{
+    int n = 0;
+    const Variant *v = table(dtype, &n);
+    for (int k = 0; k < n; ++k)
+        if (v[k].lanes_per_row == lpr && v[k].xmode == xmode && v[k].kind == kind &&
+            (warps == 0 || v[k].warps == warps))
+            return k;
+    return -1;
+}
+
+// The automatic choice: element-wise kernel for layouts the vector kernels
+// cannot take; otherwise lanes per row from the row length (a row shorter
+// than one warp-wide pass of 512 bytes shares its warp with other rows) and
+// x in shared memory unless it is long.
+int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x, int64_t M,
+                   int64_t N)
+{
+    int n = 0;
+    const Variant *v = table(dtype, &n);
+    const int64_t rb = row_bytes_of(dtype, N);
+    const bool vec_ok = rb % 16 == 0 && aligned(A, 16) && aligned(x, 16);
+    if (!vec_ok) return find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
+    const int64_t chunks = rb / 16;
+    const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
+    // Row tiles: the narrowest group that requests a whole row at once.
+    if (small_x && chunks <= static_cast<int64_t>(kTileMaxThreads) * kTileChunks) {
+        int g = 1;
+        while (static_cast<int64_t>(g) * kTileChunks < chunks) g *= 2;
+        const int warps = g > 256 ? g / 32 : 8;
+        const int k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);
+        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N)) return k;
+    }
+    // Long rows or long x: warp per row with a rolling buffer, x through L1.
+    int k = small_x ? find_variant(dtype, 32, XMODE_BULK) : find_variant(dtype, 32, XMODE_L1);
+    if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N))
+        k = find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
+    return k;
+}
+
+gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, int64_t M, int64_t N,
+                  const uint16_t *scales, void *stream)
+{
+    gemv_status_t st = validate(dtype, A, x, y, M, N, scales);
+    if (st != GEMV_OK) return st;
+    int n = 0;
+    const Variant *tab = table(dtype, &n);
+    if (vid >= n) return GEMV_ERR_INVALID_VALUE;
+    if (M == 0) return GEMV_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        launch_fill_zero(y, M, s);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+    }
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    if (vid < 0) {
+        vid = choose_variant(*d, dtype, A, x, M, N);
+        if (vid < 0) return GEMV_ERR_UNSUPPORTED;
+    }
+    const Variant &v = tab[vid];
+    if (!variant_fits(v, *d, dtype, A, x, M, N)) return GEMV_ERR_UNSUPPORTED;
+
+    GemvArgs a{};
+    a.A = A;
+    a.x = x;
+    a.y = y;
+    a.scales = scales;
+    a.M = M;
+    a.N = N;
+    a.row_bytes = row_bytes_of(dtype, N);
+    a.groups = (N + kGroup - 1) / kGroup;
+    a.nchunks = static_cast<int>(a.row_bytes / 16);
+    a.err = d->status;
+    a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    a.skip_x_copy = g_skip_x_copy.load(std::memory_order_relaxed);
+
+    int64_t blocks;
+    const size_t smem = smem_bytes(v, dtype, N);
+    if (v.xmode == XMODE_ELEM) {
+        blocks = (M + v.warps - 1) / v.warps;
+    } else {
+        blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
+        if (v.kind == KIND_TILE) {
+            const int resident = resident_blocks(*d, dtype, vid, v, smem);
+            if (resident <= 0) return GEMV_ERR_CUDA;
+            if (blocks > resident) blocks = resident;
+        }
+    }
+    v.launch(a, static_cast<unsigned>(blocks), smem, s);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+}  // namespace
+}  // namespace mbg
+
+using namespace mbg;
+
+extern "C" {
+
+gemv_status_t gemv_f32(const float *A, const float *x, float *y, int64_t M, int64_t N, void *stream)
+{
+    return run(DT_F32, -1, A, x, y, M, N, nullptr, stream);
+}
+
+gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                       void *stream)
+{
+    return run(DT_F16, -1, A, x, y, M, N, nullptr, stream);
+}
+
+gemv_status_t gemv_q8(const int8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, void *stream)
+{
+    return run(DT_Q8, -1, A, x, y, M, N, scales, stream);
+}
+
+gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, void *stream)
+{
+    return run(DT_Q4, -1, A, x, y, M, N, scales, stream);
+}
+
+int gemv_variant_count(int dtype)
+{
+    int n = 0;
+    table(dtype, &n);
+    return n;
+}
+
+gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *info)
+{
+    int n = 0;
+    const Variant *v = table(dtype, &n);
+    if (!info || variant < 0 || variant >= n) return GEMV_ERR_INVALID_VALUE;
+    const Variant &w = v[variant];
+    info->dtype = w.dtype;
+    info->kind = w.kind;
+    info->threads_per_row = w.lanes_per_row;
+    info->rows_per_group = w.rows_per_group;
+    info->unroll = w.unroll;
+    info->warps = w.warps;
+    info->xmode = w.xmode;
+    snprintf(info->name, sizeof(info->name), "%s", w.name);
+    return GEMV_OK;
+}
+
+int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N)
+{
+    if (dtype < 0 || dtype >= DT_COUNT || M <= 0 || N <= 0 || !A || !x) return -1;
+    if (dtype == DT_Q4 && (N % 2)) return -1;
+    if (!aligned(A, a_align(dtype)) || !aligned(x, x_align(dtype))) return -1;
+    DeviceState *d = current_device();
+    if (!d) return -1;
+    return choose_variant(*d, dtype, A, x, M, N);
+}
+
+gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,
+                               int64_t M, int64_t N, const uint16_t *scales, void *stream)
+{
+    if (variant < 0) return GEMV_ERR_INVALID_VALUE;
+    return run(dtype, variant, A, x, y, M, N, scales, stream);
+}
+
+gemv_status_t gemv_probe_read(const void *buf, size_t bytes, unsigned long long *sink, int variant,
+                              void *stream)
+{
+    int n = 0;
+    const ProbeVariant *pv = probe_variants(&n);
+    if (variant < 0 || variant >= n || !sink) return GEMV_ERR_INVALID_VALUE;
+    if (bytes == 0) return GEMV_OK;
+    if (!buf) return GEMV_ERR_INVALID_VALUE;
+    if (bytes % 16 || !aligned(buf, 16) || !aligned(sink, 8)) return GEMV_ERR_MISALIGNED;
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    const ProbeVariant &p = pv[variant];
+    const unsigned grid = static_cast<unsigned>(d->sm_count * p.blocks_per_sm);
+    p.launch(buf, bytes / 16, sink, grid, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+int gemv_probe_variant_count(void)
+{
+    int n = 0;
+    probe_variants(&n);
+    return n;
+}
+
+const char *gemv_probe_variant_name(int variant)
+{
+    int n = 0;
+    const ProbeVariant *pv = probe_variants(&n);
+    return (variant >= 0 && variant < n) ? pv[variant].name : nullptr;
+}
+
+static gemv_status_t dequant(int dtype, const void *A, const uint16_t *scales, float *W, int64_t M,
+                             int64_t N, void *stream)
+{
+    if (M < 0 || N < 0) return GEMV_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMV_OK;
+    if (!A || !scales || !W) return GEMV_ERR_INVALID_VALUE;
+    if (dtype == DT_Q4 && (N % 2)) return GEMV_ERR_UNSUPPORTED;
+    if (!aligned(scales, 2) || !aligned(W, 4)) return GEMV_ERR_MISALIGNED;
+    if (M > INT64_MAX / N) return GEMV_ERR_UNSUPPORTED;
+    const int64_t rb = row_bytes_of(dtype, N);
+    const bool vec = rb % 16 == 0 && aligned(A, 16);
+    launch_dequant(dtype, A, scales, W, M, N, vec, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+gemv_status_t gemv_dequant_q8(const int8_t *A, const uint16_t *scales, float *W, int64_t M,
+                              int64_t N, void *stream)
+{
+    return dequant(DT_Q8, A, scales, W, M, N, stream);
+}
+
+gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W, int64_t M,
+                              int64_t N, void *stream)
+{
+    return dequant(DT_Q4, A, scales, W, M, N, stream);
+}
+
+gemv_status_t gemv_get_device_error(void *stream)
+{
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_CUDA);
+    unsigned int word = 0;
+    e = cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_CUDA);
+    if (word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_CUDA);
+    }
+    return (word & DEVERR_TIMEOUT) ? GEMV_ERR_TIMEOUT : GEMV_OK;
+}
+
+void gemv_debug_set_wait_limit_ns(uint64_t ns)
+{
+    // 0 restores the default; anything shorter than 100 us is raised to it so
+    // that a copy that was issued always has time to land before its block
+    // exits.
+    if (ns == 0) ns = 1000000000ull;
+    if (ns < 100000ull) ns = 100000ull;
+    g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+}
+
+void gemv_debug_skip_x_copy(int on) { g_skip_x_copy.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+const char *gemv_status_string(gemv_status_t status)
+{
+    switch (status) {
+    case GEMV_OK: return "GEMV_OK";
+    case GEMV_ERR_INVALID_VALUE: return "GEMV_ERR_INVALID_VALUE";
+    case GEMV_ERR_MISALIGNED: return "GEMV_ERR_MISALIGNED";
+    case GEMV_ERR_UNSUPPORTED: return "GEMV_ERR_UNSUPPORTED";
+    case GEMV_ERR_LAUNCH: return "GEMV_ERR_LAUNCH";
+    case GEMV_ERR_TIMEOUT: return "GEMV_ERR_TIMEOUT";
+    case GEMV_ERR_CUDA: return "GEMV_ERR_CUDA";
+    default: return "GEMV_ERR_UNKNOWN";
+    }
+}
+
+int gemv_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *gemv_build_info(void)
+{
+    return "memory_bound_gemv_gb300: sm_103a, CUDA " MBG_STR(CUDART_VERSION);
+}
+
+}  // extern "C"

@@ -1,0 +1,274 @@
+// Device-side building blocks of the GEMV kernels (sm_103a).
+//
+// Streaming loads of A, bounded mbarrier waits for the bulk copy of x,
+// in-register unpacking of INT8 / INT4 codes and the FP32 dot-product
+// accumulation.  The kernels themselves are in gemv_kernels.cuh.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemv_internal.h"
+
+namespace mbg {
+
+// ---------------------------------------------------------------------------
+// Global memory
+// ---------------------------------------------------------------------------
+
+// 16-byte read-only load that bypasses L1 and asks L2 to fetch the whole
+// 256-byte block: A is read exactly once, so it should not evict x or the
+// scales from L1.  ("membound", kernel "vec": one 128-bit load per lane per
+// step, so a warp reads 512 contiguous bytes.)
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// 16-byte read-only load that may allocate in L1 (x, when it is not staged).
+__device__ __forceinline__ uint4 ld_cached16(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_half_as_float(const uint16_t *p)
+{
+    const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p));
+    return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report_error(unsigned int *err, unsigned int code)
+{
+    if (err) atomicOr(err, code);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (x staging)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy global -> shared that signals `bar` with its byte count.
+// Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Waits for phase `parity` of `bar` to complete, giving up after limit_ns.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity), "r"(2000u)
+            : "memory");
+        if (done) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Unpacking quantised codes (exact)
+// ---------------------------------------------------------------------------
+
+// Four int8 codes of a 32-bit word -> four floats, exactly.  Flipping the
+// sign bit turns code b into the unsigned byte b + 128; placing that byte in
+// the low mantissa bits of 2^23 (bit pattern 0x4B0000uu) gives the float
+// 2^23 + b + 128, and subtracting 2^23 + 128 leaves b.
+__device__ __forceinline__ void unpack_q8_word(uint32_t w, float (&f)[4])
+{
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.0f;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.0f;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.0f;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.0f;
+}
+
+// Eight int4 codes of a 32-bit word (nibble k = column k of the word: the
+// low nibble of each byte is the even column) -> eight floats, exactly.
+// XOR with 8 per nibble maps the two's-complement code q to q + 8 in [0, 15];
+// OR-ing that into the mantissa of 2^23 and subtracting 2^23 + 8 leaves q.
+__device__ __forceinline__ void unpack_q4_word(uint32_t w, float (&f)[8])
+{
+    const uint32_t u = w ^ 0x88888888u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        f[k] = __uint_as_float(0x4B000000u | ((u >> (4 * k)) & 0xFu)) - 8388616.0f;
+}
+
+// Two binary16 values packed in a 32-bit word (low half first) -> two floats.
+__device__ __forceinline__ void half2_bits_to_float(uint32_t w, float &lo, float &hi)
+{
+    asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
+// ---------------------------------------------------------------------------
+// Storage formats
+// ---------------------------------------------------------------------------
+
+template <int DT> struct Fmt;
+
+template <> struct Fmt<DT_F32> {
+    static constexpr int EPC = 4;   // elements per 16-byte chunk of A
+    static constexpr int XB = 4;    // bytes per element of x
+    static constexpr bool QUANT = false;
+};
+template <> struct Fmt<DT_F16> {
+    static constexpr int EPC = 8;
+    static constexpr int XB = 2;
+    static constexpr bool QUANT = false;
+};
+template <> struct Fmt<DT_Q8> {
+    static constexpr int EPC = 16;
+    static constexpr int XB = 2;
+    static constexpr bool QUANT = true;
+};
+template <> struct Fmt<DT_Q4> {
+    static constexpr int EPC = 32;
+    static constexpr int XB = 2;
+    static constexpr bool QUANT = true;
+};
+
+// Bytes of x that one 16-byte chunk of A multiplies.
+template <int DT> constexpr int x_chunk_bytes() { return Fmt<DT>::EPC * Fmt<DT>::XB; }
+template <int DT> constexpr int x_chunk_vecs() { return x_chunk_bytes<DT>() / 16; }
+
+// x chunk (as raw 16-byte vectors) -> floats.
+template <int DT>
+__device__ __forceinline__ void x_to_float(const uint4 (&xv)[x_chunk_vecs<DT>()],
+                                           float (&xf)[Fmt<DT>::EPC])
+{
+    if constexpr (DT == DT_F32) {
+        xf[0] = __uint_as_float(xv[0].x);
+        xf[1] = __uint_as_float(xv[0].y);
+        xf[2] = __uint_as_float(xv[0].z);
+        xf[3] = __uint_as_float(xv[0].w);
+    } else {
+#pragma unroll
+        for (int v = 0; v < x_chunk_vecs<DT>(); ++v) {
+            half2_bits_to_float(xv[v].x, xf[v * 8 + 0], xf[v * 8 + 1]);
+            half2_bits_to_float(xv[v].y, xf[v * 8 + 2], xf[v * 8 + 3]);
+            half2_bits_to_float(xv[v].z, xf[v * 8 + 4], xf[v * 8 + 5]);
+            half2_bits_to_float(xv[v].w, xf[v * 8 + 6], xf[v * 8 + 7]);
+        }
+    }
+}
+
+// One 16-byte chunk of A -> its EPC weights (codes for the quantised types).
+template <int DT>
+__device__ __forceinline__ void chunk_to_float(const uint4 a, float (&wf)[Fmt<DT>::EPC])
+{
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    if constexpr (DT == DT_F32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) wf[k] = __uint_as_float(w[k]);
+    } else if constexpr (DT == DT_F16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) half2_bits_to_float(w[k], wf[2 * k], wf[2 * k + 1]);
+    } else if constexpr (DT == DT_Q8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float f[4];
+            unpack_q8_word(w[k], f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wf[4 * k + e] = f[e];
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float f[8];
+            unpack_q4_word(w[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wf[8 * k + e] = f[e];
+        }
+    }
+}
+
+// Number of FP32 accumulators per row and lane.  Each 16-byte chunk feeds
+// its elements round-robin into them, so the dependent-add chain of one
+// accumulator is (elements per lane) / NACC long; four keep the FP32 chain at
+// N/128 for a full warp per row.
+constexpr int NACC = 4;
+
+// acc[e % NACC] += w[e] * x[e] over one chunk (unquantised), or
+// acc[e % NACC] += s * (sum of the chunk's code * x) (quantised: the scale is
+// constant over a chunk because 128 is a multiple of the chunk's width).
+template <int DT>
+__device__ __forceinline__ void chunk_fma(const float (&wf)[Fmt<DT>::EPC],
+                                          const float (&xf)[Fmt<DT>::EPC], float scale,
+                                          float (&acc)[NACC])
+{
+    if constexpr (!Fmt<DT>::QUANT) {
+        (void)scale;
+#pragma unroll
+        for (int e = 0; e < Fmt<DT>::EPC; ++e) acc[e % NACC] = fmaf(wf[e], xf[e], acc[e % NACC]);
+    } else {
+        float p[NACC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < Fmt<DT>::EPC; ++e) p[e % NACC] = fmaf(wf[e], xf[e], p[e % NACC]);
+#pragma unroll
+        for (int k = 0; k < NACC; ++k) acc[k] = fmaf(scale, p[k], acc[k]);
+    }
+}
+
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float v)
+{
+    // XOR butterfly inside aligned groups of WIDTH lanes: every lane of the
+    // group ends with the group's sum ("llama.cpp GEMV CUDA", warp_reduce_sum
+    // with __shfl_xor_sync).
+#pragma unroll
+    for (int off = WIDTH / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+}  // namespace mbg

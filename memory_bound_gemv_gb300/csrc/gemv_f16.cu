@@ -1,0 +1,49 @@
+// Compiled variants of the f16 GEMV kernels.
+//   tile_g<threads per row>_c<chunks per thread>_t<block threads>_<x staging>
+//   w<lanes per row>_r<rows per group>_u<loads in flight>_w<warps>_<x staging>
+#include "gemv_kernels.cuh"
+
+namespace mbg {
+
+static const Variant kTableF16[] = {
+    // row tiles (the automatic choice for rows up to 512 * 8 * 16 bytes)
+    MBG_TILE(DT_F16, 1, 8, 256, XMODE_BULK, "tile_g1_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 2, 8, 256, XMODE_BULK, "tile_g2_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 4, 8, 256, XMODE_BULK, "tile_g4_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 8, 8, 256, XMODE_BULK, "tile_g8_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 16, 8, 256, XMODE_BULK, "tile_g16_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 32, 8, 256, XMODE_BULK, "tile_g32_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 64, 8, 256, XMODE_BULK, "tile_g64_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 128, 8, 256, XMODE_BULK, "tile_g128_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 256, 8, 256, XMODE_BULK, "tile_g256_c8_t256_bulk"),
+    MBG_TILE(DT_F16, 512, 8, 512, XMODE_BULK, "tile_g512_c8_t512_bulk"),
+    // row-tile alternatives (block size, x through L1)
+    MBG_TILE(DT_F16, 64, 8, 512, XMODE_BULK, "tile_g64_c8_t512_bulk"),
+    MBG_TILE(DT_F16, 128, 8, 512, XMODE_BULK, "tile_g128_c8_t512_bulk"),
+    MBG_TILE(DT_F16, 256, 8, 512, XMODE_BULK, "tile_g256_c8_t512_bulk"),
+    MBG_TILE(DT_F16, 512, 4, 512, XMODE_BULK, "tile_g512_c4_t512_bulk"),
+    MBG_TILE(DT_F16, 256, 4, 256, XMODE_BULK, "tile_g256_c4_t256_bulk"),
+    MBG_TILE(DT_F16, 64, 8, 256, XMODE_L1, "tile_g64_c8_t256_l1"),
+    MBG_TILE(DT_F16, 128, 8, 256, XMODE_L1, "tile_g128_c8_t256_l1"),
+    MBG_TILE(DT_F16, 256, 8, 256, XMODE_L1, "tile_g256_c8_t256_l1"),
+    MBG_TILE(DT_F16, 512, 8, 512, XMODE_L1, "tile_g512_c8_t512_l1"),
+    // rows of a warp (or of part of one) with a rolling buffer of loads
+    MBG_VEC(DT_F16, 32, 1, 8, 4, XMODE_BULK, "w32_r1_u8_w4_bulk"),
+    MBG_VEC(DT_F16, 32, 1, 4, 8, XMODE_BULK, "w32_r1_u4_w8_bulk"),
+    MBG_VEC(DT_F16, 32, 2, 4, 4, XMODE_BULK, "w32_r2_u4_w4_bulk"),
+    MBG_VEC(DT_F16, 32, 1, 8, 4, XMODE_VEC, "w32_r1_u8_w4_vec"),
+    MBG_VEC(DT_F16, 32, 1, 8, 8, XMODE_L1, "w32_r1_u8_w8_l1"),
+    MBG_VEC(DT_F16, 16, 1, 2, 4, XMODE_BULK, "w16_r1_u2_w4_bulk"),
+    MBG_VEC(DT_F16, 4, 1, 2, 4, XMODE_BULK, "w4_r1_u2_w4_bulk"),
+    MBG_VEC(DT_F16, 1, 1, 2, 4, XMODE_BULK, "w1_r1_u2_w4_bulk"),
+    // any layout
+    MBG_ELEM(DT_F16, 4, "elem_w4"),
+};
+
+const Variant *variants_f16(int *count)
+{
+    *count = static_cast<int>(sizeof(kTableF16) / sizeof(kTableF16[0]));
+    return kTableF16;
+}
+
+}  // namespace mbg

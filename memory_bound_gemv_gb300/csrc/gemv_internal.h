@@ -1,0 +1,87 @@
+// Internal declarations shared by the kernel translation units and the C-ABI
+// shim.  Not part of the public interface (include/gemv.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mbg {
+
+enum { DT_F32 = 0, DT_F16 = 1, DT_Q8 = 2, DT_Q4 = 3, DT_COUNT = 4 };
+
+enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3 };
+
+// Kernel families: warp/sub-warp rows streamed with a rolling buffer, row
+// tiles walked by a persistent grid, element-wise fallback.
+enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2 };
+
+// Device status bits (the device status word).
+enum : unsigned int { DEVERR_TIMEOUT = 1u };
+
+// Columns per FP16 scale in the quantised formats.
+constexpr int kGroup = 128;
+
+struct GemvArgs {
+    const void *A;            // weights, row-major, row pitch `row_bytes`
+    const void *x;            // input vector
+    float *y;                 // output
+    const uint16_t *scales;   // [M][groups] binary16, quantised types only
+    int64_t M;
+    int64_t N;
+    int64_t row_bytes;        // bytes per row of A
+    int64_t groups;           // ceil(N / 128)
+    int nchunks;              // row_bytes / 16 (vector kernels)
+    unsigned int *err;        // device status word
+    uint64_t wait_limit_ns;   // bound of every device-side wait
+    int skip_x_copy;          // test hook: arm the barrier but issue no copy
+};
+
+struct Variant {
+    int dtype;
+    int lanes_per_row;   // threads sharing one row (tile kernels: up to 512)
+    int rows_per_group;  // RPW (vector kernels)
+    int unroll;          // U (vector kernels) or chunks per thread per row (tile kernels)
+    int warps;           // warps per block
+    int xmode;
+    const char *name;
+    // Launches the kernel on `grid` blocks with `smem` bytes of dynamic shared memory.
+    void (*launch)(const GemvArgs &, unsigned grid, size_t smem, cudaStream_t);
+    // Raises the kernel's dynamic shared memory limit.
+    cudaError_t (*set_smem_limit)(int bytes);
+    int kind;
+    int x_offset;        // bytes of shared memory in front of the staged x
+    // Resident blocks per SM for a given dynamic shared memory size (tile kernels).
+    cudaError_t (*occupancy)(int *blocks, size_t smem);
+    int rows_per_block() const
+    {
+        if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
+        return warps * (32 / lanes_per_row) * rows_per_group;
+    }
+};
+
+// Variant tables, one per storage type (defined in gemv_<dtype>.cu).
+const Variant *variants_f32(int *count);
+const Variant *variants_f16(int *count);
+const Variant *variants_q8(int *count);
+const Variant *variants_q4(int *count);
+
+// Probe kernels (gemv_probe.cu).
+struct ProbeVariant {
+    const char *name;
+    int threads;
+    int unroll;
+    int blocks_per_sm;
+    int segment;  // 0: grid-stride tiles, 1: one contiguous segment per warp
+    void (*launch)(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
+                   cudaStream_t s);
+};
+const ProbeVariant *probe_variants(int *count);
+
+// Dequantisation kernels (gemv_dequant.cu).
+void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, int64_t M,
+                    int64_t N, bool vec, cudaStream_t s);
+
+// N == 0: y = 0.
+void launch_fill_zero(float *y, int64_t M, cudaStream_t s);
+
+}  // namespace mbg

@@ -1,0 +1,418 @@
+// GEMV kernel templates (sm_103a).
+//
+// gemv_vec_kernel: the vectorised path.  A lane group of LPR lanes owns RPW
+// consecutive rows; lane t of the group streams the 16-byte chunks
+// t, t+LPR, t+2*LPR, ... of each of those rows, so with LPR = 32 a warp reads
+// 512 contiguous bytes of a row per step ("cuda-gemv-optimization", kernel 4;
+// "Making GEMV Fast", section "Turning that access pattern into code";
+// "membound", kernel "vec").  Short rows use LPR < 32 so that one warp serves
+// several rows at once.  U chunks per row and lane are kept in flight in a
+// rolling register buffer: the load of chunk c + U*LPR is issued before
+// chunk c is consumed.  x is staged once per block in shared memory (one bulk
+// async copy tracked by an mbarrier, or cooperative vector loads), or read
+// through L1; the first U chunks of A are requested before x is waited for,
+// so the copy of x overlaps the first DRAM round trip.  Lane partials are
+// combined with an XOR butterfly inside the group and one lane stores y.
+//
+// gemv_elem_kernel: element-wise path for layouts the vector path cannot take
+// (unaligned pointers or a row pitch that is not a multiple of 16 bytes).
+#pragma once
+
+#include "gemv_device.cuh"
+
+namespace mbg {
+
+template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
+__global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
+{
+    using F = Fmt<DT>;
+    constexpr int EPC = F::EPC;
+    constexpr int XCB = x_chunk_bytes<DT>();
+    constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int GPW = 32 / LPR;
+    constexpr int ROWS_PER_WARP = GPW * RPW;
+    constexpr int ROWS_PER_BLOCK = WARPS * ROWS_PER_WARP;
+    constexpr int CHUNKS_PER_GROUP = kGroup / EPC;  // chunks sharing one scale
+    static_assert(32 % LPR == 0, "lanes per row must divide the warp");
+    static_assert(XMODE == XMODE_BULK || XMODE == XMODE_VEC || XMODE == XMODE_L1, "xmode");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *xs = smem + 16;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t = lane % LPR;
+    const int64_t row_base = static_cast<int64_t>(blockIdx.x) * ROWS_PER_BLOCK +
+                             static_cast<int64_t>(warp) * ROWS_PER_WARP + (lane / LPR) * RPW;
+    const int nchunks = p.nchunks;
+    const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
+
+    if constexpr (XMODE == XMODE_BULK) {
+        if (threadIdx.x == 0) {
+            const uint32_t b = smem_addr(bar);
+            mbar_init(b, 1);
+            mbar_arrive_expect_tx(b, xbytes);
+            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
+        }
+    }
+
+    // Rows of this lane group (clamped to the last row; results of clamped
+    // rows are discarded) and the first U chunks of each.
+    const bool active = row_base < p.M;
+    const int my_chunks = active ? nchunks : 0;
+    const unsigned char *rowp[RPW];
+    const uint16_t *srow[RPW];
+    bool rvalid[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int64_t row = row_base + r;
+        rvalid[r] = row < p.M;
+        const int64_t rr = row < p.M ? row : p.M - 1;
+        rowp[r] = static_cast<const unsigned char *>(p.A) + rr * p.row_bytes;
+        srow[r] = F::QUANT ? p.scales + rr * p.groups : nullptr;
+    }
+
+    uint4 buf[RPW][U];
+    float sbuf[RPW][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = t + u * LPR;
+        if (c < my_chunks) {
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                buf[r][u] = ld_stream16(rowp[r] + static_cast<size_t>(c) * 16);
+                if constexpr (F::QUANT) sbuf[r][u] = ld_half_as_float(srow[r] + c / CHUNKS_PER_GROUP);
+                else sbuf[r][u] = 0.f;
+            }
+        }
+    }
+
+    if constexpr (XMODE == XMODE_VEC) {
+        const uint4 *src = static_cast<const uint4 *>(p.x);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs);
+        for (uint32_t i = threadIdx.x; i < xbytes / 16; i += WARPS * 32) dst[i] = ld_cached16(src + i);
+    }
+    if constexpr (XMODE == XMODE_BULK || XMODE == XMODE_VEC) __syncthreads();
+    if constexpr (XMODE == XMODE_BULK) {
+        if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
+            if (threadIdx.x == 0) report_error(p.err, DEVERR_TIMEOUT);
+            // A copy that was issued may still land: give it one more bounded
+            // wait before the block's shared memory is released.
+            if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns);
+            return;
+        }
+    }
+
+    const unsigned char *xsrc =
+        (XMODE == XMODE_L1) ? static_cast<const unsigned char *>(p.x) : xs;
+
+    float acc[RPW][NACC];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int k = 0; k < NACC; ++k) acc[r][k] = 0.f;
+
+    for (int c0 = t; c0 < my_chunks; c0 += LPR * U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + u * LPR;
+            if (c < my_chunks) {
+                uint4 xv[XV];
+#pragma unroll
+                for (int v = 0; v < XV; ++v) {
+                    const unsigned char *px = xsrc + static_cast<size_t>(c) * XCB + 16 * v;
+                    if constexpr (XMODE == XMODE_L1) xv[v] = ld_cached16(px);
+                    else xv[v] = *reinterpret_cast<const uint4 *>(px);
+                }
+                float xf[EPC];
+                x_to_float<DT>(xv, xf);
+
+                uint4 cur[RPW];
+                float sc[RPW];
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    cur[r] = buf[r][u];
+                    sc[r] = sbuf[r][u];
+                }
+                const int cn = c + LPR * U;
+                if (cn < my_chunks) {
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) {
+                        buf[r][u] = ld_stream16(rowp[r] + static_cast<size_t>(cn) * 16);
+                        if constexpr (F::QUANT)
+                            sbuf[r][u] = ld_half_as_float(srow[r] + cn / CHUNKS_PER_GROUP);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    float wf[EPC];
+                    chunk_to_float<DT>(cur[r], wf);
+                    chunk_fma<DT>(wf, xf, sc[r], acc[r]);
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        float s = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+        s = group_sum<LPR>(s);
+        if (t == (r % LPR) && rvalid[r]) p.y[row_base + r] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row-tile kernel
+// ---------------------------------------------------------------------------
+//
+// G threads share one row and request all of it at once: thread g of the
+// group loads chunks g, g+G, ..., g+(CPT-1)*G (so G*CPT*16 bytes must cover
+// the row).  A block of T threads holds T/G consecutive rows (a tile); the
+// grid is persistent and walks tiles in grid-stride order, issuing the loads
+// of its next tile before it reduces the current one.  At any moment the
+// loads in flight therefore cover a dense band of consecutive rows, which is
+// how HBM3e delivers its bandwidth (scattered per-warp streams reach far
+// less).  Lane partials are summed with an XOR butterfly; groups wider than a
+// warp combine their warps' partials through shared memory (double-buffered,
+// one block barrier per tile: every thread of a block walks the same tiles)
+// ("llama.cpp GEMV CUDA": a block-wide row with a warp reduction, warp sums
+// in shared memory and a second warp reduction).
+template <int DT, int G, int CPT, int T, int XMODE>
+__global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
+{
+    using F = Fmt<DT>;
+    constexpr int EPC = F::EPC;
+    constexpr int XCB = x_chunk_bytes<DT>();
+    constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int RT = T / G;                       // rows per tile
+    constexpr bool WIDE = G > 32;                   // group spans several warps
+    constexpr int GW = WIDE ? G / 32 : 1;           // warps per group
+    constexpr int LW = WIDE ? 32 : G;               // shuffle width
+    constexpr int CHUNKS_PER_GROUP = kGroup / EPC;
+    constexpr int PART_BYTES = WIDE ? 2 * (T / 32) * 4 : 0;
+    constexpr int X_OFFSET = (16 + PART_BYTES + 15) / 16 * 16;
+    static_assert(T % G == 0 && (G <= 32 ? 32 % G == 0 : G % 32 == 0), "group shape");
+    static_assert(XMODE == XMODE_BULK || XMODE == XMODE_L1, "xmode");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    float *part = reinterpret_cast<float *>(smem + 16);
+    unsigned char *xs = smem + X_OFFSET;
+
+    const int tid = threadIdx.x;
+    const int grp = tid / G;
+    const int tg = tid % G;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nchunks = p.nchunks;
+    const int64_t ntiles = (p.M + RT - 1) / RT;
+    const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
+
+    if constexpr (XMODE == XMODE_BULK) {
+        if (tid == 0) {
+            const uint32_t b = smem_addr(bar);
+            mbar_init(b, 1);
+            mbar_arrive_expect_tx(b, xbytes);
+            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
+        }
+    }
+
+    uint4 cur[CPT], nxt[CPT];
+    float scur[CPT], snxt[CPT];
+
+    auto load_tile = [&](int64_t tile, uint4 (&buf)[CPT], float (&sb)[CPT]) {
+        const int64_t row = tile * RT + grp;
+        if (row < p.M) {
+            const unsigned char *rp = static_cast<const unsigned char *>(p.A) + row * p.row_bytes;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = tg + k * G;
+                if (c < nchunks) {
+                    buf[k] = ld_stream16(rp + static_cast<size_t>(c) * 16);
+                    if constexpr (F::QUANT)
+                        sb[k] = ld_half_as_float(p.scales + row * p.groups + c / CHUNKS_PER_GROUP);
+                }
+            }
+        }
+    };
+
+    int64_t tile = blockIdx.x;
+    if (tile < ntiles) load_tile(tile, cur, scur);
+
+    if constexpr (XMODE == XMODE_BULK) {
+        __syncthreads();
+        if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
+            if (tid == 0) report_error(p.err, DEVERR_TIMEOUT);
+            if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns);
+            return;
+        }
+    }
+    const unsigned char *xsrc = (XMODE == XMODE_L1) ? static_cast<const unsigned char *>(p.x) : xs;
+
+    int parity = 0;
+    for (; tile < ntiles; tile += gridDim.x) {
+        const int64_t next = tile + gridDim.x;
+        if (next < ntiles) load_tile(next, nxt, snxt);
+
+        const int64_t row = tile * RT + grp;
+        const bool valid = row < p.M;
+        float acc[NACC] = {0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = tg + k * G;
+                if (c < nchunks) {
+                    uint4 xv[XV];
+#pragma unroll
+                    for (int v = 0; v < XV; ++v) {
+                        const unsigned char *px = xsrc + static_cast<size_t>(c) * XCB + 16 * v;
+                        if constexpr (XMODE == XMODE_L1) xv[v] = ld_cached16(px);
+                        else xv[v] = *reinterpret_cast<const uint4 *>(px);
+                    }
+                    float xf[EPC];
+                    x_to_float<DT>(xv, xf);
+                    float wf[EPC];
+                    chunk_to_float<DT>(cur[k], wf);
+                    chunk_fma<DT>(wf, xf, F::QUANT ? scur[k] : 0.f, acc);
+                }
+            }
+        }
+        float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        s = group_sum<LW>(s);
+        if constexpr (WIDE) {
+            float *pp = part + parity * (T / 32);
+            if (lane == 0) pp[warp] = s;
+            __syncthreads();
+            if (tg < 32) {
+                float v = lane < GW ? pp[grp * GW + lane] : 0.f;
+                v = group_sum<32>(v);
+                if (tg == 0 && valid) p.y[row] = v;
+            }
+            parity ^= 1;
+        } else {
+            if (tg == 0 && valid) p.y[row] = s;
+        }
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            cur[k] = nxt[k];
+            scur[k] = snxt[k];
+        }
+    }
+}
+
+template <int DT, int G, int CPT, int T, int XMODE>
+constexpr int tile_x_offset()
+{
+    return (16 + (G > 32 ? 2 * (T / 32) * 4 : 0) + 15) / 16 * 16;
+}
+
+// Element weight (i, j) as FP32; the quantised types return FP32(s) * q,
+// which is exact.
+template <int DT>
+__device__ __forceinline__ float elem_weight(const GemvArgs &p, int64_t i, int64_t j)
+{
+    const unsigned char *row = static_cast<const unsigned char *>(p.A) + i * p.row_bytes;
+    if constexpr (DT == DT_F32) {
+        return __ldg(reinterpret_cast<const float *>(row) + j);
+    } else if constexpr (DT == DT_F16) {
+        return ld_half_as_float(reinterpret_cast<const uint16_t *>(row) + j);
+    } else {
+        const float s = ld_half_as_float(p.scales + i * p.groups + j / kGroup);
+        int q;
+        if constexpr (DT == DT_Q8) {
+            q = static_cast<int>(static_cast<signed char>(__ldg(reinterpret_cast<const char *>(row) + j)));
+        } else {
+            const unsigned b = __ldg(row + (j >> 1));
+            const unsigned nib = (j & 1) ? (b >> 4) : (b & 0xFu);
+            q = static_cast<int>(nib) - ((nib & 8u) ? 16 : 0);
+        }
+        return s * static_cast<float>(q);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float elem_x(const GemvArgs &p, int64_t j)
+{
+    if constexpr (DT == DT_F32) return __ldg(static_cast<const float *>(p.x) + j);
+    else return ld_half_as_float(static_cast<const uint16_t *>(p.x) + j);
+}
+
+template <int DT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) gemv_elem_kernel(const GemvArgs p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+    if (row >= p.M) return;  // whole warp leaves together
+    float acc[NACC] = {0.f, 0.f, 0.f, 0.f};
+    int k = 0;
+    for (int64_t j = lane; j < p.N; j += 32, ++k) {
+        acc[k & (NACC - 1)] = fmaf(elem_weight<DT>(p, row, j), elem_x<DT>(p, j), acc[k & (NACC - 1)]);
+    }
+    float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    s = group_sum<32>(s);
+    if (lane == 0) p.y[row] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Variant-table glue
+// ---------------------------------------------------------------------------
+
+template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
+void launch_vec(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+{
+    gemv_vec_kernel<DT, LPR, RPW, U, WARPS, XMODE><<<grid, WARPS * 32, smem, s>>>(a);
+}
+
+template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
+cudaError_t smem_limit_vec(int bytes)
+{
+    return cudaFuncSetAttribute(gemv_vec_kernel<DT, LPR, RPW, U, WARPS, XMODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DT, int WARPS>
+void launch_elem(const GemvArgs &a, unsigned grid, size_t, cudaStream_t s)
+{
+    gemv_elem_kernel<DT, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
+}
+
+template <int DT, int WARPS>
+cudaError_t smem_limit_elem(int)
+{
+    return cudaSuccess;
+}
+
+template <int DT, int G, int CPT, int T, int XMODE>
+void launch_tile(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+{
+    gemv_tile_kernel<DT, G, CPT, T, XMODE><<<grid, T, smem, s>>>(a);
+}
+
+template <int DT, int G, int CPT, int T, int XMODE>
+cudaError_t smem_limit_tile(int bytes)
+{
+    return cudaFuncSetAttribute(gemv_tile_kernel<DT, G, CPT, T, XMODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DT, int G, int CPT, int T, int XMODE>
+cudaError_t occupancy_tile(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_tile_kernel<DT, G, CPT, T, XMODE>,
+                                                         T, smem);
+}
+
+#define MBG_TILE(DT, G, CPT, T, XM, NAME)                                                    \
+    Variant{DT, G, 1, CPT, T / 32, XM, NAME, &launch_tile<DT, G, CPT, T, XM>,                 \
+            &smem_limit_tile<DT, G, CPT, T, XM>, KIND_TILE, tile_x_offset<DT, G, CPT, T, XM>(), \
+            &occupancy_tile<DT, G, CPT, T, XM>}
+
+#define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
+    Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \
+            &smem_limit_vec<DT, LPR, RPW, U, W, XM>, KIND_VEC, 16, nullptr}
+#define MBG_ELEM(DT, W, NAME) \
+    Variant{DT, 32, 1, 1, W, XMODE_ELEM, NAME, &launch_elem<DT, W>, &smem_limit_elem<DT, W>, \
+            KIND_ELEM, 0, nullptr}
+
+}  // namespace mbg

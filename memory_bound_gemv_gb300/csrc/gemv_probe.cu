@@ -1,0 +1,94 @@
+// Pure-read bandwidth probe ("membound", section "Why GEMV, and why MBU": the
+// read ceiling measured on the same card is the denominator for a GEMV,
+// whose traffic is almost all reads).
+//
+// The probe uses the GEMV kernels' load instruction (16-byte, read-only, L1
+// no-allocate, 256-byte L2 fetch) and their rolling buffer of U loads in
+// flight per lane.  Two read patterns:
+//   segment: each warp streams one contiguous stretch of the buffer with its
+//            lanes 16 bytes apart -- the access pattern of a warp-per-row GEMV;
+//   stride:  blocks walk tiles of THREADS*U vectors in grid-stride order.
+// Every loaded word is XOR-folded; each warp XORs its fold into *sink, so no
+// load can be dropped as dead code.
+#include "gemv_device.cuh"
+
+namespace mbg {
+
+template <int THREADS, int U, int SEGMENT>
+__global__ void __launch_bounds__(THREADS) probe_read_kernel(const uint4 *buf, size_t n16,
+                                                             unsigned long long *sink)
+{
+    uint32_t fold = 0;
+    const int lane = threadIdx.x & 31;
+    if constexpr (SEGMENT) {
+        const size_t warps = static_cast<size_t>(gridDim.x) * (THREADS / 32);
+        const size_t w = static_cast<size_t>(blockIdx.x) * (THREADS / 32) + (threadIdx.x >> 5);
+        size_t seg = (n16 + warps - 1) / warps;
+        seg = (seg + 31) & ~static_cast<size_t>(31);
+        const size_t begin = w * seg;
+        const size_t end = begin + seg < n16 ? begin + seg : n16;
+        if (begin < end) {
+            const uint4 *base = buf + begin;
+            const size_t n = end - begin;
+            uint4 b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const size_t c = lane + static_cast<size_t>(u) * 32;
+                if (c < n) b[u] = ld_stream16(base + c);
+            }
+            for (size_t c0 = lane; c0 < n; c0 += 32 * U) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const size_t c = c0 + static_cast<size_t>(u) * 32;
+                    if (c < n) {
+                        const uint4 v = b[u];
+                        const size_t cn = c + 32 * U;
+                        if (cn < n) b[u] = ld_stream16(base + cn);
+                        fold ^= v.x ^ v.y ^ v.z ^ v.w;
+                    }
+                }
+            }
+        }
+    } else {
+        const size_t tile = static_cast<size_t>(THREADS) * U;
+        const size_t step = static_cast<size_t>(gridDim.x) * tile;
+        for (size_t t0 = static_cast<size_t>(blockIdx.x) * tile; t0 < n16; t0 += step) {
+            uint4 b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const size_t c = t0 + static_cast<size_t>(u) * THREADS + threadIdx.x;
+                b[u] = c < n16 ? ld_stream16(buf + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) fold ^= b[u].x ^ b[u].y ^ b[u].z ^ b[u].w;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) fold ^= __shfl_xor_sync(0xffffffffu, fold, off);
+    if (lane == 0 && fold) atomicXor(sink, static_cast<unsigned long long>(fold));
+}
+
+template <int THREADS, int U, int SEGMENT>
+void launch_probe(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
+                  cudaStream_t s)
+{
+    probe_read_kernel<THREADS, U, SEGMENT>
+        <<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
+}
+
+static const ProbeVariant kProbes[] = {
+    {"segment_t128_u8_b8", 128, 8, 8, 1, &launch_probe<128, 8, 1>},
+    {"segment_t256_u8_b4", 256, 8, 4, 1, &launch_probe<256, 8, 1>},
+    {"segment_t128_u16_b6", 128, 16, 6, 1, &launch_probe<128, 16, 1>},
+    {"stride_t256_u8_b4", 256, 8, 4, 0, &launch_probe<256, 8, 0>},
+    {"stride_t512_u4_b4", 512, 4, 4, 0, &launch_probe<512, 4, 0>},
+    {"stride_t256_u16_b4", 256, 16, 4, 0, &launch_probe<256, 16, 0>},
+};
+
+const ProbeVariant *probe_variants(int *count)
+{
+    *count = static_cast<int>(sizeof(kProbes) / sizeof(kProbes[0]));
+    return kProbes;
+}
+
+}  // namespace mbg
