@@ -144,6 +144,8 @@ typedef struct {
     int rows_per_group;  /* rows one lane group streams together (family 0, x reuse) */
     int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread */
     int warps;           /* warps per block */
+    int math;            /* 0: operands converted to FP32; 1: binary16 operands into
+                            mixed-precision FMAs with FP32 accumulation */
     int xmode;          /* 0: x copied to shared memory by a bulk async copy,
                            1: x copied to shared memory by vector loads,
                            2: x read through the L1 cache, 3: element-wise kernel */

@@ -43,7 +43,8 @@ KINDS = {0: "vec", 1: "tile", 2: "elem"}
 class VariantInfo(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("kind", ctypes.c_int), ("threads_per_row", ctypes.c_int),
                 ("rows_per_group", ctypes.c_int), ("unroll", ctypes.c_int),
-                ("warps", ctypes.c_int), ("xmode", ctypes.c_int), ("name", ctypes.c_char * 48)]
+                ("warps", ctypes.c_int), ("math", ctypes.c_int), ("xmode", ctypes.c_int),
+                ("name", ctypes.c_char * 48)]
 
 
 _lock = threading.Lock()
@@ -247,7 +248,8 @@ def variants(dtype: str) -> List[dict]:
         out.append({"id": k, "name": info.name.decode(), "kind": KINDS[info.kind],
                     "threads_per_row": info.threads_per_row,
                     "rows_per_group": info.rows_per_group, "unroll": info.unroll,
-                    "warps": info.warps, "xmode": XMODES[info.xmode]})
+                    "warps": info.warps, "math": "mixed" if info.math else "f32",
+                    "xmode": XMODES[info.xmode]})
     return out
 
 

@@ -334,6 +334,7 @@ gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *inf
     info->rows_per_group = w.rows_per_group;
     info->unroll = w.unroll;
     info->warps = w.warps;
+    info->math = w.math;
     info->xmode = w.xmode;
     snprintf(info->name, sizeof(info->name), "%s", w.name);
     return GEMV_OK;

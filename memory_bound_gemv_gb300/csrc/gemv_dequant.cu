@@ -1,5 +1,6 @@
-// Dequantisation to FP32 with the GEMV kernels' own unpacking code, so that
-// comparing its output bit for bit with the oracle's q * s checks that code
+// Dequantisation to FP32 with the GEMV kernels' own unpacking code (the
+// binary16 codes of the mixed-precision path), so that comparing its output
+// bit for bit with the oracle's q * s checks that code
 // ("membound", section "dequant GEMV": the reference is computed on the
 // dequantised weights, q * s exactly).  Also the N == 0 fill.
 #include "gemv_kernels.cuh"
@@ -19,8 +20,25 @@ __global__ void dequant_vec_kernel(const unsigned char *A, const uint16_t *scale
         const int64_t i = k / nchunks;
         const int64_t c = k - i * nchunks;
         const uint4 a = ld_stream16(A + i * row_bytes + c * 16);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
         float wf[EPC];
-        chunk_to_float<DT>(a, wf);
+        // the binary16 codes of the mixed-precision GEMV path, widened exactly
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (DT == DT_Q8) {
+                uint32_t h[2];
+                q8_codes_h2(w[k], h);
+                half2_bits_to_float(h[0], wf[4 * k + 0], wf[4 * k + 1]);
+                half2_bits_to_float(h[1], wf[4 * k + 2], wf[4 * k + 3]);
+            } else {
+                uint32_t h[4];
+                q4_codes_h2(w[k], h);
+                half2_bits_to_float(h[0], wf[8 * k + 0], wf[8 * k + 4]);
+                half2_bits_to_float(h[1], wf[8 * k + 1], wf[8 * k + 5]);
+                half2_bits_to_float(h[2], wf[8 * k + 2], wf[8 * k + 6]);
+                half2_bits_to_float(h[3], wf[8 * k + 3], wf[8 * k + 7]);
+            }
+        }
         const float s = ld_half_as_float(scales + i * groups + (c * EPC) / kGroup);
         float *out = W + i * N + c * EPC;
 #pragma unroll

@@ -260,6 +260,132 @@ __device__ __forceinline__ void chunk_fma(const float (&wf)[Fmt<DT>::EPC],
     }
 }
 
+// ---------------------------------------------------------------------------
+// Mixed-precision path: binary16 operands, FP32 accumulation, no conversions
+// ---------------------------------------------------------------------------
+//
+// fma.rn.f32.f16 (sm_100 and later) multiplies two binary16 values and adds
+// an FP32 accumulator.  The product of two binary16 significands (11 bits
+// each) is exact in FP32, so c + a*b is rounded once, exactly as
+// fmaf(float(a), float(b), c) would be.  On this GPU it issues at the full
+// FP32 rate, while a binary16 -> FP32 conversion issues at half rate.
+
+// c0 += lo(a) * lo(b);  c1 += hi(a) * hi(b)
+__device__ __forceinline__ void mfma_pair(uint32_t a, uint32_t b, float &c0, float &c1)
+{
+    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+        " fma.rn.f32.f16 %0, a0, b0, %0;\n fma.rn.f32.f16 %1, a1, b1, %1;\n}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(a), "r"(b));
+}
+
+// c0 += lo(a) * lo(b0);  c1 += hi(a) * lo(b1)  (codes paired across x words)
+__device__ __forceinline__ void mfma_cross_lo(uint32_t a, uint32_t b0, uint32_t b1, float &c0,
+                                              float &c1)
+{
+    asm("{\n .reg .f16 a0, a1, p0, p1, q0, q1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {p0, p1}, %3;\n"
+        " mov.b32 {q0, q1}, %4;\n fma.rn.f32.f16 %0, a0, p0, %0;\n fma.rn.f32.f16 %1, a1, q0, %1;\n}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(a), "r"(b0), "r"(b1));
+}
+
+// c0 += lo(a) * hi(b0);  c1 += hi(a) * hi(b1)
+__device__ __forceinline__ void mfma_cross_hi(uint32_t a, uint32_t b0, uint32_t b1, float &c0,
+                                              float &c1)
+{
+    asm("{\n .reg .f16 a0, a1, p0, p1, q0, q1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {p0, p1}, %3;\n"
+        " mov.b32 {q0, q1}, %4;\n fma.rn.f32.f16 %0, a0, p1, %0;\n fma.rn.f32.f16 %1, a1, q1, %1;\n}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(a), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Four int8 codes -> two pairs of exact binary16 values, in column order:
+// h[0] = (q0, q1), h[1] = (q2, q3).  The sign flip gives the byte q + 128;
+// pairing it with 0x64 forms the binary16 value 1024 + q + 128, and
+// subtracting 1152 (0x6480) leaves q.
+__device__ __forceinline__ void q8_codes_h2(uint32_t w, uint32_t (&h)[2])
+{
+    const uint32_t u = w ^ 0x80808080u;
+    h[0] = hsub2_bits(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u);
+    h[1] = hsub2_bits(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
+}
+
+// Eight int4 codes of a word (nibble k = column k) -> four pairs of exact
+// binary16 values, paired four columns apart: h[0] = (q0, q4),
+// h[1] = (q1, q5), h[2] = (q2, q6), h[3] = (q3, q7).  After the XOR each
+// nibble holds q + 8.  A nibble in bits 0-3 of a half OR-ed into 0x6400 is
+// 1024 + (q + 8), minus 1032 (0x6408) gives q; a nibble in bits 4-7 gives
+// 1024 + 16 (q + 8), and times 1/16 (0x2C00) minus 72 (0xD480) gives q.
+__device__ __forceinline__ void q4_codes_h2(uint32_t w, uint32_t (&h)[4])
+{
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t v = u >> 8;
+    h[0] = hsub2_bits((u & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+    h[1] = hfma2_bits((u & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+    h[2] = hsub2_bits((v & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+    h[3] = hfma2_bits((v & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+}
+
+// One 16-byte chunk of A times its x chunk (binary16), accumulated in FP32.
+// Quantised chunks are summed into partials and scaled once per chunk
+// (the chunk lies inside one 128-column group).
+template <int DT>
+__device__ __forceinline__ void chunk_dot_mixed(const uint4 a, const uint4 (&xv)[x_chunk_vecs<DT>()],
+                                                float scale, float (&acc)[NACC])
+{
+    static_assert(DT != DT_F32, "FP32 weights take the FP32 path");
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    if constexpr (DT == DT_F16) {
+        (void)scale;
+        mfma_pair(w[0], xv[0].x, acc[0], acc[1]);
+        mfma_pair(w[1], xv[0].y, acc[2], acc[3]);
+        mfma_pair(w[2], xv[0].z, acc[0], acc[1]);
+        mfma_pair(w[3], xv[0].w, acc[2], acc[3]);
+    } else if constexpr (DT == DT_Q8) {
+        float p[NACC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t h[2];
+            q8_codes_h2(w[k], h);
+            const uint4 &x = xv[k >> 1];
+            const uint32_t x01 = (k & 1) ? x.z : x.x;
+            const uint32_t x23 = (k & 1) ? x.w : x.y;
+            mfma_pair(h[0], x01, p[0], p[1]);
+            mfma_pair(h[1], x23, p[2], p[3]);
+        }
+#pragma unroll
+        for (int k = 0; k < NACC; ++k) acc[k] = fmaf(scale, p[k], acc[k]);
+    } else {
+        float p[NACC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t h[4];
+            q4_codes_h2(w[k], h);
+            const uint4 &x = xv[k];  // x words (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+            mfma_cross_lo(h[0], x.x, x.z, p[0], p[1]);  // q0*x0, q4*x4
+            mfma_cross_hi(h[1], x.x, x.z, p[2], p[3]);  // q1*x1, q5*x5
+            mfma_cross_lo(h[2], x.y, x.w, p[0], p[1]);  // q2*x2, q6*x6
+            mfma_cross_hi(h[3], x.y, x.w, p[2], p[3]);  // q3*x3, q7*x7
+        }
+#pragma unroll
+        for (int k = 0; k < NACC; ++k) acc[k] = fmaf(scale, p[k], acc[k]);
+    }
+}
+
 template <int WIDTH>
 __device__ __forceinline__ float group_sum(float v)
 {

@@ -27,6 +27,10 @@ static const Variant kTableF16[] = {
     MBG_TILE(DT_F16, 128, 8, 256, XMODE_L1, "tile_g128_c8_t256_l1"),
     MBG_TILE(DT_F16, 256, 8, 256, XMODE_L1, "tile_g256_c8_t256_l1"),
     MBG_TILE(DT_F16, 512, 8, 512, XMODE_L1, "tile_g512_c8_t512_l1"),
+    // row tiles with operands converted to FP32 (for comparison)
+    MBG_TILE_M(DT_F16, 64, 8, 256, XMODE_BULK, MATH_F32, "tile_g64_c8_t256_bulk_f32math"),
+    MBG_TILE_M(DT_F16, 256, 8, 256, XMODE_BULK, MATH_F32, "tile_g256_c8_t256_bulk_f32math"),
+    MBG_TILE_M(DT_F16, 512, 4, 512, XMODE_BULK, MATH_F32, "tile_g512_c4_t512_bulk_f32math"),
     // rows of a warp (or of part of one) with a rolling buffer of loads
     MBG_VEC(DT_F16, 32, 1, 8, 4, XMODE_BULK, "w32_r1_u8_w4_bulk"),
     MBG_VEC(DT_F16, 32, 1, 4, 8, XMODE_BULK, "w32_r1_u4_w8_bulk"),

@@ -15,6 +15,10 @@ enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3 };
 // tiles walked by a persistent grid, element-wise fallback.
 enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2 };
 
+// Dot-product arithmetic: operands converted to FP32, or binary16 operands
+// fed to mixed-precision FMAs with FP32 accumulation.
+enum { MATH_F32 = 0, MATH_MIXED = 1 };
+
 // Device status bits (the device status word).
 enum : unsigned int { DEVERR_TIMEOUT = 1u };
 
@@ -52,6 +56,8 @@ struct Variant {
     int x_offset;        // bytes of shared memory in front of the staged x
     // Resident blocks per SM for a given dynamic shared memory size (tile kernels).
     cudaError_t (*occupancy)(int *blocks, size_t smem);
+    int math;            // MATH_F32 or MATH_MIXED
+    int stages;          // bulk-pipeline depth (KIND_BULK)
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
@@ -71,7 +77,7 @@ struct ProbeVariant {
     int threads;
     int unroll;
     int blocks_per_sm;
-    int segment;  // 0: grid-stride tiles, 1: one contiguous segment per warp
+    int segment;  // 0: grid-stride tiles, 1: one contiguous segment per warp, 2: prefetching tiles
     void (*launch)(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
                    cudaStream_t s);
 };

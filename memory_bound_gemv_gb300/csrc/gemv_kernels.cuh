@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
 // one block barrier per tile: every thread of a block walks the same tiles)
 // ("llama.cpp GEMV CUDA": a block-wide row with a warp reduction, warp sums
 // in shared memory and a second warp reduction).
-template <int DT, int G, int CPT, int T, int XMODE>
+template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     constexpr int X_OFFSET = (16 + PART_BYTES + 15) / 16 * 16;
     static_assert(T % G == 0 && (G <= 32 ? 32 % G == 0 : G % 32 == 0), "group shape");
     static_assert(XMODE == XMODE_BULK || XMODE == XMODE_L1, "xmode");
+    static_assert(MATH == MATH_F32 || DT != DT_F32, "FP32 weights use FP32 math");
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
@@ -270,11 +271,15 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
                         if constexpr (XMODE == XMODE_L1) xv[v] = ld_cached16(px);
                         else xv[v] = *reinterpret_cast<const uint4 *>(px);
                     }
-                    float xf[EPC];
-                    x_to_float<DT>(xv, xf);
-                    float wf[EPC];
-                    chunk_to_float<DT>(cur[k], wf);
-                    chunk_fma<DT>(wf, xf, F::QUANT ? scur[k] : 0.f, acc);
+                    if constexpr (MATH == MATH_MIXED) {
+                        chunk_dot_mixed<DT>(cur[k], xv, F::QUANT ? scur[k] : 0.f, acc);
+                    } else {
+                        float xf[EPC];
+                        x_to_float<DT>(xv, xf);
+                        float wf[EPC];
+                        chunk_to_float<DT>(cur[k], wf);
+                        chunk_fma<DT>(wf, xf, F::QUANT ? scur[k] : 0.f, acc);
+                    }
                 }
             }
         }
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     }
 }
 
-template <int DT, int G, int CPT, int T, int XMODE>
+template <int DT, int G, int CPT, int T>
 constexpr int tile_x_offset()
 {
     return (16 + (G > 32 ? 2 * (T / 32) * 4 : 0) + 15) / 16 * 16;
@@ -383,36 +388,39 @@ cudaError_t smem_limit_elem(int)
     return cudaSuccess;
 }
 
-template <int DT, int G, int CPT, int T, int XMODE>
+template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 void launch_tile(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
 {
-    gemv_tile_kernel<DT, G, CPT, T, XMODE><<<grid, T, smem, s>>>(a);
+    gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH><<<grid, T, smem, s>>>(a);
 }
 
-template <int DT, int G, int CPT, int T, int XMODE>
+template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 cudaError_t smem_limit_tile(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_tile_kernel<DT, G, CPT, T, XMODE>,
+    return cudaFuncSetAttribute(gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DT, int G, int CPT, int T, int XMODE>
+template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 cudaError_t occupancy_tile(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_tile_kernel<DT, G, CPT, T, XMODE>,
-                                                         T, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        blocks, gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>, T, smem);
 }
 
-#define MBG_TILE(DT, G, CPT, T, XM, NAME)                                                    \
-    Variant{DT, G, 1, CPT, T / 32, XM, NAME, &launch_tile<DT, G, CPT, T, XM>,                 \
-            &smem_limit_tile<DT, G, CPT, T, XM>, KIND_TILE, tile_x_offset<DT, G, CPT, T, XM>(), \
-            &occupancy_tile<DT, G, CPT, T, XM>}
+#define MBG_TILE_M(DT, G, CPT, T, XM, MATH, NAME)                                              \
+    Variant{DT, G, 1, CPT, T / 32, XM, NAME, &launch_tile<DT, G, CPT, T, XM, MATH>,             \
+            &smem_limit_tile<DT, G, CPT, T, XM, MATH>, KIND_TILE, tile_x_offset<DT, G, CPT, T>(), \
+            &occupancy_tile<DT, G, CPT, T, XM, MATH>, MATH, 0}
+// FP32 weights use FP32 arithmetic; the other types default to the mixed path.
+#define MBG_TILE(DT, G, CPT, T, XM, NAME) \
+    MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \
-            &smem_limit_vec<DT, LPR, RPW, U, W, XM>, KIND_VEC, 16, nullptr}
+            &smem_limit_vec<DT, LPR, RPW, U, W, XM>, KIND_VEC, 16, nullptr, MATH_F32, 0}
 #define MBG_ELEM(DT, W, NAME) \
     Variant{DT, 32, 1, 1, W, XMODE_ELEM, NAME, &launch_elem<DT, W>, &smem_limit_elem<DT, W>, \
-            KIND_ELEM, 0, nullptr}
+            KIND_ELEM, 0, nullptr, MATH_F32, 0}
 
 }  // namespace mbg

@@ -4,10 +4,13 @@
 //
 // The probe uses the GEMV kernels' load instruction (16-byte, read-only, L1
 // no-allocate, 256-byte L2 fetch) and their rolling buffer of U loads in
-// flight per lane.  Two read patterns:
+// flight per lane.  Three read patterns:
 //   segment: each warp streams one contiguous stretch of the buffer with its
 //            lanes 16 bytes apart -- the access pattern of a warp-per-row GEMV;
-//   stride:  blocks walk tiles of THREADS*U vectors in grid-stride order.
+//   stride:  blocks walk tiles of THREADS*U vectors in grid-stride order;
+//   tile:    the row-tile GEMV's pattern: a persistent grid walks tiles of
+//            THREADS*U vectors in grid-stride order and requests the next tile
+//            before folding the current one.
 // Every loaded word is XOR-folded; each warp XORs its fold into *sink, so no
 // load can be dropped as dead code.
 #include "gemv_device.cuh"
@@ -68,6 +71,42 @@ __global__ void __launch_bounds__(THREADS) probe_read_kernel(const uint4 *buf, s
     if (lane == 0 && fold) atomicXor(sink, static_cast<unsigned long long>(fold));
 }
 
+template <int THREADS, int U>
+__global__ void __launch_bounds__(THREADS) probe_tile_kernel(const uint4 *buf, size_t n16,
+                                                             unsigned long long *sink)
+{
+    uint32_t fold = 0;
+    const size_t tile = static_cast<size_t>(THREADS) * U;
+    const size_t ntiles = (n16 + tile - 1) / tile;
+    uint4 cur[U], nxt[U];
+    auto load = [&](size_t t, uint4 (&b)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t c = t * tile + static_cast<size_t>(u) * THREADS + threadIdx.x;
+            b[u] = c < n16 ? ld_stream16(buf + c) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    size_t t = blockIdx.x;
+    if (t < ntiles) load(t, cur);
+    for (; t < ntiles; t += gridDim.x) {
+        if (t + gridDim.x < ntiles) load(t + gridDim.x, nxt);
+#pragma unroll
+        for (int u = 0; u < U; ++u) fold ^= cur[u].x ^ cur[u].y ^ cur[u].z ^ cur[u].w;
+#pragma unroll
+        for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) fold ^= __shfl_xor_sync(0xffffffffu, fold, off);
+    if ((threadIdx.x & 31) == 0 && fold) atomicXor(sink, static_cast<unsigned long long>(fold));
+}
+
+template <int THREADS, int U>
+void launch_probe_tile(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
+                       cudaStream_t s)
+{
+    probe_tile_kernel<THREADS, U><<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
+}
+
 template <int THREADS, int U, int SEGMENT>
 void launch_probe(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
                   cudaStream_t s)
@@ -83,6 +122,10 @@ static const ProbeVariant kProbes[] = {
     {"stride_t256_u8_b4", 256, 8, 4, 0, &launch_probe<256, 8, 0>},
     {"stride_t512_u4_b4", 512, 4, 4, 0, &launch_probe<512, 4, 0>},
     {"stride_t256_u16_b4", 256, 16, 4, 0, &launch_probe<256, 16, 0>},
+    {"tile_t256_u8_b2", 256, 8, 2, 2, &launch_probe_tile<256, 8>},
+    {"tile_t512_u4_b2", 512, 4, 2, 2, &launch_probe_tile<512, 4>},
+    {"tile_t256_u8_b4", 256, 8, 4, 2, &launch_probe_tile<256, 8>},
+    {"tile_t512_u8_b1", 512, 8, 1, 2, &launch_probe_tile<512, 8>},
 };
 
 const ProbeVariant *probe_variants(int *count)
