@@ -135,12 +135,16 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
  * Families: 0 = rows of a warp (or of a fraction of one) streamed with a
  * rolling buffer of loads; 1 = row tiles: a group of threads requests a whole
  * row at once and a persistent grid walks consecutive rows in order;
- * 2 = element-wise kernel for layouts without 16-byte alignment.
+ * 2 = element-wise kernel for layouts without 16-byte alignment;
+ * 3 = bulk-copy pipeline: tiles of consecutive rows streamed into a ring of
+ * shared-memory stages by bulk async copies (rows_per_group = rows per stage,
+ * threads_per_row = consumer threads of the block, plus one producer warp).
  */
 typedef struct {
     int dtype;           /* gemv_dtype_t */
     int kind;            /* kernel family, see above */
-    int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1) */
+    int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1),
+                            the consumer threads of the block (family 3) */
     int rows_per_group;  /* rows one lane group streams together (family 0, x reuse) */
     int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread */
     int warps;           /* warps per block */

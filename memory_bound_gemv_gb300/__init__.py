@@ -37,7 +37,7 @@ class GemvError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
 
 
-KINDS = {0: "vec", 1: "tile", 2: "elem"}
+KINDS = {0: "vec", 1: "tile", 2: "elem", 3: "bulk"}
 
 
 class VariantInfo(ctypes.Structure):

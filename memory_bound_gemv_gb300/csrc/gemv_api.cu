@@ -142,6 +142,13 @@ gemv_status_t validate(int dtype, const void *A, const void *x, const float *y, 
 // Dynamic shared memory of variant v for a row of N columns.
 size_t smem_bytes(const Variant &v, int dtype, int64_t N)
 {
+    if (v.kind == KIND_BULK) {
+        const int64_t rb = row_bytes_of(dtype, N);
+        const BulkLayout L = bulk_layout(v.stages, v.rows_per_group, v.warps * 32, rb,
+                                         N * x_elem_bytes(dtype), (N + kGroup - 1) / kGroup,
+                                         dtype == DT_Q8 || dtype == DT_Q4);
+        return static_cast<size_t>(L.total);
+    }
     if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)
         return static_cast<size_t>(v.x_offset) + static_cast<size_t>(N) * x_elem_bytes(dtype);
     if (v.kind == KIND_TILE) return static_cast<size_t>(v.x_offset);
@@ -150,7 +157,7 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N)
 
 // Can variant v serve this call?
 bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void *A, const void *x,
-                  int64_t M, int64_t N)
+                  int64_t M, int64_t N, const uint16_t *scales)
 {
     if (v.xmode == XMODE_ELEM) {
         const int64_t blocks = (M + v.warps - 1) / v.warps;
@@ -160,6 +167,15 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
     if (rb % 16 || !aligned(A, 16) || !aligned(x, 16)) return false;
     if (rb / 16 > INT_MAX / 64) return false;
     if (static_cast<int64_t>(smem_bytes(v, dtype, N)) > d.max_smem) return false;
+    if (v.kind == KIND_BULK) {
+        // one stage (rows + their scales) is one transaction count of an mbarrier
+        const int64_t g = (N + kGroup - 1) / kGroup;
+        const bool quant = dtype == DT_Q8 || dtype == DT_Q4;
+        if (quant && ((2 * g) % 16 || !aligned(scales, 16))) return false;
+        const int64_t tx = v.rows_per_group * (rb + (quant ? 2 * g : 0));
+        if (tx >= (1 << 20)) return false;
+        return true;  // persistent grid
+    }
     if (v.kind == KIND_TILE) {
         // every row must be covered by one request per thread
         if (rb / 16 > static_cast<int64_t>(v.lanes_per_row) * v.unroll) return false;
@@ -206,7 +222,7 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
 // than one warp-wide pass of 512 bytes shares its warp with other rows) and
 // x in shared memory unless it is long.
 int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x, int64_t M,
-                   int64_t N)
+                   int64_t N, const uint16_t *scales)
 {
     int n = 0;
     const Variant *v = table(dtype, &n);
@@ -221,11 +237,11 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
         while (static_cast<int64_t>(g) * kTileChunks < chunks) g *= 2;
         const int warps = g > 256 ? g / 32 : 8;
         const int k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);
-        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N)) return k;
+        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales)) return k;
     }
     // Long rows or long x: warp per row with a rolling buffer, x through L1.
     int k = small_x ? find_variant(dtype, 32, XMODE_BULK) : find_variant(dtype, 32, XMODE_L1);
-    if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N))
+    if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N, scales))
         k = find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     return k;
 }
@@ -248,11 +264,11 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     DeviceState *d = current_device();
     if (!d) return GEMV_ERR_CUDA;
     if (vid < 0) {
-        vid = choose_variant(*d, dtype, A, x, M, N);
+        vid = choose_variant(*d, dtype, A, x, M, N, scales);
         if (vid < 0) return GEMV_ERR_UNSUPPORTED;
     }
     const Variant &v = tab[vid];
-    if (!variant_fits(v, *d, dtype, A, x, M, N)) return GEMV_ERR_UNSUPPORTED;
+    if (!variant_fits(v, *d, dtype, A, x, M, N, scales)) return GEMV_ERR_UNSUPPORTED;
 
     GemvArgs a{};
     a.A = A;
@@ -274,7 +290,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
         blocks = (M + v.warps - 1) / v.warps;
     } else {
         blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
-        if (v.kind == KIND_TILE) {
+        if (v.kind == KIND_TILE || v.kind == KIND_BULK) {
             const int resident = resident_blocks(*d, dtype, vid, v, smem);
             if (resident <= 0) return GEMV_ERR_CUDA;
             if (blocks > resident) blocks = resident;
@@ -347,7 +363,7 @@ int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int6
     if (!aligned(A, a_align(dtype)) || !aligned(x, x_align(dtype))) return -1;
     DeviceState *d = current_device();
     if (!d) return -1;
-    return choose_variant(*d, dtype, A, x, M, N);
+    return choose_variant(*d, dtype, A, x, M, N, nullptr);
 }
 
 gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,

@@ -1,4 +1,5 @@
 // Compiled variants of the f16 GEMV kernels.
+//   bulk_t<consumer threads>_r<rows per stage>_s<pipeline stages>
 //   tile_g<threads per row>_c<chunks per thread>_t<block threads>_<x staging>
 //   w<lanes per row>_r<rows per group>_u<loads in flight>_w<warps>_<x staging>
 #include "gemv_kernels.cuh"
@@ -6,6 +7,16 @@
 namespace mbg {
 
 static const Variant kTableF16[] = {
+    // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
+    MBG_BULK(DT_F16, 256, 1, 4, "bulk_t256_r1_s4"),
+    MBG_BULK(DT_F16, 256, 1, 3, "bulk_t256_r1_s3"),
+    MBG_BULK(DT_F16, 512, 1, 4, "bulk_t512_r1_s4"),
+    MBG_BULK(DT_F16, 256, 2, 4, "bulk_t256_r2_s4"),
+    MBG_BULK(DT_F16, 512, 2, 4, "bulk_t512_r2_s4"),
+    MBG_BULK(DT_F16, 256, 4, 4, "bulk_t256_r4_s4"),
+    MBG_BULK(DT_F16, 512, 4, 4, "bulk_t512_r4_s4"),
+    MBG_BULK(DT_F16, 256, 8, 3, "bulk_t256_r8_s3"),
+    MBG_BULK(DT_F16, 512, 8, 4, "bulk_t512_r8_s4"),
     // row tiles (the automatic choice for rows up to 512 * 8 * 16 bytes)
     MBG_TILE(DT_F16, 1, 8, 256, XMODE_BULK, "tile_g1_c8_t256_bulk"),
     MBG_TILE(DT_F16, 2, 8, 256, XMODE_BULK, "tile_g2_c8_t256_bulk"),

@@ -13,7 +13,7 @@ enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3 };
 
 // Kernel families: warp/sub-warp rows streamed with a rolling buffer, row
 // tiles walked by a persistent grid, element-wise fallback.
-enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2 };
+enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3 };
 
 // Dot-product arithmetic: operands converted to FP32, or binary16 operands
 // fed to mixed-precision FMAs with FP32 accumulation.
@@ -61,9 +61,35 @@ struct Variant {
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
+        if (kind == KIND_BULK) return rows_per_group;
         return warps * (32 / lanes_per_row) * rows_per_group;
     }
 };
+
+// Shared-memory layout of the bulk-pipeline kernel (host and device agree on
+// it): S "full" and S "reduced" barriers, the x barrier and the abort flag,
+// one set of warp partials per stage, x, S stages of RS rows of A, and
+// (quantised) S stages of RS rows of scales.  T counts consumer threads.
+struct BulkLayout {
+    int part, x, stage, scale, total;   // byte offsets and total size
+    int stage_bytes, scale_bytes;       // capacity of one stage
+};
+
+__host__ __device__ inline int round16(int64_t v) { return static_cast<int>((v + 15) / 16 * 16); }
+
+__host__ __device__ inline BulkLayout bulk_layout(int S, int RS, int T, int64_t row_bytes,
+                                                  int64_t x_bytes, int64_t groups, bool quant)
+{
+    BulkLayout L;
+    L.part = round16(8 * (2 * S + 1) + 4);
+    L.x = L.part + round16(static_cast<int64_t>(S) * (T / 32) * RS * 4);
+    L.stage = L.x + round16(x_bytes);
+    L.stage_bytes = static_cast<int>(RS * row_bytes);
+    L.scale = L.stage + S * L.stage_bytes;
+    L.scale_bytes = quant ? round16(RS * 2 * groups) : 0;
+    L.total = L.scale + S * L.scale_bytes;
+    return L;
+}
 
 // Variant tables, one per storage type (defined in gemv_<dtype>.cu).
 const Variant *variants_f32(int *count);

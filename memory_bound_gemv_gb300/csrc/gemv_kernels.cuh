@@ -306,6 +306,194 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy pipeline kernel (warp-specialised)
+// ---------------------------------------------------------------------------
+//
+// A tile of RS consecutive rows is one contiguous byte range of A, so one
+// bulk async copy (cp.async.bulk, completion counted on an mbarrier) moves a
+// whole tile into shared memory.  Each block of the persistent grid keeps S
+// tiles in flight in a ring of stages: memory-level parallelism comes from
+// the copy engine, not from registers, and the tiles in flight across the
+// grid form one dense band of consecutive rows.
+//
+// Warp roles.  T/32 consumer warps wait on a stage's "full" barrier, read the
+// tile from shared memory (thread t takes chunks t, t+T, ... of every row of
+// the tile and loads each x chunk once for all RS rows), reduce their partial
+// sums per row with an XOR butterfly, store one partial per warp and row, and
+// arrive on the stage's "reduced" barrier.  One producer warp waits on
+// "reduced", adds the warp partials of each row, writes y and refills the
+// stage with the tile S positions ahead.  No block-wide barrier sits in the
+// loop, so consumer warps never wait for one another.  Quantised tiles bring
+// their rows' scales along in a second bulk copy on the same barrier.
+//
+// Every wait is bounded.  A thread whose wait gives up reports the status
+// word and raises the block's abort flag; every warp then leaves its loop
+// (each decision made warp-uniform first), and the producer first waits
+// (bounded) for the copies it still has in flight, so no copy can land in
+// shared memory after the block has exited.
+template <int DT, int T, int RS, int S, int MATH>
+__global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
+{
+    using F = Fmt<DT>;
+    constexpr int XCB = x_chunk_bytes<DT>();
+    constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int NW = T / 32;  // consumer warps
+    constexpr int CPG = kGroup / F::EPC;
+    static_assert(MATH == MATH_F32 || DT != DT_F32, "FP32 weights use FP32 math");
+    static_assert(NW <= 32, "the producer warp adds one partial per consumer warp");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nchunks = p.nchunks;
+    const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
+    const BulkLayout L = bulk_layout(S, RS, T, p.row_bytes, xbytes, p.groups, F::QUANT);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *red = full + S;
+    uint64_t *xbar = red + S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(xbar + 1);
+    float *part = reinterpret_cast<float *>(smem + L.part);
+    const unsigned char *xs = smem + L.x;
+    const int64_t ntiles = (p.M + RS - 1) / RS;
+    const int64_t grid = gridDim.x;
+    // iterations of this block: tiles blockIdx.x, blockIdx.x + grid, ...
+    const int64_t iters = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / grid + 1 : 0;
+
+    auto issue = [&](int64_t it) {
+        const int slot = static_cast<int>(it % S);
+        const int64_t r0 = (blockIdx.x + it * grid) * RS;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
+        const uint32_t bytes = static_cast<uint32_t>(rows * p.row_bytes);
+        const uint32_t sbytes = F::QUANT ? static_cast<uint32_t>(rows * 2 * p.groups) : 0u;
+        const uint32_t b = smem_addr(&full[slot]);
+        mbar_arrive_expect_tx(b, bytes + sbytes);
+        bulk_copy_g2s(smem_addr(smem + L.stage + slot * L.stage_bytes),
+                      static_cast<const unsigned char *>(p.A) + r0 * p.row_bytes, bytes, b);
+        if constexpr (F::QUANT)
+            bulk_copy_g2s(smem_addr(smem + L.scale + slot * L.scale_bytes), p.scales + r0 * p.groups,
+                          sbytes, b);
+    };
+    auto fail = [&]() {
+        report_error(p.err, DEVERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&red[s]), NW);
+        }
+        mbar_init(smem_addr(xbar), 1);
+        *abort_flag = 0;
+    }
+    __syncthreads();
+
+    if (warp == NW) {
+        // ---------------- producer warp ----------------
+        int64_t issued = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
+            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
+            for (; issued < S && issued < iters; ++issued) issue(issued);
+        }
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        int64_t done = 0;
+        for (; done < iters; ++done) {
+            const int slot = static_cast<int>(done % S);
+            bool ok = mbar_wait_bounded(smem_addr(&red[slot]), static_cast<uint32_t>((done / S) & 1),
+                                        p.wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ok) && !__any_sync(0xffffffffu, *abort_flag != 0);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) fail();
+                break;
+            }
+            const int64_t r0 = (blockIdx.x + done * grid) * RS;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
+            const float *pp = part + slot * NW * RS;
+#pragma unroll
+            for (int r = 0; r < RS; ++r) {
+                float v = lane < NW ? pp[lane * RS + r] : 0.f;
+                v = group_sum<32>(v);
+                if (lane == 0 && r < rows) p.y[r0 + r] = v;
+            }
+            __syncwarp();
+            if (lane == 0 && issued < iters) issue(issued);
+            ++issued;
+            if (issued > iters) issued = iters;
+        }
+        if (lane == 0) {
+            // copies issued for iterations [done, issued) may still be in flight
+            for (int64_t j = done; j < issued; ++j)
+                mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
+                                  p.wait_limit_ns);
+            if (*abort_flag) {
+                // the x copy, too, may still be in flight
+                if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    // (every exit decision is made warp-uniform before the warp's shuffles)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns))) {
+        if (lane == 0) fail();
+        return;
+    }
+    for (int64_t it = 0; it < iters; ++it) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
+        const int slot = static_cast<int>(it % S);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]),
+                                                        static_cast<uint32_t>((it / S) & 1),
+                                                        p.wait_limit_ns))) {
+            if (lane == 0) fail();
+            return;
+        }
+        const int64_t r0 = (blockIdx.x + it * grid) * RS;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
+        const unsigned char *st = smem + L.stage + slot * L.stage_bytes;
+        const uint16_t *ss = reinterpret_cast<const uint16_t *>(smem + L.scale + slot * L.scale_bytes);
+        float acc[RS][NACC];
+#pragma unroll
+        for (int r = 0; r < RS; ++r)
+#pragma unroll
+            for (int k = 0; k < NACC; ++k) acc[r][k] = 0.f;
+#pragma unroll 2
+        for (int c = tid; c < nchunks; c += T) {
+            uint4 xv[XV];
+#pragma unroll
+            for (int v = 0; v < XV; ++v)
+                xv[v] = *reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(c) * XCB + 16 * v);
+            float xf[MATH == MATH_F32 ? F::EPC : 1];
+            if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
+#pragma unroll
+            for (int r = 0; r < RS; ++r) {
+                if (r < rows) {
+                    const uint4 a =
+                        *reinterpret_cast<const uint4 *>(st + r * p.row_bytes + static_cast<size_t>(c) * 16);
+                    float sc = 0.f;
+                    if constexpr (F::QUANT) sc = __half2float(__ushort_as_half(ss[r * p.groups + c / CPG]));
+                    if constexpr (MATH == MATH_MIXED) {
+                        chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
+                    } else {
+                        float wf[F::EPC];
+                        chunk_to_float<DT>(a, wf);
+                        chunk_fma<DT>(wf, xf, sc, acc[r]);
+                    }
+                }
+            }
+        }
+        float *pp = part + slot * NW * RS;
+#pragma unroll
+        for (int r = 0; r < RS; ++r) {
+            float v = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+            v = group_sum<32>(v);
+            if (lane == 0) pp[warp * RS + r] = v;
+        }
+        if (lane == 0) mbar_arrive(smem_addr(&red[slot]));
+    }
+}
+
 template <int DT, int G, int CPT, int T>
 constexpr int tile_x_offset()
 {
@@ -415,6 +603,33 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
 // FP32 weights use FP32 arithmetic; the other types default to the mixed path.
 #define MBG_TILE(DT, G, CPT, T, XM, NAME) \
     MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
+
+template <int DT, int T, int RS, int S, int MATH>
+void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+{
+    gemv_bulk_kernel<DT, T, RS, S, MATH><<<grid, T + 32, smem, s>>>(a);
+}
+
+template <int DT, int T, int RS, int S, int MATH>
+cudaError_t smem_limit_bulk(int bytes)
+{
+    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DT, int T, int RS, int S, int MATH>
+cudaError_t occupancy_bulk(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH>,
+                                                         T + 32, smem);
+}
+
+#define MBG_BULK_M(DT, T, RS, S, MATH, NAME)                                                    \
+    Variant{DT, T, RS, 1, T / 32, XMODE_BULK, NAME, &launch_bulk<DT, T, RS, S, MATH>,            \
+            &smem_limit_bulk<DT, T, RS, S, MATH>, KIND_BULK, 0, &occupancy_bulk<DT, T, RS, S, MATH>, \
+            MATH, S}
+#define MBG_BULK(DT, T, RS, S, NAME) \
+    MBG_BULK_M(DT, T, RS, S, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -213,9 +213,10 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     bulk = [v["id"] for v in mbg.variants(dtype) if v["xmode"] == "bulk" and v["kind"] == "vec"][0]
     tile = [v["id"] for v in mbg.variants(dtype) if v["xmode"] == "bulk" and v["kind"] == "tile"
             and v["threads_per_row"] == 128][0]
+    pipe = [v["id"] for v in mbg.variants(dtype) if v["kind"] == "bulk"][0]
     assert mbg.gemv_get_device_error() == mbg.OK
     y_ref, den = reference(dtype, inp, M, N)
-    for vid in (bulk, tile):
+    for vid in (bulk, tile, pipe):
         try:
             mbg.debug_set_wait_limit_ns(2_000_000)  # 2 ms
             mbg.debug_skip_x_copy(True)             # nothing is copied: the wait must run out
