@@ -187,6 +187,33 @@ template <> struct Fmt<DT_Q4> {
 template <int DT> constexpr int x_chunk_bytes() { return Fmt<DT>::EPC * Fmt<DT>::XB; }
 template <int DT> constexpr int x_chunk_vecs() { return x_chunk_bytes<DT>() / 16; }
 
+// x in shared memory is kept vector-major: 16-byte vector v of chunk c sits at
+// byte (v * nchunks + c) * 16.  Lane t of a warp reading vector v of chunk t
+// then touches consecutive 16-byte slots, free of bank conflicts, whatever
+// the number of vectors per chunk (INT4 needs four: 32 binary16 values of x
+// per 16 bytes of A; read chunk-major they would be 64 bytes apart per lane,
+// a 16-way conflict).  For FP32 and FP16 (one vector per chunk) this is
+// simply x in its own order, so a plain bulk copy stages it.
+__device__ __forceinline__ const uint4 *x_smem_vec(const unsigned char *xs, int nchunks, int c, int v)
+{
+    return reinterpret_cast<const uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16);
+}
+
+// Cooperative staging of x into the vector-major layout by threads
+// t = 0 .. nt-1 (reads are coalesced in x's own order).
+template <int DT>
+__device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x, int nchunks, int t,
+                                               int nt)
+{
+    constexpr int XV = x_chunk_vecs<DT>();
+    const uint4 *src = static_cast<const uint4 *>(x);
+    for (int i = t; i < nchunks * XV; i += nt) {
+        const int c = i / XV;
+        const int v = i - c * XV;
+        *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = ld_cached16(src + i);
+    }
+}
+
 // x chunk (as raw 16-byte vectors) -> floats.
 template <int DT>
 __device__ __forceinline__ void x_to_float(const uint4 (&xv)[x_chunk_vecs<DT>()],

@@ -48,7 +48,11 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
     const int nchunks = p.nchunks;
     const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
 
-    if constexpr (XMODE == XMODE_BULK) {
+    // x staging: one bulk copy when x is in its own order in shared memory
+    // (one vector per chunk), a cooperative transposing load otherwise.
+    constexpr bool XBULK = XMODE == XMODE_BULK && XV == 1;
+    constexpr bool XCOOP = (XMODE == XMODE_BULK && XV > 1) || XMODE == XMODE_VEC;
+    if constexpr (XBULK) {
         if (threadIdx.x == 0) {
             const uint32_t b = smem_addr(bar);
             mbar_init(b, 1);
@@ -88,13 +92,9 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
         }
     }
 
-    if constexpr (XMODE == XMODE_VEC) {
-        const uint4 *src = static_cast<const uint4 *>(p.x);
-        uint4 *dst = reinterpret_cast<uint4 *>(xs);
-        for (uint32_t i = threadIdx.x; i < xbytes / 16; i += WARPS * 32) dst[i] = ld_cached16(src + i);
-    }
+    if constexpr (XCOOP) stage_x_vmajor<DT>(xs, p.x, nchunks, threadIdx.x, WARPS * 32);
     if constexpr (XMODE == XMODE_BULK || XMODE == XMODE_VEC) __syncthreads();
-    if constexpr (XMODE == XMODE_BULK) {
+    if constexpr (XBULK) {
         if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
             if (threadIdx.x == 0) report_error(p.err, DEVERR_TIMEOUT);
             // A copy that was issued may still land: give it one more bounded
@@ -121,9 +121,10 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
                 uint4 xv[XV];
 #pragma unroll
                 for (int v = 0; v < XV; ++v) {
-                    const unsigned char *px = xsrc + static_cast<size_t>(c) * XCB + 16 * v;
-                    if constexpr (XMODE == XMODE_L1) xv[v] = ld_cached16(px);
-                    else xv[v] = *reinterpret_cast<const uint4 *>(px);
+                    if constexpr (XMODE == XMODE_L1)
+                        xv[v] = ld_cached16(xsrc + static_cast<size_t>(c) * XCB + 16 * v);
+                    else
+                        xv[v] = *x_smem_vec(xsrc, nchunks, c, v);
                 }
                 float xf[EPC];
                 x_to_float<DT>(xv, xf);
@@ -210,7 +211,11 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     const int64_t ntiles = (p.M + RT - 1) / RT;
     const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
 
-    if constexpr (XMODE == XMODE_BULK) {
+    // x staging: one bulk copy when x is in its own order in shared memory
+    // (one vector per chunk), a cooperative transposing load otherwise.
+    constexpr bool XBULK = XMODE == XMODE_BULK && XV == 1;
+    constexpr bool XCOOP = XMODE == XMODE_BULK && XV > 1;
+    if constexpr (XBULK) {
         if (tid == 0) {
             const uint32_t b = smem_addr(bar);
             mbar_init(b, 1);
@@ -241,8 +246,9 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     int64_t tile = blockIdx.x;
     if (tile < ntiles) load_tile(tile, cur, scur);
 
-    if constexpr (XMODE == XMODE_BULK) {
-        __syncthreads();
+    if constexpr (XCOOP) stage_x_vmajor<DT>(xs, p.x, nchunks, tid, T);
+    if constexpr (XMODE == XMODE_BULK) __syncthreads();
+    if constexpr (XBULK) {
         if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
             if (tid == 0) report_error(p.err, DEVERR_TIMEOUT);
             if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns);
@@ -267,9 +273,10 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
                     uint4 xv[XV];
 #pragma unroll
                     for (int v = 0; v < XV; ++v) {
-                        const unsigned char *px = xsrc + static_cast<size_t>(c) * XCB + 16 * v;
-                        if constexpr (XMODE == XMODE_L1) xv[v] = ld_cached16(px);
-                        else xv[v] = *reinterpret_cast<const uint4 *>(px);
+                        if constexpr (XMODE == XMODE_L1)
+                            xv[v] = ld_cached16(xsrc + static_cast<size_t>(c) * XCB + 16 * v);
+                        else
+                            xv[v] = *x_smem_vec(xsrc, nchunks, c, v);
                     }
                     if constexpr (MATH == MATH_MIXED) {
                         chunk_dot_mixed<DT>(cur[k], xv, F::QUANT ? scur[k] : 0.f, acc);
@@ -392,8 +399,10 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         // ---------------- producer warp ----------------
         int64_t issued = 0;
         if (lane == 0) {
-            mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
-            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
+            if constexpr (XV == 1) {
+                mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
+                if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
+            }
             for (; issued < S && issued < iters; ++issued) issue(issued);
         }
         issued = __shfl_sync(0xffffffffu, issued, 0);
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
             for (int64_t j = done; j < issued; ++j)
                 mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
                                   p.wait_limit_ns);
-            if (*abort_flag) {
+            if (XV == 1 && *abort_flag) {
                 // the x copy, too, may still be in flight
                 if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns);
             }
@@ -436,9 +445,16 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 
     // ---------------- consumer warps ----------------
     // (every exit decision is made warp-uniform before the warp's shuffles)
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns))) {
-        if (lane == 0) fail();
-        return;
+    if constexpr (XV == 1) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns))) {
+            if (lane == 0) fail();
+            return;
+        }
+    } else {
+        // several vectors of x per chunk: transpose x into shared memory,
+        // then a named barrier of the consumer warps only
+        stage_x_vmajor<DT>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T);
+        asm volatile("bar.sync 1, %0;" ::"r"(T) : "memory");
     }
     for (int64_t it = 0; it < iters; ++it) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
@@ -462,8 +478,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         for (int c = tid; c < nchunks; c += T) {
             uint4 xv[XV];
 #pragma unroll
-            for (int v = 0; v < XV; ++v)
-                xv[v] = *reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(c) * XCB + 16 * v);
+            for (int v = 0; v < XV; ++v) xv[v] = *x_smem_vec(xs, nchunks, c, v);
             float xf[MATH == MATH_F32 ? F::EPC : 1];
             if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
