@@ -508,7 +508,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": recorded_traffic(w.name, vinfo["name"]),
-                "kernel": f"gemv_vec_kernel {vinfo['name']}"}
+                "kernel": f"gemv_{vinfo['kind']}_kernel {vinfo['name']}"}
     clocks = sampler.summary() if sampler is not None else {"sm_mhz": None, "note": "disabled"}
 
     cpu = None
@@ -577,9 +577,17 @@ def run_profile(args):
     A = torch.from_numpy(inp["A"].view(np.float16) if w.dtype == "f16" else inp["A"]).cuda()
     x = torch.from_numpy(inp["x"] if w.dtype == "f32" else inp["x"].view(np.float16)).cuda()
     S = torch.from_numpy(inp["scales"].view(np.float16)).cuda() if w.quantised else None
-    y = mbg.gemv(w.dtype, A, x, S)
+    if args.variant:
+        vid = [v["id"] for v in mbg.variants(w.dtype) if v["name"] == args.variant]
+        if not vid:
+            raise SystemExit(f"no variant {args.variant!r} for {w.dtype}")
+        vid = vid[0]
+        y = mbg.gemv_run_variant(w.dtype, vid, A, x, S)
+    else:
+        vid = mbg.select_variant(w.dtype, A, x)
+        y = mbg.gemv(w.dtype, A, x, S)
     torch.cuda.synchronize()
-    print(json.dumps({"profile": w.name, "variant": mbg.variants(w.dtype)[mbg.select_variant(w.dtype, A, x)]["name"],
+    print(json.dumps({"profile": w.name, "variant": mbg.variants(w.dtype)[vid]["name"],
                       "y0": float(y[0].item())}))
     return 0
 
@@ -602,6 +610,7 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile", action="store_true", help="one launch of the GEMV, for ncu")
+    p.add_argument("--variant", default=None, help="kernel variant name for --profile")
     p.add_argument("--json-out", default=None)
     args = p.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:

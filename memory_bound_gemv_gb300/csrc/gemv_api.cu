@@ -217,10 +217,14 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
     return -1;
 }
 
-// The automatic choice: element-wise kernel for layouts the vector kernels
-// cannot take; otherwise lanes per row from the row length (a row shorter
-// than one warp-wide pass of 512 bytes shares its warp with other rows) and
-// x in shared memory unless it is long.
+// The automatic choice (measured on GB300 over the workload families):
+// - layouts the vector kernels cannot take: element-wise kernel;
+// - INT8: the bulk-copy pipeline, with about 16 KB of rows per stage;
+// - otherwise row tiles with the narrowest group that requests a whole row at
+//   once; x through L1 for groups of 128 threads or more (FP32/FP16 rows of
+//   at least 8 KB), in shared memory below that;
+// - rows too long for a tile, or x too long for shared memory: warp per row
+//   with a rolling buffer.
 int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x, int64_t M,
                    int64_t N, const uint16_t *scales)
 {
@@ -231,15 +235,25 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if (!vec_ok) return find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     const int64_t chunks = rb / 16;
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
-    // Row tiles: the narrowest group that requests a whole row at once.
+    if (dtype == DT_Q8 && small_x) {
+        int rs = 1;
+        while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
+        for (int k = 0; k < n; ++k) {
+            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == 8 &&
+                variant_fits(v[k], d, dtype, A, x, M, N, scales))
+                return k;
+        }
+    }
     if (small_x && chunks <= static_cast<int64_t>(kTileMaxThreads) * kTileChunks) {
         int g = 1;
         while (static_cast<int64_t>(g) * kTileChunks < chunks) g *= 2;
         const int warps = g > 256 ? g / 32 : 8;
-        const int k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);
+        const bool via_l1 = (dtype == DT_F32 || dtype == DT_F16) && g >= 128;
+        int k = find_variant(dtype, g, via_l1 ? XMODE_L1 : XMODE_BULK, KIND_TILE, warps);
+        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales)) return k;
+        k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);
         if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales)) return k;
     }
-    // Long rows or long x: warp per row with a rolling buffer, x through L1.
     int k = small_x ? find_variant(dtype, 32, XMODE_BULK) : find_variant(dtype, 32, XMODE_L1);
     if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N, scales))
         k = find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
