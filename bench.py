@@ -363,8 +363,8 @@ def run_ours(args):
     vid = mbg.select_variant(w.dtype, A0, x)
     vinfo = mbg.variants(w.dtype)[vid]
 
-    def launch(i):
-        mbg.gemv(w.dtype, As[i % copies], x, Ss[i % copies], y=y)
+    def launch(i, overlap=False):
+        mbg.gemv(w.dtype, As[i % copies], x, Ss[i % copies], y=y, overlap=overlap)
 
     # first launch: keep the result for the parity sample of the cpu_baseline leg
     with torch.cuda.stream(stream):
@@ -451,6 +451,40 @@ def run_ours(args):
     per_launch = elapsed / max(1, args.steps)
     value = gbs(world * args.steps * step_bytes, t_max)
 
+    # ---- the same chain launched with programmatic dependent launch ----
+    # (gemv_ex with GEMV_FLAG_OVERLAP_PRECEDING: each launch may start while
+    # the previous one finishes; weights are never written by the chain)
+    overlap = None
+    if not args.no_overlap and n_full > 0:
+        g_ov = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(copies):
+                launch(i, overlap=True)
+        stream.synchronize()
+        with torch.cuda.graph(g_ov, stream=stream):
+            for i in range(batch):
+                launch(i, overlap=True)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, w_full)):
+                g_ov.replay()
+        stream.synchronize()
+        barrier()
+        with torch.cuda.stream(stream):
+            o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            o0.record(stream)
+            for _ in range(n_full):
+                g_ov.replay()
+            o1.record(stream)
+        o1.synchronize()
+        barrier()
+        ov_t = max_over_ranks(o0.elapsed_time(o1) * 1e-3, dev)
+        ov_steps = n_full * batch
+        overlap = {"value": gbs(world * ov_steps * step_bytes, ov_t), "unit": "GB/s", "steps": ov_steps,
+                   "ms_per_step": ov_t / ov_steps * 1e3,
+                   "how": "same graph of back-to-back launches, each launched with programmatic "
+                          "dependent launch (weights requested before waiting for the previous launch)"}
+        del g_ov
+
     # ---- the same launches without graphs (host-launched stream), for context ----
     eager_steps = min(args.steps, 2000)
     with torch.cuda.stream(stream):
@@ -468,6 +502,8 @@ def run_ours(args):
     probe_all = {k: max(probe_before[k], probe_after[k]) for k in probe_before}
     best_probe = max(probe_all, key=probe_all.get)
     ceiling = probe_all[best_probe]
+    if overlap is not None:
+        overlap["mbu_probe_pct"] = 100.0 * overlap["value"] / world / ceiling
 
     # ---- end to end: x from pinned host memory, y back to pinned host memory ----
     e2e = None
@@ -551,6 +587,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "eager_stream_gbs": eager_gbs,
+        "overlap": overlap,
         "ms_per_launch": per_launch * 1e3,
     }
     if rank == 0:
@@ -609,6 +646,7 @@ def main(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-overlap", action="store_true")
     p.add_argument("--profile", action="store_true", help="one launch of the GEMV, for ncu")
     p.add_argument("--variant", default=None, help="kernel variant name for --profile")
     p.add_argument("--json-out", default=None)

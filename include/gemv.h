@@ -100,6 +100,29 @@ gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, 
                       const uint16_t *scales, void *stream);
 
 /*
+ * Any of the four GEMVs (dtype: gemv_dtype_t) with launch flags.  scales is
+ * ignored for FP32/FP16.
+ *
+ * GEMV_FLAG_OVERLAP_PRECEDING: the caller guarantees that A and scales are
+ * not written by the kernel that precedes this call on `stream` (model
+ * weights in a decode loop are the intended case).  The GEMV is then launched
+ * with programmatic dependent launch: its blocks may start while the
+ * preceding kernel is still running and begin streaming A and scales at once;
+ * they read x and write y only after the preceding kernel has completed and
+ * its memory is visible (griddepcontrol.wait).  Every GEMV kernel of this
+ * library signals early that its successor may start, so a chain of GEMVs on
+ * one stream overlaps each launch's start-up with the previous one's tail.
+ * Kernel families without this support are launched normally.  Any other flag
+ * bit returns GEMV_ERR_INVALID_VALUE.
+ * Launch overlap as described for NVIDIA's programmatic dependent launch;
+ * the pages have no counterpart (their kernels are timed one launch at a time,
+ * "membound", "Results").
+ */
+#define GEMV_FLAG_OVERLAP_PRECEDING 1u
+gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, unsigned flags, void *stream);
+
+/*
  * Pure-read bandwidth probe: streams buf[0..bytes) once with the same
  * 16-byte read-only loads the GEMV kernels use and folds every word into
  * *sink with XOR (so no load is dead code).  bytes must be a multiple of 16

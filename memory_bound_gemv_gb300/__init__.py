@@ -64,6 +64,7 @@ def _declare(L):
         "gemv_variant_info": [i32, i32, ctypes.POINTER(VariantInfo)],
         "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
         "gemv_get_device_error": [vp],
+        "gemv_ex": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -212,8 +213,32 @@ def gemv_q4(A, x, scales, y=None, stream=None):
     return _quant("gemv_q4", Q4, A, x, scales, y, stream)
 
 
-def gemv(dtype: str, A, x, scales=None, y=None, stream=None):
+FLAG_OVERLAP_PRECEDING = 1
+
+
+def gemv_ex(dtype: str, A, x, scales=None, y=None, stream=None, flags: int = 0):
+    """Any GEMV with launch flags (``FLAG_OVERLAP_PRECEDING``: A and scales are
+    not written by the kernel just before this call on the stream)."""
+    torch = _torch()
+    dt = DTYPES[dtype]
+    M, N = _mn(A, dt)
+    a_types = {F32: (torch.float32,), F16: _f16_types(), Q8: (torch.int8,), Q4: (torch.uint8,)}[dt]
+    _check(A, "A", a_types, tuple(A.shape))
+    _check(x, "x", (torch.float32,) if dt == F32 else _f16_types(), (N,), A.device)
+    s_ptr = None
+    if dt in (Q8, Q4):
+        _check(scales, "scales", _f16_types(), (M, (N + GROUP - 1) // GROUP), A.device)
+        s_ptr = scales.data_ptr()
+    y = _out(y, M, A.device)
+    _raise(lib().gemv_ex(dt, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, s_ptr, flags,
+                         _stream_ptr(stream)), "gemv_ex")
+    return y
+
+
+def gemv(dtype: str, A, x, scales=None, y=None, stream=None, overlap: bool = False):
     """Dispatch on the storage type name: 'f32', 'f16', 'q8', 'q4'."""
+    if overlap:
+        return gemv_ex(dtype, A, x, scales, y, stream, FLAG_OVERLAP_PRECEDING)
     if dtype == "f32":
         return gemv_f32(A, x, y, stream)
     if dtype == "f16":

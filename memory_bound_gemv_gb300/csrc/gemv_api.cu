@@ -261,7 +261,7 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
 }
 
 gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, int64_t M, int64_t N,
-                  const uint16_t *scales, void *stream)
+                  const uint16_t *scales, void *stream, unsigned flags = 0)
 {
     gemv_status_t st = validate(dtype, A, x, y, M, N, scales);
     if (st != GEMV_OK) return st;
@@ -297,6 +297,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     a.err = d->status;
     a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     a.skip_x_copy = g_skip_x_copy.load(std::memory_order_relaxed);
+    a.pdl = ((flags & GEMV_FLAG_OVERLAP_PRECEDING) && v.supports_pdl()) ? 1 : 0;
 
     int64_t blocks;
     const size_t smem = smem_bytes(v, dtype, N);
@@ -310,7 +311,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
             if (blocks > resident) blocks = resident;
         }
     }
-    v.launch(a, static_cast<unsigned>(blocks), smem, s);
+    v.launch(a, static_cast<unsigned>(blocks), smem, s, a.pdl != 0);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
 }
@@ -343,6 +344,13 @@ gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, 
                       const uint16_t *scales, void *stream)
 {
     return run(DT_Q4, -1, A, x, y, M, N, scales, stream);
+}
+
+gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t M, int64_t N,
+                      const uint16_t *scales, unsigned flags, void *stream)
+{
+    if (flags & ~static_cast<unsigned>(GEMV_FLAG_OVERLAP_PRECEDING)) return GEMV_ERR_INVALID_VALUE;
+    return run(dtype, -1, A, x, y, M, N, scales, stream, flags);
 }
 
 int gemv_variant_count(int dtype)

@@ -52,6 +52,14 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (if it was launched with programmatic serialisation) start its
+// blocks while this grid still runs; wait blocks until the preceding grid has
+// finished and its memory operations are visible.  Both are no-ops for
+// kernels launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report_error(unsigned int *err, unsigned int code)
 {
     if (err) atomicOr(err, code);

@@ -25,6 +25,12 @@ enum : unsigned int { DEVERR_TIMEOUT = 1u };
 // Columns per FP16 scale in the quantised formats.
 constexpr int kGroup = 128;
 
+// Row tiles whose warp partials are combined behind one block barrier.  One:
+// the barrier after every tile keeps a block's warps in step, so each block
+// requests its next tile as one dense unit; batching 8 tiles per barrier let
+// the warps drift apart and measured 5-25 % slower on GB300.
+constexpr int kTileBatch = 1;
+
 struct GemvArgs {
     const void *A;            // weights, row-major, row pitch `row_bytes`
     const void *x;            // input vector
@@ -38,6 +44,8 @@ struct GemvArgs {
     unsigned int *err;        // device status word
     uint64_t wait_limit_ns;   // bound of every device-side wait
     int skip_x_copy;          // test hook: arm the barrier but issue no copy
+    int pdl;                  // launched with programmatic serialisation: stream the
+                              // weights before waiting for the preceding kernel
 };
 
 struct Variant {
@@ -49,7 +57,7 @@ struct Variant {
     int xmode;
     const char *name;
     // Launches the kernel on `grid` blocks with `smem` bytes of dynamic shared memory.
-    void (*launch)(const GemvArgs &, unsigned grid, size_t smem, cudaStream_t);
+    void (*launch)(const GemvArgs &, unsigned grid, size_t smem, cudaStream_t, bool pdl);
     // Raises the kernel's dynamic shared memory limit.
     cudaError_t (*set_smem_limit)(int bytes);
     int kind;
@@ -58,6 +66,7 @@ struct Variant {
     cudaError_t (*occupancy)(int *blocks, size_t smem);
     int math;            // MATH_F32 or MATH_MIXED
     int stages;          // bulk-pipeline depth (KIND_BULK)
+    bool supports_pdl() const { return kind == KIND_TILE || kind == KIND_BULK; }
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
     unsigned char *xs = smem + 16;
 
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t = lane % LPR;
@@ -175,8 +176,8 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
 // loads in flight therefore cover a dense band of consecutive rows, which is
 // how HBM3e delivers its bandwidth (scattered per-warp streams reach far
 // less).  Lane partials are summed with an XOR butterfly; groups wider than a
-// warp combine their warps' partials through shared memory (double-buffered,
-// one block barrier per tile: every thread of a block walks the same tiles)
+// warp combine their warps' partials through shared memory, one block barrier
+// per batch of tiles (every thread of a block walks the same tiles)
 // ("llama.cpp GEMV CUDA": a block-wide row with a warp reduction, warp sums
 // in shared memory and a second warp reduction).
 template <int DT, int G, int CPT, int T, int XMODE, int MATH>
@@ -191,7 +192,9 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     constexpr int GW = WIDE ? G / 32 : 1;           // warps per group
     constexpr int LW = WIDE ? 32 : G;               // shuffle width
     constexpr int CHUNKS_PER_GROUP = kGroup / EPC;
-    constexpr int PART_BYTES = WIDE ? 2 * (T / 32) * 4 : 0;
+    constexpr int NW = T / 32;
+    constexpr int KB = kTileBatch;                  // tiles per deferred reduction
+    constexpr int PART_BYTES = WIDE ? 2 * KB * NW * 4 : 0;
     constexpr int X_OFFSET = (16 + PART_BYTES + 15) / 16 * 16;
     static_assert(T % G == 0 && (G <= 32 ? 32 % G == 0 : G % 32 == 0), "group shape");
     static_assert(XMODE == XMODE_BULK || XMODE == XMODE_L1, "xmode");
@@ -215,13 +218,21 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     // (one vector per chunk), a cooperative transposing load otherwise.
     constexpr bool XBULK = XMODE == XMODE_BULK && XV == 1;
     constexpr bool XCOOP = XMODE == XMODE_BULK && XV > 1;
-    if constexpr (XBULK) {
+    // With programmatic dependent launch the first tile of weights is
+    // requested before waiting for the preceding kernel; x is read and y
+    // written only after that wait.
+    pdl_trigger();
+    const bool pdl = p.pdl != 0;
+    auto stage_x_bulk = [&]() {
         if (tid == 0) {
             const uint32_t b = smem_addr(bar);
             mbar_init(b, 1);
             mbar_arrive_expect_tx(b, xbytes);
             if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
         }
+    };
+    if constexpr (XBULK) {
+        if (!pdl) stage_x_bulk();
     }
 
     uint4 cur[CPT], nxt[CPT];
@@ -245,6 +256,10 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 
     int64_t tile = blockIdx.x;
     if (tile < ntiles) load_tile(tile, cur, scur);
+    if (pdl) {
+        pdl_wait();
+        if constexpr (XBULK) stage_x_bulk();
+    }
 
     if constexpr (XCOOP) stage_x_vmajor<DT>(xs, p.x, nchunks, tid, T);
     if constexpr (XMODE == XMODE_BULK) __syncthreads();
@@ -257,7 +272,26 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     }
     const unsigned char *xsrc = (XMODE == XMODE_L1) ? static_cast<const unsigned char *>(p.x) : xs;
 
-    int parity = 0;
+    // Groups wider than a warp leave one partial per warp and tile in shared
+    // memory; every KB tiles (kTileBatch) one block barrier makes a batch
+    // visible and the warps finish those rows (two batch buffers alternate, so
+    // the next batch can be written while the previous one is read).
+    int half = 0, fill = 0;
+    int64_t batch_tile0 = tile;
+    auto flush = [&](int count) {
+        __syncthreads();
+        const float *pb = part + half * KB * NW;
+        for (int e = warp; e < count * RT; e += NW) {
+            const int k = e / RT, g = e - k * RT;
+            const int64_t r = (batch_tile0 + static_cast<int64_t>(k) * gridDim.x) * RT + g;
+            float v = lane < GW ? pb[k * NW + g * GW + lane] : 0.f;
+            v = group_sum<32>(v);
+            if (lane == 0 && r < p.M) p.y[r] = v;
+        }
+        half ^= 1;
+        fill = 0;
+    };
+
     for (; tile < ntiles; tile += gridDim.x) {
         const int64_t next = tile + gridDim.x;
         if (next < ntiles) load_tile(next, nxt, snxt);
@@ -293,15 +327,9 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
         float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         s = group_sum<LW>(s);
         if constexpr (WIDE) {
-            float *pp = part + parity * (T / 32);
-            if (lane == 0) pp[warp] = s;
-            __syncthreads();
-            if (tg < 32) {
-                float v = lane < GW ? pp[grp * GW + lane] : 0.f;
-                v = group_sum<32>(v);
-                if (tg == 0 && valid) p.y[row] = v;
-            }
-            parity ^= 1;
+            if (fill == 0) batch_tile0 = tile;
+            if (lane == 0) part[(half * KB + fill) * NW + warp] = s;
+            if (++fill == KB) flush(KB);
         } else {
             if (tg == 0 && valid) p.y[row] = s;
         }
@@ -310,6 +338,9 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
             cur[k] = nxt[k];
             scur[k] = snxt[k];
         }
+    }
+    if constexpr (WIDE) {
+        if (fill > 0) flush(fill);
     }
 }
 
@@ -385,6 +416,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         *abort_flag = 1;
     };
 
+    pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -399,6 +431,12 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         // ---------------- producer warp ----------------
         int64_t issued = 0;
         if (lane == 0) {
+            // with programmatic dependent launch the weights stream in before
+            // the wait for the preceding kernel; x only after it
+            if (p.pdl) {
+                for (; issued < S && issued < iters; ++issued) issue(issued);
+                pdl_wait();
+            }
             if constexpr (XV == 1) {
                 mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
                 if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
@@ -406,6 +444,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
             for (; issued < S && issued < iters; ++issued) issue(issued);
         }
         issued = __shfl_sync(0xffffffffu, issued, 0);
+        if (p.pdl) pdl_wait();  // the whole producer warp writes y only after the wait
         int64_t done = 0;
         for (; done < iters; ++done) {
             const int slot = static_cast<int>(done % S);
@@ -445,6 +484,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 
     // ---------------- consumer warps ----------------
     // (every exit decision is made warp-uniform before the warp's shuffles)
+    if (p.pdl) pdl_wait();
     if constexpr (XV == 1) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns))) {
             if (lane == 0) fail();
@@ -512,7 +552,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 template <int DT, int G, int CPT, int T>
 constexpr int tile_x_offset()
 {
-    return (16 + (G > 32 ? 2 * (T / 32) * 4 : 0) + 15) / 16 * 16;
+    return (16 + (G > 32 ? 2 * kTileBatch * (T / 32) * 4 : 0) + 15) / 16 * 16;
 }
 
 // Element weight (i, j) as FP32; the quantised types return FP32(s) * q,
@@ -549,6 +589,7 @@ __device__ __forceinline__ float elem_x(const GemvArgs &p, int64_t j)
 template <int DT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) gemv_elem_kernel(const GemvArgs p)
 {
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
     if (row >= p.M) return;  // whole warp leaves together
@@ -567,7 +608,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_elem_kernel(const GemvArgs p)
 // ---------------------------------------------------------------------------
 
 template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
-void launch_vec(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+void launch_vec(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool)
 {
     gemv_vec_kernel<DT, LPR, RPW, U, WARPS, XMODE><<<grid, WARPS * 32, smem, s>>>(a);
 }
@@ -580,7 +621,7 @@ cudaError_t smem_limit_vec(int bytes)
 }
 
 template <int DT, int WARPS>
-void launch_elem(const GemvArgs &a, unsigned grid, size_t, cudaStream_t s)
+void launch_elem(const GemvArgs &a, unsigned grid, size_t, cudaStream_t s, bool)
 {
     gemv_elem_kernel<DT, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
 }
@@ -591,10 +632,33 @@ cudaError_t smem_limit_elem(int)
     return cudaSuccess;
 }
 
-template <int DT, int G, int CPT, int T, int XMODE, int MATH>
-void launch_tile(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+// Launch, optionally with programmatic stream serialisation (the kernel may
+// start before the preceding kernel on the stream has finished).
+template <typename Kernel>
+void launch_maybe_pdl(Kernel k, const GemvArgs &a, unsigned grid, unsigned block, size_t smem,
+                      cudaStream_t s, bool pdl)
 {
-    gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH><<<grid, T, smem, s>>>(a);
+    if (!pdl) {
+        k<<<grid, block, smem, s>>>(a);
+        return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, k, a);  // errors surface through cudaGetLastError
+}
+
+template <int DT, int G, int CPT, int T, int XMODE, int MATH>
+void launch_tile(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    launch_maybe_pdl(gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>, a, grid, T, smem, s, pdl);
 }
 
 template <int DT, int G, int CPT, int T, int XMODE, int MATH>
@@ -620,9 +684,9 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
     MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
 
 template <int DT, int T, int RS, int S, int MATH>
-void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s)
+void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    gemv_bulk_kernel<DT, T, RS, S, MATH><<<grid, T + 32, smem, s>>>(a);
+    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH>, a, grid, T + 32, smem, s, pdl);
 }
 
 template <int DT, int T, int RS, int S, int MATH>

@@ -128,3 +128,10 @@ def test_product_package_does_not_reference_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "gemv_oracle" not in text, f
+
+
+def test_gemv_ex_rejects_unknown_flags():
+    L = mbg.lib()
+    assert L.gemv_ex(mbg.F16, FAKE, FAKE, FAKE, 4, 8, None, 2, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex(mbg.F16, FAKE, FAKE, FAKE, -1, 8, None, 1, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex(9, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE

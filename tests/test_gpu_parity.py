@@ -245,3 +245,67 @@ def test_runs_on_a_side_stream():
 
 def test_tolerances_are_the_stated_ones():
     assert TOL == {"f32": 1e-5, "f16": 2e-3, "q8": 2e-3, "q4": 2e-3}
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_overlap_flag_parity(dtype):
+    for (M, N) in ((300, 4096), (64, 14336), (1000, 1024)):
+        inp = synth.make(synth.random_case(dtype, M, N, 60 + M))
+        y_ref, den = reference(dtype, inp, M, N)
+        t = upload(dtype, inp)
+        y = mbg.gemv(dtype, t["A"], t["x"], t.get("scales"), overlap=True)
+        torch.cuda.synchronize()
+        assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} overlap {M}x{N}")
+
+
+def _chain_inputs():
+    w1 = synth.random_case("f32", 4096, 1024, 71)
+    w2 = synth.random_case("f32", 512, 4096, 72)
+    i1, i2 = synth.make(w1), synth.make(w2)
+    t1, t2 = upload("f32", i1), upload("f32", i2)
+    return i1, i2, t1, t2
+
+
+def test_overlapped_chain_sees_the_previous_result():
+    """y1 = A1 x, then y2 = A2 y1 launched to overlap its predecessor: y2 must
+    use the finished y1 (y1 is cleared before every round)."""
+    i1, i2, t1, t2 = _chain_inputs()
+    y1 = torch.empty(4096, device="cuda")
+    y2 = torch.empty(512, device="cuda")
+    mbg.gemv("f32", t1["A"], t1["x"], y=y1)
+    torch.cuda.synchronize()
+    y1_ref = y1.cpu().numpy().copy()
+    y2_ref, den = oracle.load().gemv("f32", i2["A"], y1_ref, 512, 4096)
+    for _ in range(20):
+        y1.zero_()
+        mbg.gemv("f32", t1["A"], t1["x"], y=y1, overlap=True)
+        mbg.gemv("f32", t2["A"], y1, y=y2, overlap=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(y1.cpu().numpy(), y1_ref)
+    assert_close("f32", y2.cpu().numpy(), y2_ref, den, "overlapped chain")
+
+
+def test_overlapped_chain_in_a_cuda_graph():
+    i1, i2, t1, t2 = _chain_inputs()
+    y1 = torch.empty(4096, device="cuda")
+    y2 = torch.empty(512, device="cuda")
+    mbg.gemv("f32", t1["A"], t1["x"], y=y1)
+    torch.cuda.synchronize()
+    y2_ref, den = oracle.load().gemv("f32", i2["A"], y1.cpu().numpy(), 512, 4096)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            mbg.gemv("f32", t1["A"], t1["x"], y=y1, overlap=True)
+            mbg.gemv("f32", t2["A"], y1, y=y2, overlap=True)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(8):
+            y1.zero_()
+            mbg.gemv("f32", t1["A"], t1["x"], y=y1, overlap=True)
+            mbg.gemv("f32", t2["A"], y1, y=y2, overlap=True)
+    y2.fill_(-1.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close("f32", y2.cpu().numpy(), y2_ref, den, "overlapped chain in a graph")
+    assert mbg.gemv_get_device_error() == mbg.OK
