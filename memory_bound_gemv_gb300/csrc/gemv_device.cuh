@@ -65,6 +65,25 @@ __device__ __forceinline__ void report_error(unsigned int *err, unsigned int cod
     if (err) atomicOr(err, code);
 }
 
+// Shared-memory loads with 32-bit shared-space addresses (keeps the hot loops'
+// address arithmetic in 32-bit registers).  Volatile so that they stay after
+// the mbarrier waits that make the data visible.
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_half_as_float(uint32_t addr)
+{
+    unsigned short b;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(addr));
+    return __half2float(__ushort_as_half(b));
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier + bulk async copy (x staging)
 // ---------------------------------------------------------------------------
@@ -208,17 +227,33 @@ __device__ __forceinline__ const uint4 *x_smem_vec(const unsigned char *xs, int 
 }
 
 // Cooperative staging of x into the vector-major layout by threads
-// t = 0 .. nt-1 (reads are coalesced in x's own order).
+// t = 0 .. nt-1 (reads are coalesced in x's own order).  Loads are issued in
+// batches of eight per thread before any of them is stored, so staging costs
+// one memory round trip per batch instead of one per vector.
 template <int DT>
 __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x, int nchunks, int t,
                                                int nt)
 {
     constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int B = 8;
     const uint4 *src = static_cast<const uint4 *>(x);
-    for (int i = t; i < nchunks * XV; i += nt) {
-        const int c = i / XV;
-        const int v = i - c * XV;
-        *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = ld_cached16(src + i);
+    const int n = nchunks * XV;
+    for (int base = t; base < n; base += B * nt) {
+        uint4 r[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int i = base + j * nt;
+            if (i < n) r[j] = ld_cached16(src + i);
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int i = base + j * nt;
+            if (i < n) {
+                const int c = i / XV;
+                const int v = i - c * XV;
+                *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = r[j];
+            }
+        }
     }
 }
 
@@ -364,20 +399,31 @@ __device__ __forceinline__ void q8_codes_h2(uint32_t w, uint32_t (&h)[2])
     h[1] = hsub2_bits(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
 }
 
+// d = c ? (a ^ b) : b, bit by bit (one LOP3, lookup table 0x6C).
+__device__ __forceinline__ uint32_t lop3_sel_xor(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6C;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Eight int4 codes of a word (nibble k = column k) -> four pairs of exact
 // binary16 values, paired four columns apart: h[0] = (q0, q4),
-// h[1] = (q1, q5), h[2] = (q2, q6), h[3] = (q3, q7).  After the XOR each
-// nibble holds q + 8.  A nibble in bits 0-3 of a half OR-ed into 0x6400 is
-// 1024 + (q + 8), minus 1032 (0x6408) gives q; a nibble in bits 4-7 gives
-// 1024 + 16 (q + 8), and times 1/16 (0x2C00) minus 72 (0xD480) gives q.
+// h[1] = (q1, q5), h[2] = (q2, q6), h[3] = (q3, q7).  One LOP3 per pair
+// keeps two nibbles (mask c), flips their top bit (two's complement q ->
+// q + 8 in [0, 15]) and fills the rest of each half with 0x6400: a nibble in
+// bits 0-3 of a half gives 1024 + (q + 8), minus 1032 (0x6408) is q; a
+// nibble in bits 4-7 gives 1024 + 16 (q + 8), times 1/16 (0x2C00) minus 72
+// (0xD480) is q.  The XOR constant is the same in every nibble, so the upper
+// four nibbles use the word shifted right by 8 with the same constants.
+// (ALU cost: one shift and four LOP3 per eight codes.)
 __device__ __forceinline__ void q4_codes_h2(uint32_t w, uint32_t (&h)[4])
 {
-    const uint32_t u = w ^ 0x88888888u;
-    const uint32_t v = u >> 8;
-    h[0] = hsub2_bits((u & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-    h[1] = hfma2_bits((u & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
-    h[2] = hsub2_bits((v & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-    h[3] = hfma2_bits((v & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+    const uint32_t v = w >> 8;
+    h[0] = hsub2_bits(lop3_sel_xor(w, 0x64086408u, 0x000F000Fu), 0x64086408u);
+    h[1] = hfma2_bits(lop3_sel_xor(w, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
+    h[2] = hsub2_bits(lop3_sel_xor(v, 0x64086408u, 0x000F000Fu), 0x64086408u);
+    h[3] = hfma2_bits(lop3_sel_xor(v, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
 }
 
 // One 16-byte chunk of A times its x chunk (binary16), accumulated in FP32.

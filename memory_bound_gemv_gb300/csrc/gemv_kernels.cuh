@@ -238,17 +238,18 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     uint4 cur[CPT], nxt[CPT];
     float scur[CPT], snxt[CPT];
 
+    // Addresses: one row pointer per tile, then compile-time offsets k*G*16.
     auto load_tile = [&](int64_t tile, uint4 (&buf)[CPT], float (&sb)[CPT]) {
         const int64_t row = tile * RT + grp;
         if (row < p.M) {
-            const unsigned char *rp = static_cast<const unsigned char *>(p.A) + row * p.row_bytes;
+            const unsigned char *rp =
+                static_cast<const unsigned char *>(p.A) + row * p.row_bytes + tg * 16;
+            const uint16_t *sp = F::QUANT ? p.scales + row * p.groups : nullptr;
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
-                const int c = tg + k * G;
-                if (c < nchunks) {
-                    buf[k] = ld_stream16(rp + static_cast<size_t>(c) * 16);
-                    if constexpr (F::QUANT)
-                        sb[k] = ld_half_as_float(p.scales + row * p.groups + c / CHUNKS_PER_GROUP);
+                if (tg + k * G < nchunks) {
+                    buf[k] = ld_stream16(rp + k * G * 16);
+                    if constexpr (F::QUANT) sb[k] = ld_half_as_float(sp + (tg + k * G) / CHUNKS_PER_GROUP);
                 }
             }
         }
@@ -270,7 +271,13 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
             return;
         }
     }
-    const unsigned char *xsrc = (XMODE == XMODE_L1) ? static_cast<const unsigned char *>(p.x) : xs;
+    // x addresses of this thread's first chunk: global (through L1) or 32-bit
+    // shared-space addresses of each vector-major x plane
+    const unsigned char *xg = static_cast<const unsigned char *>(p.x) + tg * XCB;
+    uint32_t xb[XV];
+#pragma unroll
+    for (int v = 0; v < XV; ++v)
+        xb[v] = smem_addr(xs) + static_cast<uint32_t>(v) * static_cast<uint32_t>(nchunks) * 16u + tg * 16u;
 
     // Groups wider than a warp leave one partial per warp and tile in shared
     // memory; every KB tiles (kTileBatch) one block barrier makes a batch
@@ -308,9 +315,9 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 #pragma unroll
                     for (int v = 0; v < XV; ++v) {
                         if constexpr (XMODE == XMODE_L1)
-                            xv[v] = ld_cached16(xsrc + static_cast<size_t>(c) * XCB + 16 * v);
+                            xv[v] = ld_cached16(xg + k * G * XCB + 16 * v);
                         else
-                            xv[v] = *x_smem_vec(xsrc, nchunks, c, v);
+                            xv[v] = lds128(xb[v] + k * G * 16);
                     }
                     if constexpr (MATH == MATH_MIXED) {
                         chunk_dot_mixed<DT>(cur[k], xv, F::QUANT ? scur[k] : 0.f, acc);
@@ -507,8 +514,13 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         }
         const int64_t r0 = (blockIdx.x + it * grid) * RS;
         const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
-        const unsigned char *st = smem + L.stage + slot * L.stage_bytes;
-        const uint16_t *ss = reinterpret_cast<const uint16_t *>(smem + L.scale + slot * L.scale_bytes);
+        // 32-bit shared-space addresses, per-row offsets hoisted out of the loop
+        const uint32_t st = smem_addr(smem + L.stage + slot * L.stage_bytes);
+        const uint32_t ss = smem_addr(smem + L.scale + slot * L.scale_bytes);
+        const uint32_t xa = smem_addr(xs);
+        const uint32_t xstride = static_cast<uint32_t>(nchunks) * 16u;
+        const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+        const uint32_t gb = static_cast<uint32_t>(2 * p.groups);
         float acc[RS][NACC];
 #pragma unroll
         for (int r = 0; r < RS; ++r)
@@ -516,18 +528,19 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
             for (int k = 0; k < NACC; ++k) acc[r][k] = 0.f;
 #pragma unroll 2
         for (int c = tid; c < nchunks; c += T) {
+            const uint32_t c16 = static_cast<uint32_t>(c) * 16u;
             uint4 xv[XV];
 #pragma unroll
-            for (int v = 0; v < XV; ++v) xv[v] = *x_smem_vec(xs, nchunks, c, v);
+            for (int v = 0; v < XV; ++v) xv[v] = lds128(xa + v * xstride + c16);
             float xf[MATH == MATH_F32 ? F::EPC : 1];
             if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
             for (int r = 0; r < RS; ++r) {
                 if (r < rows) {
-                    const uint4 a =
-                        *reinterpret_cast<const uint4 *>(st + r * p.row_bytes + static_cast<size_t>(c) * 16);
+                    const uint4 a = lds128(st + r * rb + c16);
                     float sc = 0.f;
-                    if constexpr (F::QUANT) sc = __half2float(__ushort_as_half(ss[r * p.groups + c / CPG]));
+                    if constexpr (F::QUANT)
+                        sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c / CPG));
                     if constexpr (MATH == MATH_MIXED) {
                         chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
                     } else {
