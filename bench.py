@@ -601,6 +601,100 @@ def run_ours(args):
     return 0
 
 
+SOFTMAX_METRIC = "achieved HBM GB/s (one read + one write per element) and MBU% vs measured copy ceiling for FP16 row softmax"
+
+
+def run_softmax(args):
+    """Row softmax ("membound", "Bonus kernel"): bytes = 2 (read) + 2 (write) per element;
+    the denominator is the copy probe, because the kernel reads and writes every element."""
+    import numpy as np
+    import torch
+
+    import memory_bound_gemv_gb300 as mbg
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = synth.SOFTMAX_WORKLOADS[args.workload]
+    bits = synth.weight_rows(w, 0, w.M)
+    x0 = torch.from_numpy(bits.view(np.float16)).to(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    copies = rotation_copies(2 * w.M * w.N, l2)
+    xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+    y = torch.empty_like(x0)
+    step_bytes = 4 * w.M * w.N
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        mbg.gemv_softmax_f16(x0, y=y)
+    stream.synchronize()
+    y_first = y.cpu().numpy().view(np.uint16).copy()
+
+    half = (int(args.probe_gib * (1 << 30)) // 2) // 16 * 16
+    src = torch.randint(-2 ** 31, 2 ** 31 - 1, (half // 4,), dtype=torch.int32, device=dev)
+    dst = torch.empty_like(src)
+
+    def copy_probe():
+        res = {}
+        with torch.cuda.stream(stream):
+            for v, name in enumerate(mbg.copy_probe_variants()):
+                for _ in range(2):
+                    mbg.gemv_probe_copy(src, dst, v)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.probe_reps):
+                    mbg.gemv_probe_copy(src, dst, v)
+                e1.record(stream)
+                e1.synchronize()
+                res[name] = gbs(2 * half * args.probe_reps, e0.elapsed_time(e1) * 1e-3)
+        return res
+
+    before = copy_probe()
+    batch = copies * max(1, math.ceil(min(args.graph_batch, 50) / copies))
+    n_full, n_tail = split_steps(args.steps, batch)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(batch):
+            mbg.gemv_softmax_f16(xs[i % copies], y=y)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // batch)):
+            g.replay()
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(max(1, n_full)):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    steps = max(1, n_full) * batch
+    t = e0.elapsed_time(e1) * 1e-3
+    after = copy_probe()
+    best = {k: max(before[k], after[k]) for k in before}
+    ceiling = max(best.values())
+    value = gbs(steps * step_bytes, t)
+    rows = sorted({0, w.M // 2, w.M - 1})
+    import oracle
+    ref = oracle.load().softmax(bits, w.M, w.N, rows=rows, threads=cpu_threads())
+    got = y_first[rows].view(np.float16).astype(np.float64)
+    err = float(np.max(np.abs(got - ref) / np.maximum(ref, 1e-4)))
+    peak, peak_kind = measured_peak()
+    line = {"metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": t / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded SplitMix64 normal(0, 2) logits rounded to FP16)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "rotation_copies": copies,
+                       "l2_policy": "inputs larger than L2: the logits rotate through the copies",
+                       "launch": f"CUDA graph of {batch} back-to-back launches"},
+            "mbu": {"copy_probe_gbs": ceiling, "mbu_copy_pct": 100.0 * value / ceiling, "probes": best},
+            "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
+                         "frac": value / peak, "peak_kind": peak_kind, "traffic": None},
+            "parity_rows_max_rel_err": err, "gpu_launches": steps}
+    print(json.dumps(line), flush=True)
+    if args.json_out:
+        with open(args.json_out, "w") as f:
+            json.dump(line, f, indent=1)
+    return 0
+
+
 def run_profile(args):
     """Each kernel launched once (for an ncu capture of the top kernel)."""
     import numpy as np
@@ -635,7 +729,9 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=30000)
     p.add_argument("--warmup", type=int, default=300)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--op", choices=("gemv", "softmax"), default="gemv")
+    p.add_argument("--workload", default=None,
+                   choices=sorted(synth.WORKLOADS) + sorted(synth.SOFTMAX_WORKLOADS))
     p.add_argument("--graph-batch", type=int, default=100)
     p.add_argument("--probe-gib", type=float, default=1.0)
     p.add_argument("--probe-reps", type=int, default=10)
@@ -653,6 +749,14 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         p.error("--steps must be >= 1 and --warmup >= 0")
+    if args.workload is None:
+        args.workload = "softmax_8192x8192" if args.op == "softmax" else DEFAULT_WORKLOAD
+    if args.op == "softmax":
+        if args.workload not in synth.SOFTMAX_WORKLOADS:
+            p.error("--op softmax needs a softmax_* workload")
+        return run_softmax(args)
+    if args.workload not in synth.WORKLOADS:
+        p.error("GEMV workloads: " + ", ".join(sorted(synth.WORKLOADS)))
     if args.impl == "reference":
         return run_reference(args)
     if args.profile:

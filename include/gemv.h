@@ -138,6 +138,36 @@ int gemv_probe_variant_count(void);
 const char *gemv_probe_variant_name(int variant);
 
 /*
+ * Copy probe: reads src[0..bytes) and writes it to dst with the same 16-byte
+ * streaming loads (and streaming stores) -- the read + write ceiling that a
+ * balanced kernel such as the row softmax is quoted against ("membound",
+ * section "Bonus kernel: online softmax": the copy ceiling, not pure read, is
+ * the denominator of a kernel that reads and writes every element once).
+ * bytes a multiple of 16, both pointers 16-byte aligned, no overlap.
+ */
+gemv_status_t gemv_probe_copy(const void *src, void *dst, size_t bytes, int variant, void *stream);
+int gemv_probe_copy_variant_count(void);
+const char *gemv_probe_copy_variant_name(int variant);
+
+/*
+ * Row softmax of binary16 data: y[i, j] = exp(x[i,j] - m_i) / sum_k exp(x[i,k] - m_i)
+ * with m_i the maximum of row i, FP32 arithmetic, binary16 output (round to
+ * nearest even).  x and y: binary16 [M][N] row-major; y may be x (in place).
+ * "membound", section "Bonus kernel: online softmax" (the online update of
+ * the running maximum and sum, Milakov & Gimelshein).  Rows of up to 131072
+ * columns with N % 8 == 0 and 16-byte aligned pointers are read once and
+ * written once (one block, or a cluster of up to eight blocks combining
+ * their partial maxima and sums through distributed shared memory); any other
+ * shape uses two passes over the row.  Rows whose elements are all -inf are
+ * not supported (their result is unspecified).
+ */
+gemv_status_t gemv_softmax_f16(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, void *stream);
+int gemv_softmax_variant_count(void);
+const char *gemv_softmax_variant_name(int variant);
+gemv_status_t gemv_softmax_run_variant(int variant, const uint16_t *x, uint16_t *y, int64_t M,
+                                       int64_t N, void *stream);
+
+/*
  * Dequantise to FP32: W[i*N + j] = FP32(s[i, j/128]) * q[i,j], using the
  * same unpacking code as the GEMV kernels.  The product is exact, so W must
  * equal the oracle's dequantised weights bit for bit.  Test helper:

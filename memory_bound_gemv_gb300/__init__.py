@@ -65,6 +65,9 @@ def _declare(L):
         "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
         "gemv_get_device_error": [vp],
         "gemv_ex": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
+        "gemv_softmax_f16": [vp, vp, i64, i64, vp],
+        "gemv_softmax_run_variant": [i32, vp, vp, i64, i64, vp],
+        "gemv_probe_copy": [vp, vp, ctypes.c_size_t, i32, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -78,6 +81,12 @@ def _declare(L):
     L.gemv_variant_count.restype = i32
     L.gemv_select_variant.argtypes = [i32, vp, vp, i64, i64]
     L.gemv_select_variant.restype = i32
+    for name in ("gemv_softmax_variant_count", "gemv_probe_copy_variant_count"):
+        getattr(L, name).argtypes = []
+        getattr(L, name).restype = i32
+    for name in ("gemv_softmax_variant_name", "gemv_probe_copy_variant_name"):
+        getattr(L, name).argtypes = [i32]
+        getattr(L, name).restype = ctypes.c_char_p
     L.gemv_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.gemv_debug_set_wait_limit_ns.restype = None
     L.gemv_debug_skip_x_copy.argtypes = [i32]
@@ -314,6 +323,44 @@ def gemv_probe_read(buf, sink, variant: int = 0, stream=None):
     nbytes = buf.numel() * buf.element_size()
     _raise(lib().gemv_probe_read(buf.data_ptr(), nbytes, sink.data_ptr(), variant, _stream_ptr(stream)),
            "gemv_probe_read")
+
+
+def gemv_softmax_f16(x, y=None, stream=None, variant: Optional[int] = None):
+    """Row softmax of an FP16 matrix x [M, N] -> FP16 y (may be x itself)."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    M, N = x.shape
+    _check(x, "x", _f16_types(), (M, N))
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", _f16_types(), (M, N), x.device)
+    L = lib()
+    if variant is None:
+        st = L.gemv_softmax_f16(x.data_ptr(), y.data_ptr(), M, N, _stream_ptr(stream))
+    else:
+        st = L.gemv_softmax_run_variant(variant, x.data_ptr(), y.data_ptr(), M, N, _stream_ptr(stream))
+    _raise(st, "gemv_softmax_f16")
+    return y
+
+
+def softmax_variants() -> List[str]:
+    L = lib()
+    return [L.gemv_softmax_variant_name(k).decode() for k in range(L.gemv_softmax_variant_count())]
+
+
+def gemv_probe_copy(src, dst, variant: int = 0, stream=None):
+    """Copy src to dst (same byte size, 16-byte multiple) with the probe kernel."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst differ in size")
+    _raise(lib().gemv_probe_copy(src.data_ptr(), dst.data_ptr(), nbytes, variant, _stream_ptr(stream)),
+           "gemv_probe_copy")
+
+
+def copy_probe_variants() -> List[str]:
+    L = lib()
+    return [L.gemv_probe_copy_variant_name(k).decode() for k in range(L.gemv_probe_copy_variant_count())]
 
 
 def gemv_get_device_error(stream=None) -> int:

@@ -455,6 +455,52 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
     return dequant(DT_Q4, A, scales, W, M, N, stream);
 }
 
+static gemv_status_t softmax_run(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
+                                 void *stream)
+{
+    if (M < 0 || N < 0) return GEMV_ERR_INVALID_VALUE;
+    if (variant >= softmax_variant_count()) return GEMV_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMV_OK;
+    if (!x || !y) return GEMV_ERR_INVALID_VALUE;
+    if (!aligned(x, 2) || !aligned(y, 2)) return GEMV_ERR_MISALIGNED;
+    if (M > INT64_MAX / N) return GEMV_ERR_UNSUPPORTED;
+    if (!current_device()) return GEMV_ERR_CUDA;
+    const cudaError_t e = launch_softmax(x, y, M, N, variant, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return GEMV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+gemv_status_t gemv_softmax_f16(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, void *stream)
+{
+    return softmax_run(x, y, M, N, -1, stream);
+}
+
+gemv_status_t gemv_softmax_run_variant(int variant, const uint16_t *x, uint16_t *y, int64_t M,
+                                       int64_t N, void *stream)
+{
+    if (variant < 0) return GEMV_ERR_INVALID_VALUE;
+    return softmax_run(x, y, M, N, variant, stream);
+}
+
+int gemv_softmax_variant_count(void) { return softmax_variant_count(); }
+const char *gemv_softmax_variant_name(int variant) { return softmax_variant_name(variant); }
+
+gemv_status_t gemv_probe_copy(const void *src, void *dst, size_t bytes, int variant, void *stream)
+{
+    if (variant < 0 || variant >= copy_variant_count()) return GEMV_ERR_INVALID_VALUE;
+    if (bytes == 0) return GEMV_OK;
+    if (!src || !dst) return GEMV_ERR_INVALID_VALUE;
+    if (bytes % 16 || !aligned(src, 16) || !aligned(dst, 16)) return GEMV_ERR_MISALIGNED;
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    const cudaError_t e = launch_copy_probe(src, dst, bytes, variant, d->sm_count,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+int gemv_probe_copy_variant_count(void) { return copy_variant_count(); }
+const char *gemv_probe_copy_variant_name(int variant) { return copy_variant_name(variant); }
+
 gemv_status_t gemv_get_device_error(void *stream)
 {
     DeviceState *d = current_device();

@@ -125,4 +125,17 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
 // N == 0: y = 0.
 void launch_fill_zero(float *y, int64_t M, cudaStream_t s);
 
+// Row softmax (gemv_softmax.cu).  variant < 0 chooses; cudaErrorNotSupported
+// when the variant cannot serve the shape or alignment.
+cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
+                           cudaStream_t s);
+int softmax_variant_count();
+const char *softmax_variant_name(int v);
+
+// Copy probe (gemv_softmax.cu).
+cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, int variant, int sm_count,
+                              cudaStream_t s);
+int copy_variant_count();
+const char *copy_variant_name(int v);
+
 }  // namespace mbg

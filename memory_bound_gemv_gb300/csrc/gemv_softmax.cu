@@ -1,0 +1,328 @@
+// Row softmax of binary16 data ("membound", section "Bonus kernel: online
+// softmax": y_j = exp(x_j - m) / sum_k exp(x_k - m) with m the row maximum,
+// combined with the online update m' = max(m, m2), d' = d e^(m - m') +
+// d2 e^(m2 - m')), and a copy probe for its read + write ceiling.
+//
+// softmax_vec_kernel: a row is read once into registers (16-byte loads), each
+// thread keeps exp(x_j - m_t) for its own maximum m_t and its partial sum,
+// the (max, sum) pairs are combined across the warp, the block and -- for
+// rows wider than one block holds -- the thread-block cluster through
+// distributed shared memory, and the row is written once.  HBM traffic is one
+// read and one write per element (the page's version re-reads the row through
+// L2 for a second pass; with the row in registers there is no second read).
+//
+// softmax_elem_kernel: any layout or length.  One block per row, the page's
+// two passes: the online update over the row, then exp(x - m) / d re-reading
+// the row.
+#include <cooperative_groups.h>
+#include <cuda_fp16.h>
+
+#include "gemv_device.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace mbg {
+
+// (m, d) pairs: running maximum and sum of exp(x - m).  An empty side has
+// m = -inf and d = 0.
+struct MaxSum {
+    float m, d;
+};
+
+__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b)
+{
+    if (a.m == -INFINITY) return b;
+    if (b.m == -INFINITY) return a;
+    const float m = fmaxf(a.m, b.m);
+    return {m, a.d * __expf(a.m - m) + b.d * __expf(b.m - m)};
+}
+
+__device__ __forceinline__ MaxSum warp_combine(MaxSum v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        MaxSum o;
+        o.m = __shfl_xor_sync(0xffffffffu, v.m, off);
+        o.d = __shfl_xor_sync(0xffffffffu, v.d, off);
+        v = combine(v, o);
+    }
+    return v;
+}
+
+// Combine over the block; every thread receives the result.  `red` holds at
+// least 33 MaxSum entries of shared memory.
+template <int T>
+__device__ __forceinline__ MaxSum block_combine(MaxSum v, MaxSum *red)
+{
+    constexpr int NW = T / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_combine(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        MaxSum w = lane < NW ? red[lane] : MaxSum{-INFINITY, 0.f};
+        w = warp_combine(w);
+        if (lane == 0) red[32] = w;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+__device__ __forceinline__ void st_stream16(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Two floats -> binary16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// C CTAs (a cluster) per row, T threads per CTA, EPT elements per thread.
+// Requires N % 8 == 0, 16-byte aligned x and y, and N <= C * T * EPT.
+template <int T, int EPT, int C>
+__global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint16_t *y, int N)
+{
+    constexpr int VPT = EPT / 8;  // 16-byte vectors per thread
+    __shared__ MaxSum red[33];
+    __shared__ MaxSum cta_result;
+
+    const int tid = threadIdx.x;
+    const int rank = C > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) / C;
+    const int seg = rank * T * EPT;
+    const uint16_t *xr = x + row * N;
+    uint16_t *yr = y + row * N;
+
+    uint4 raw[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int e0 = seg + 8 * (k * T + tid);
+        raw[k] = e0 < N ? ld_stream16(xr + e0) : make_uint4(0, 0, 0, 0);
+    }
+
+    float v[EPT];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int e0 = seg + 8 * (k * T + tid);
+        half2_bits_to_float(raw[k].x, v[8 * k + 0], v[8 * k + 1]);
+        half2_bits_to_float(raw[k].y, v[8 * k + 2], v[8 * k + 3]);
+        half2_bits_to_float(raw[k].z, v[8 * k + 4], v[8 * k + 5]);
+        half2_bits_to_float(raw[k].w, v[8 * k + 6], v[8 * k + 7]);
+        if (e0 < N) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m = fmaxf(m, v[8 * k + e]);
+        }
+    }
+    // e_j = exp(x_j - m_t) for this thread's maximum; kept for the output
+    float d = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int e0 = seg + 8 * (k * T + tid);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            v[8 * k + e] = e0 < N ? __expf(v[8 * k + e] - m) : 0.f;
+            d += v[8 * k + e];
+        }
+    }
+    MaxSum mine{m, d};
+    if (m == -INFINITY) mine = {-INFINITY, 0.f};
+    MaxSum tot = block_combine<T>(mine, red);
+
+    if constexpr (C > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        if (tid == 0) cta_result = tot;
+        cluster.sync();  // every CTA's partial is written
+        MaxSum all{-INFINITY, 0.f};
+#pragma unroll
+        for (int r = 0; r < C; ++r) all = combine(all, *cluster.map_shared_rank(&cta_result, r));
+        cluster.sync();  // no CTA leaves while another still reads its shared memory
+        tot = all;
+    }
+
+    const float scale = (mine.m == -INFINITY) ? 0.f : __expf(mine.m - tot.m) / tot.d;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int e0 = seg + 8 * (k * T + tid);
+        if (e0 < N) {
+            uint4 o;
+            o.x = pack_half2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+            o.y = pack_half2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+            o.z = pack_half2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+            o.w = pack_half2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+            st_stream16(yr + e0, o);
+        }
+    }
+}
+
+// Any layout, any length: one block per row, two passes over the row.
+template <int T>
+__global__ void __launch_bounds__(T) softmax_elem_kernel(const uint16_t *x, uint16_t *y, int64_t N)
+{
+    __shared__ MaxSum red[33];
+    const int64_t row = blockIdx.x;
+    const uint16_t *xr = x + row * N;
+    uint16_t *yr = y + row * N;
+    MaxSum acc{-INFINITY, 0.f};
+    for (int64_t j = threadIdx.x; j < N; j += T) {
+        const float v = ld_half_as_float(xr + j);
+        if (v == -INFINITY) continue;  // contributes exp(-inf) = 0
+        if (v > acc.m) {
+            acc.d = acc.d * __expf(acc.m - v) + 1.f;  // acc.m = -inf gives 0 * 0
+            acc.m = v;
+        } else {
+            acc.d += __expf(v - acc.m);
+        }
+    }
+    const MaxSum tot = block_combine<T>(acc, red);
+    const float inv = 1.f / tot.d;
+    for (int64_t j = threadIdx.x; j < N; j += T) {
+        const float v = ld_half_as_float(xr + j);
+        reinterpret_cast<__half *>(yr)[j] = __float2half_rn(__expf(v - tot.m) * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Copy probe (read + write ceiling)
+// ---------------------------------------------------------------------------
+
+template <int THREADS, int U>
+__global__ void __launch_bounds__(THREADS) probe_copy_kernel(const uint4 *src, uint4 *dst, size_t n16)
+{
+    const size_t tile = static_cast<size_t>(THREADS) * U;
+    for (size_t t0 = static_cast<size_t>(blockIdx.x) * tile; t0 < n16; t0 += static_cast<size_t>(gridDim.x) * tile) {
+        uint4 b[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t c = t0 + static_cast<size_t>(u) * THREADS + threadIdx.x;
+            if (c < n16) b[u] = ld_stream16(src + c);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t c = t0 + static_cast<size_t>(u) * THREADS + threadIdx.x;
+            if (c < n16) st_stream16(dst + c, b[u]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launch glue
+// ---------------------------------------------------------------------------
+
+template <int T, int EPT, int C>
+cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N, cudaStream_t s)
+{
+    const unsigned grid = static_cast<unsigned>(M * C);
+    if constexpr (C == 1) {
+        softmax_vec_kernel<T, EPT, 1><<<grid, T, 0, s>>>(x, y, N);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(T);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, softmax_vec_kernel<T, EPT, C>, x, y, N);
+    }
+}
+
+struct SoftmaxVariant {
+    int threads, ept, cluster;
+    const char *name;
+    cudaError_t (*launch)(const uint16_t *, uint16_t *, int64_t, int, cudaStream_t);
+    int capacity() const { return threads * ept * cluster; }
+};
+
+static const SoftmaxVariant kSoftmax[] = {
+    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec<128, 8, 1>},
+    {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec<256, 16, 1>},
+    {256, 32, 1, "sm_t256_e32_c1", &launch_softmax_vec<256, 32, 1>},
+    {512, 32, 1, "sm_t512_e32_c1", &launch_softmax_vec<512, 32, 1>},
+    {512, 32, 2, "sm_t512_e32_c2", &launch_softmax_vec<512, 32, 2>},
+    {512, 32, 4, "sm_t512_e32_c4", &launch_softmax_vec<512, 32, 4>},
+    {512, 32, 8, "sm_t512_e32_c8", &launch_softmax_vec<512, 32, 8>},
+};
+constexpr int kSoftmaxVariants = static_cast<int>(sizeof(kSoftmax) / sizeof(kSoftmax[0]));
+
+int softmax_variant_count() { return kSoftmaxVariants + 1; }
+
+const char *softmax_variant_name(int v)
+{
+    if (v >= 0 && v < kSoftmaxVariants) return kSoftmax[v].name;
+    return v == kSoftmaxVariants ? "sm_elem_t256" : nullptr;
+}
+
+// Chooses (variant < 0) or runs a given variant; returns a CUDA error, or
+// cudaErrorNotSupported when the variant cannot serve the shape.
+cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
+                           cudaStream_t s)
+{
+    const bool vec_ok = N % 8 == 0 && N <= (1 << 30) &&
+                        (reinterpret_cast<uintptr_t>(x) % 16) == 0 &&
+                        (reinterpret_cast<uintptr_t>(y) % 16) == 0;
+    if (variant < 0) {
+        variant = kSoftmaxVariants;
+        if (vec_ok) {
+            for (int k = 0; k < kSoftmaxVariants; ++k) {
+                if (kSoftmax[k].capacity() >= N) {
+                    variant = k;
+                    break;
+                }
+            }
+        }
+    }
+    if (variant < kSoftmaxVariants) {
+        const SoftmaxVariant &v = kSoftmax[variant];
+        if (!vec_ok || N > v.capacity()) return cudaErrorNotSupported;
+        if (M * v.cluster > 0x7fffffffLL) return cudaErrorNotSupported;
+        return v.launch(x, y, M, static_cast<int>(N), s);
+    }
+    if (M > 0x7fffffffLL) return cudaErrorNotSupported;
+    softmax_elem_kernel<256><<<static_cast<unsigned>(M), 256, 0, s>>>(x, y, N);
+    return cudaGetLastError();
+}
+
+struct CopyVariant {
+    const char *name;
+    int blocks_per_sm;
+    void (*launch)(const void *, void *, size_t, unsigned, cudaStream_t);
+};
+
+template <int THREADS, int U>
+void launch_copy(const void *src, void *dst, size_t n16, unsigned grid, cudaStream_t s)
+{
+    probe_copy_kernel<THREADS, U>
+        <<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16);
+}
+
+static const CopyVariant kCopy[] = {
+    {"copy_t256_u4_b4", 4, &launch_copy<256, 4>},
+    {"copy_t256_u8_b4", 4, &launch_copy<256, 8>},
+    {"copy_t512_u4_b2", 2, &launch_copy<512, 4>},
+    {"copy_t256_u8_b2", 2, &launch_copy<256, 8>},
+};
+
+int copy_variant_count() { return static_cast<int>(sizeof(kCopy) / sizeof(kCopy[0])); }
+const char *copy_variant_name(int v) { return (v >= 0 && v < copy_variant_count()) ? kCopy[v].name : nullptr; }
+
+cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, int variant, int sm_count,
+                              cudaStream_t s)
+{
+    const CopyVariant &c = kCopy[variant];
+    c.launch(src, dst, bytes / 16, static_cast<unsigned>(sm_count * c.blocks_per_sm), s);
+    return cudaGetLastError();
+}
+
+}  // namespace mbg

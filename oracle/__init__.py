@@ -18,6 +18,9 @@ the pages it follows in the C file's header:
   workload definition, the page leaves the order open).
 * FLOP and byte counts -- "Making GEMV Fast", sections "Memory Access" and
   "Computation".
+* row softmax -- "membound", section "Bonus kernel: online softmax" (the
+  oracle is the plain definition; the page's online update reaches the same
+  value up to rounding).
 
 Every function is pinned by ``tests/test_oracle.py`` against values fixed by
 the pages or by mathematics (worked example, identity, unit vectors, all-ones
@@ -95,6 +98,8 @@ class Oracle:
         L.oracle_bytes.restype = ctypes.c_double
         L.oracle_bytes.argtypes = [i32, i64, i64]
         L.oracle_mutant_id.restype = i32
+        L.oracle_softmax_f16.restype = i32
+        L.oracle_softmax_f16.argtypes = [vp, i64, i64, vp, i64, vp, i32]
         self._L = L
 
     # -- binary16 --------------------------------------------------------
@@ -147,6 +152,21 @@ class Oracle:
         if fn(A.ctypes.data, s.ctypes.data, M, N, W.ctypes.data) != 0:
             raise ValueError(f"oracle rejected the arguments of {dtype} dequant")
         return W
+
+    # -- row softmax ---------------------------------------------------------
+    def softmax(self, x_bits, M: int, N: int, rows: Optional[Sequence[int]] = None,
+                threads: int = 1) -> np.ndarray:
+        """Row softmax of binary16 bits [M, N] in double: [nrows, N]."""
+        x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
+        if rows is None:
+            r_ptr, nrows = None, M
+        else:
+            r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+            r_ptr, nrows = r.ctypes.data, r.size
+        y = np.empty((max(nrows, 0), N), dtype=np.float64)
+        if self._L.oracle_softmax_f16(x.ctypes.data, M, N, r_ptr, nrows, y.ctypes.data, threads) != 0:
+            raise ValueError("oracle rejected the arguments of softmax")
+        return y
 
     # -- counting model ------------------------------------------------------
     def flops(self, M: int, N: int) -> float:

@@ -39,6 +39,9 @@
  * "Computation"): FLOPs = M(2N-1) = 2MN - M; FP32 bytes = 4(MN + N + M),
  * generalised per storage type as bytes(A) + bytes(scales) + bytes(x) + 4M.
  *
+ * The file also holds the row softmax of the same pages' second memory-bound
+ * decode kernel (see oracle_softmax_f16).
+ *
  * Built with ORACLE_MUTANT=k (k > 0) it contains one deliberate mistake; the
  * test-suite builds those variants to show that its pins catch each one.
  */
@@ -258,6 +261,53 @@ double oracle_bytes(int kind, int64_t M, int64_t N)
     case ORACLE_Q4: return m * n / 2.0 + 2.0 * m * (double)n_groups(N) + 2.0 * n + 4.0 * m;
     default: return -1.0;
     }
+}
+
+/* ---- row softmax ----------------------------------------------------------
+ *
+ * "membound", section "Bonus kernel: online softmax": each row of an FP16
+ * matrix is mapped to exp(x_j - m) / sum_k exp(x_k - m) with m the row
+ * maximum.  The page computes it with the online update of the running
+ * maximum and sum; the oracle is the plain definition (the online form reaches
+ * the same value up to rounding), in double precision, columns ascending.
+ * y receives nrows rows of N doubles.
+ */
+int oracle_softmax_f16(const uint16_t *x, int64_t M, int64_t N, const int64_t *rows, int64_t nrows,
+                       double *y, int threads)
+{
+    if (M < 0 || N < 0 || nrows < 0 || (M > 0 && N > 0 && (!x || !y))) return -1;
+    if (!rows) nrows = M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) return -1;
+    }
+    if (threads < 1) threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        const uint16_t *xi = x + i * N;
+        double *yi = y + r * N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = oracle_dec16(xi[j]);
+            if (v > m || j == 0) m = v;
+        }
+#if ORACLE_MUTANT == 8
+        m = 0.0; /* maximum not subtracted */
+#endif
+        double sum = 0.0;
+#if ORACLE_MUTANT == 9
+        const int64_t jend = N > 0 ? N - 1 : 0; /* last term left out of the sum */
+#else
+        const int64_t jend = N;
+#endif
+        for (int64_t j = 0; j < jend; ++j) sum += exp(oracle_dec16(xi[j]) - m);
+#if ORACLE_MUTANT == 10
+        sum = (double)N; /* normalised by the length instead of the sum */
+#endif
+        for (int64_t j = 0; j < N; ++j) yi[j] = exp(oracle_dec16(xi[j]) - m) / sum;
+    }
+    return 0;
 }
 
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -210,6 +210,17 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 
+#: Row-softmax inputs of the same decode workloads ("membound", "Bonus kernel":
+#: 8192x8192, 4096x32768 and 1024x131072 FP16).  The page gives no value
+#: distribution; logits are drawn from normal(0, 2) and rounded to FP16.
+SOFTMAX_WORKLOADS: Dict[str, Workload] = {
+    "softmax_8192x8192": _wl("softmax_8192x8192", "f16", 8192, 8192, 81, ("normal", 2.0), ("normal", 2.0)),
+    "softmax_4096x32768": _wl("softmax_4096x32768", "f16", 4096, 32768, 82, ("normal", 2.0), ("normal", 2.0)),
+    "softmax_1024x131072": _wl("softmax_1024x131072", "f16", 1024, 131072, 83, ("normal", 2.0),
+                               ("normal", 2.0)),
+}
+
+
 def _draw(dist: Tuple, seed: int, tag: int, start: int, count: int) -> np.ndarray:
     kind = dist[0]
     if kind == "uniform":

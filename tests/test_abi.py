@@ -135,3 +135,15 @@ def test_gemv_ex_rejects_unknown_flags():
     assert L.gemv_ex(mbg.F16, FAKE, FAKE, FAKE, 4, 8, None, 2, None) == mbg.ERR_INVALID_VALUE
     assert L.gemv_ex(mbg.F16, FAKE, FAKE, FAKE, -1, 8, None, 1, None) == mbg.ERR_INVALID_VALUE
     assert L.gemv_ex(9, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+
+
+def test_softmax_and_copy_validation():
+    L = mbg.lib()
+    assert L.gemv_softmax_f16(FAKE, FAKE, -1, 8, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_softmax_f16(None, None, 0, 8, None) == mbg.OK
+    assert L.gemv_softmax_f16(None, FAKE, 2, 8, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_softmax_f16(FAKE + 1, FAKE, 2, 8, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_softmax_run_variant(10_000, FAKE, FAKE, 2, 8, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_probe_copy(FAKE, FAKE, 4096, -1, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_probe_copy(FAKE, FAKE + 8, 4096, 0, None) == mbg.ERR_MISALIGNED
+    assert len(mbg.softmax_variants()) >= 2 and len(mbg.copy_probe_variants()) >= 1

@@ -221,8 +221,50 @@ def pin_counts(orc):
     assert orc.flops(0, 5) == 0 and orc.flops(5, 0) == 0
 
 
+def _f16(vals):
+    return synth.to_f16_bits(np.asarray(vals, dtype=np.float64))
+
+
+def pin_softmax_closed_forms(orc):
+    import math
+    # a constant row gives 1/N everywhere
+    for N in (1, 3, 1000):
+        y = orc.softmax(_f16(np.full((2, N), 0.75)), 2, N)
+        assert np.allclose(y, 1.0 / N, rtol=1e-14, atol=0)
+    # two elements: y0 = 1 / (1 + e^(x1 - x0))
+    for a, b in ((0.0, 1.0), (-3.5, 2.25), (7.0, 7.0)):
+        y = orc.softmax(_f16([[a, b]]), 1, 2)[0]
+        assert abs(y[0] - 1.0 / (1.0 + math.exp(b - a))) < 1e-15
+        assert abs(y[1] - 1.0 / (1.0 + math.exp(a - b))) < 1e-15
+    # large inputs: the maximum is subtracted, so nothing overflows
+    y = orc.softmax(_f16([[60000.0, 60000.0, 59968.0]]), 1, 3)[0]
+    assert np.all(np.isfinite(y)) and abs(y[0] - y[1]) == 0.0
+    # shifting a row by a constant leaves the result unchanged (integer inputs stay exact)
+    xi = synth.integers(3, 2, 0, 64, -8, 8).astype(np.float64)
+    y1 = orc.softmax(_f16([xi]), 1, 64)[0]
+    y2 = orc.softmax(_f16([xi + 5.0]), 1, 64)[0]
+    assert np.allclose(y1, y2, rtol=1e-14, atol=0)
+
+
+def pin_softmax_sums_and_brute_force(orc):
+    import math
+    w = synth.random_case("f16", 5, 37, 91)
+    bits = synth.weight_rows(synth.Workload("sm", "f16", 5, 37, 91, ("normal", 2.0), ("normal", 2.0)), 0, 5)
+    y = orc.softmax(bits, 5, 37)
+    assert np.allclose(y.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    vals = bits.view(np.float16).astype(np.float64)
+    for i in range(5):
+        m = max(vals[i])
+        e = [math.exp(v - m) for v in vals[i]]
+        s = math.fsum(e)
+        for j in range(37):
+            assert abs(y[i, j] - e[j] / s) <= 1e-15 * max(1.0, e[j] / s)
+    del w
+
+
 PINS = [pin_dec16_all_patterns, pin_rowmajor_worked_example, pin_identity, pin_unit_vectors,
-        pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts]
+        pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts,
+        pin_softmax_closed_forms, pin_softmax_sums_and_brute_force]
 
 
 @pytest.fixture(scope="module")
@@ -283,7 +325,8 @@ def test_error_metric():
 MUTANTS = {1: "int4 nibble order swapped", 2: "int4 read as offset-8",
            3: "scale group width 64", 4: "A read column-major",
            5: "binary16 subnormals decoded as normals", 6: "last column dropped",
-           7: "scale row pitch floor(N/128)"}
+           7: "scale row pitch floor(N/128)", 8: "softmax without the maximum subtracted",
+           9: "softmax sum missing its last term", 10: "softmax normalised by N"}
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[k] for k in sorted(MUTANTS)])
