@@ -3,7 +3,8 @@
 // combined with the online update m' = max(m, m2), d' = d e^(m - m') +
 // d2 e^(m2 - m')), and a copy probe for its read + write ceiling.
 //
-// softmax_vec_kernel: a row is read once into registers (16-byte loads), each
+// softmax_vec_kernel: a row is read once into registers (16-byte loads; the
+// persistent grid loads the next row while it finishes the current one), each
 // thread keeps exp(x_j - m_t) for its own maximum m_t and its partial sum,
 // the (max, sum) pairs are combined across the warp, the block and -- for
 // rows wider than one block holds -- the thread-block cluster through
@@ -85,8 +86,12 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 
 // C CTAs (a cluster) per row, T threads per CTA, EPT elements per thread.
 // Requires N % 8 == 0, 16-byte aligned x and y, and N <= C * T * EPT.
+// Cluster k handles rows k, k + nclusters, ... and loads its segment of the
+// next row into registers before it reduces and writes the current one, so a
+// persistent grid keeps reads in flight while it finishes a row.  All CTAs of
+// a cluster walk the same rows, so they meet the same cluster barriers.
 template <int T, int EPT, int C>
-__global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint16_t *y, int N)
+__global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N)
 {
     constexpr int VPT = EPT / 8;  // 16-byte vectors per thread
     __shared__ MaxSum red[33];
@@ -94,69 +99,90 @@ __global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint1
 
     const int tid = threadIdx.x;
     const int rank = C > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) / C;
+    const int64_t nclusters = gridDim.x / C;
     const int seg = rank * T * EPT;
-    const uint16_t *xr = x + row * N;
-    uint16_t *yr = y + row * N;
 
-    uint4 raw[VPT];
+    auto load = [&](int64_t row, uint4 (&raw)[VPT]) {
+        const uint16_t *xr = x + row * N;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int e0 = seg + 8 * (k * T + tid);
-        raw[k] = e0 < N ? ld_stream16(xr + e0) : make_uint4(0, 0, 0, 0);
-    }
-
-    float v[EPT];
-    float m = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int e0 = seg + 8 * (k * T + tid);
-        half2_bits_to_float(raw[k].x, v[8 * k + 0], v[8 * k + 1]);
-        half2_bits_to_float(raw[k].y, v[8 * k + 2], v[8 * k + 3]);
-        half2_bits_to_float(raw[k].z, v[8 * k + 4], v[8 * k + 5]);
-        half2_bits_to_float(raw[k].w, v[8 * k + 6], v[8 * k + 7]);
-        if (e0 < N) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) m = fmaxf(m, v[8 * k + e]);
+        for (int k = 0; k < VPT; ++k) {
+            const int e0 = seg + 8 * (k * T + tid);
+            raw[k] = e0 < N ? ld_stream16(xr + e0) : make_uint4(0, 0, 0, 0);
         }
+    };
+
+    // Only single-block rows prefetch (a persistent grid); the extra registers
+    // would halve the occupancy of the cluster variants, which run one
+    // cluster per row instead.
+    constexpr bool PREFETCH = C == 1;
+    uint4 nxt[PREFETCH ? VPT : 1];
+    int64_t row = blockIdx.x / C;
+    if constexpr (PREFETCH) {
+        if (row < M) load(row, nxt);
     }
-    // e_j = exp(x_j - m_t) for this thread's maximum; kept for the output
-    float d = 0.f;
+    for (; row < M; row += nclusters) {
+        uint4 raw[VPT];
+        if constexpr (PREFETCH) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int e0 = seg + 8 * (k * T + tid);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            v[8 * k + e] = e0 < N ? __expf(v[8 * k + e] - m) : 0.f;
-            d += v[8 * k + e];
+            for (int k = 0; k < VPT; ++k) raw[k] = nxt[k];
+            if (row + nclusters < M) load(row + nclusters, nxt);
+        } else {
+            load(row, raw);
         }
-    }
-    MaxSum mine{m, d};
-    if (m == -INFINITY) mine = {-INFINITY, 0.f};
-    MaxSum tot = block_combine<T>(mine, red);
 
-    if constexpr (C > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        if (tid == 0) cta_result = tot;
-        cluster.sync();  // every CTA's partial is written
-        MaxSum all{-INFINITY, 0.f};
+        float v[EPT];
+        float m = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < C; ++r) all = combine(all, *cluster.map_shared_rank(&cta_result, r));
-        cluster.sync();  // no CTA leaves while another still reads its shared memory
-        tot = all;
-    }
+        for (int k = 0; k < VPT; ++k) {
+            const int e0 = seg + 8 * (k * T + tid);
+            half2_bits_to_float(raw[k].x, v[8 * k + 0], v[8 * k + 1]);
+            half2_bits_to_float(raw[k].y, v[8 * k + 2], v[8 * k + 3]);
+            half2_bits_to_float(raw[k].z, v[8 * k + 4], v[8 * k + 5]);
+            half2_bits_to_float(raw[k].w, v[8 * k + 6], v[8 * k + 7]);
+            if (e0 < N) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m = fmaxf(m, v[8 * k + e]);
+            }
+        }
+        // e_j = exp(x_j - m_t) for this thread's maximum; kept for the output
+        float d = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int e0 = seg + 8 * (k * T + tid);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[8 * k + e] = e0 < N ? __expf(v[8 * k + e] - m) : 0.f;
+                d += v[8 * k + e];
+            }
+        }
+        MaxSum mine{m, d};
+        if (m == -INFINITY) mine = {-INFINITY, 0.f};
+        MaxSum tot = block_combine<T>(mine, red);
 
-    const float scale = (mine.m == -INFINITY) ? 0.f : __expf(mine.m - tot.m) / tot.d;
+        if constexpr (C > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            if (tid == 0) cta_result = tot;
+            cluster.sync();  // every CTA's partial is written
+            MaxSum all{-INFINITY, 0.f};
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int e0 = seg + 8 * (k * T + tid);
-        if (e0 < N) {
-            uint4 o;
-            o.x = pack_half2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
-            o.y = pack_half2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
-            o.z = pack_half2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
-            o.w = pack_half2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
-            st_stream16(yr + e0, o);
+            for (int r = 0; r < C; ++r) all = combine(all, *cluster.map_shared_rank(&cta_result, r));
+            cluster.sync();  // no CTA moves on while another still reads its partial
+            tot = all;
+        }
+
+        const float scale = (mine.m == -INFINITY) ? 0.f : __expf(mine.m - tot.m) / tot.d;
+        uint16_t *yr = y + row * N;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int e0 = seg + 8 * (k * T + tid);
+            if (e0 < N) {
+                uint4 o;
+                o.x = pack_half2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+                o.y = pack_half2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+                o.z = pack_half2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+                o.w = pack_half2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+                st_stream16(yr + e0, o);
+            }
         }
     }
 }
@@ -215,12 +241,49 @@ __global__ void __launch_bounds__(THREADS) probe_copy_kernel(const uint4 *src, u
 // Launch glue
 // ---------------------------------------------------------------------------
 
+// Resident clusters (of C blocks) for this kernel: the persistent grid size.
+template <int T, int EPT, int C>
+int resident_clusters()
+{
+    static int cached = -1;  // a kernel's occupancy does not change during the process
+    if (cached >= 0) return cached;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int n = 0;
+    if constexpr (C == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, softmax_vec_kernel<T, EPT, 1>, T, 0) ==
+            cudaSuccess)
+            n = per_sm * sms;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C * sms);
+        cfg.blockDim = dim3(T);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, softmax_vec_kernel<T, EPT, C>, &cfg) != cudaSuccess) n = 0;
+    }
+    cached = n > 0 ? n : sms;
+    return cached;
+}
+
 template <int T, int EPT, int C>
 cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N, cudaStream_t s)
 {
-    const unsigned grid = static_cast<unsigned>(M * C);
+    // single-block rows: a persistent grid that prefetches the next row;
+    // cluster rows: one cluster per row (measured faster: the scheduler keeps
+    // more clusters in flight than a persistent grid of resident clusters)
+    int64_t clusters = M;
+    if constexpr (C == 1) clusters = M < resident_clusters<T, EPT, C>() ? M : resident_clusters<T, EPT, C>();
+    const unsigned grid = static_cast<unsigned>(clusters * C);
     if constexpr (C == 1) {
-        softmax_vec_kernel<T, EPT, 1><<<grid, T, 0, s>>>(x, y, N);
+        softmax_vec_kernel<T, EPT, 1><<<grid, T, 0, s>>>(x, y, M, N);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -234,7 +297,7 @@ cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N,
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, softmax_vec_kernel<T, EPT, C>, x, y, N);
+        return cudaLaunchKernelEx(&cfg, softmax_vec_kernel<T, EPT, C>, x, y, M, N);
     }
 }
 
@@ -245,6 +308,8 @@ struct SoftmaxVariant {
     int capacity() const { return threads * ept * cluster; }
 };
 
+// The automatic choice is the first entry whose capacity covers the row;
+// the T = 256 cluster entries after it are alternatives for comparison.
 static const SoftmaxVariant kSoftmax[] = {
     {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec<128, 8, 1>},
     {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec<256, 16, 1>},
@@ -253,6 +318,9 @@ static const SoftmaxVariant kSoftmax[] = {
     {512, 32, 2, "sm_t512_e32_c2", &launch_softmax_vec<512, 32, 2>},
     {512, 32, 4, "sm_t512_e32_c4", &launch_softmax_vec<512, 32, 4>},
     {512, 32, 8, "sm_t512_e32_c8", &launch_softmax_vec<512, 32, 8>},
+    {256, 32, 2, "sm_t256_e32_c2", &launch_softmax_vec<256, 32, 2>},
+    {256, 32, 4, "sm_t256_e32_c4", &launch_softmax_vec<256, 32, 4>},
+    {256, 32, 8, "sm_t256_e32_c8", &launch_softmax_vec<256, 32, 8>},
 };
 constexpr int kSoftmaxVariants = static_cast<int>(sizeof(kSoftmax) / sizeof(kSoftmax[0]));
 
@@ -286,7 +354,6 @@ cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N,
     if (variant < kSoftmaxVariants) {
         const SoftmaxVariant &v = kSoftmax[variant];
         if (!vec_ok || N > v.capacity()) return cudaErrorNotSupported;
-        if (M * v.cluster > 0x7fffffffLL) return cudaErrorNotSupported;
         return v.launch(x, y, M, static_cast<int>(N), s);
     }
     if (M > 0x7fffffffLL) return cudaErrorNotSupported;
