@@ -42,7 +42,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemv_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 
-KIND = {"f32": 0, "f16": 1, "q8": 2, "q4": 3}
+KIND = {"f32": 0, "f16": 1, "q8": 2, "q4": 3, "f16x32": 4, "q8row": 5}
 
 _lock = threading.Lock()
 _cache = {}
@@ -81,11 +81,11 @@ class Oracle:
         L.oracle_dec16.argtypes = [ctypes.c_uint16]
         L.oracle_dec16_array.restype = None
         L.oracle_dec16_array.argtypes = [vp, vp, i64]
-        for name in ("oracle_gemv_f32", "oracle_gemv_f16"):
+        for name in ("oracle_gemv_f32", "oracle_gemv_f16", "oracle_gemv_f16_xf32"):
             f = getattr(L, name)
             f.restype = i32
             f.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp, i32]
-        for name in ("oracle_gemv_q8", "oracle_gemv_q4"):
+        for name in ("oracle_gemv_q8", "oracle_gemv_q4", "oracle_gemv_q8_rowscale"):
             f = getattr(L, name)
             f.restype = i32
             f.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp, i32]
@@ -117,7 +117,9 @@ class Oracle:
 
         Storage formats: f32 -> float32 A [M, N], x [N]; f16 -> uint16 bits;
         q8 -> int8 A [M, N]; q4 -> uint8 A [M, N/2]; x FP16 bits for q8/q4;
-        scales FP16 bits [M, ceil(N/128)].  Returns (y, den) as float64.
+        scales FP16 bits [M, ceil(N/128)]; f16x32 -> uint16 bits A, float32
+        x; q8row -> int8 A, FP16 bits scales [M] (one per row).  Returns
+        (y, den) as float64.
         """
         A = np.ascontiguousarray(A)
         x = np.ascontiguousarray(x)
@@ -128,13 +130,15 @@ class Oracle:
             r_ptr, nrows = r.ctypes.data, r.size
         y = np.empty(max(nrows, 0), dtype=np.float64)
         den = np.empty(max(nrows, 0), dtype=np.float64)
-        if dtype in ("f32", "f16"):
-            fn = self._L.oracle_gemv_f32 if dtype == "f32" else self._L.oracle_gemv_f16
+        if dtype in ("f32", "f16", "f16x32"):
+            fn = {"f32": self._L.oracle_gemv_f32, "f16": self._L.oracle_gemv_f16,
+                  "f16x32": self._L.oracle_gemv_f16_xf32}[dtype]
             rc = fn(A.ctypes.data, x.ctypes.data, M, N, r_ptr, nrows,
                     y.ctypes.data, den.ctypes.data, threads)
-        elif dtype in ("q8", "q4"):
+        elif dtype in ("q8", "q4", "q8row"):
             s = np.ascontiguousarray(scales)
-            fn = self._L.oracle_gemv_q8 if dtype == "q8" else self._L.oracle_gemv_q4
+            fn = {"q8": self._L.oracle_gemv_q8, "q4": self._L.oracle_gemv_q4,
+                  "q8row": self._L.oracle_gemv_q8_rowscale}[dtype]
             rc = fn(A.ctypes.data, x.ctypes.data, s.ctypes.data, M, N, r_ptr, nrows,
                     y.ctypes.data, den.ctypes.data, threads)
         else:

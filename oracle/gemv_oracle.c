@@ -22,6 +22,10 @@
  *        with g = ceil(N/128) FP16 scales per row ("membound", section
  *        "dequant GEMV": weights dequantised in register as q times the
  *        group scale; the reference there is computed on q*s exactly).
+ *   f16 weights with FP32 x: w = dec16(A[i*N+j]), x = x[j] (FP32 storage)
+ *        ("llama.cpp GEMV CUDA", implementation note: FP32 hidden state).
+ *   q8 with one scale per row: w = dec16(S[i]) * (int8)A[i*N+j] ("membound",
+ *        section "dequant GEMV": the page's kernel keeps one scale per row).
  *
  * Alongside y it returns den[i] = sum_j |w(i,j)| * |x(j)|, the normaliser of
  * the parity metric |y_gpu - y_ref| / den.
@@ -140,11 +144,27 @@ static double w_q4(const uint8_t *A, const uint16_t *S, int64_t N, int64_t i, in
 
 /* ---- one row ------------------------------------------------------------- */
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_Q8 = 2, ORACLE_Q4 = 3 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_Q8 = 2, ORACLE_Q4 = 3, ORACLE_F16X32 = 4,
+       ORACLE_Q8ROW = 5 };
+
+/* one FP16 scale per row: S[i] */
+static double w_q8row(const int8_t *A, const uint16_t *S, int64_t N, int64_t i, int64_t j)
+{
+#if ORACLE_MUTANT == 11
+    const double s = oracle_dec16(S[0]); /* every row scaled by row 0's scale */
+#else
+    const double s = oracle_dec16(S[i]);
+#endif
+    return s * (double)A[i * N + j];
+}
 
 static double x_of(int kind, const void *x, int64_t j)
 {
-    if (kind == ORACLE_F32) return (double)((const float *)x)[j];
+#if ORACLE_MUTANT == 12
+    if (kind == ORACLE_F32) return (double)((const float *)x)[j]; /* FP32 x read as binary16 */
+#else
+    if (kind == ORACLE_F32 || kind == ORACLE_F16X32) return (double)((const float *)x)[j];
+#endif
     return oracle_dec16(((const uint16_t *)x)[j]);
 }
 
@@ -153,8 +173,10 @@ static double w_of(int kind, const void *A, const uint16_t *S, int64_t M, int64_
 {
     switch (kind) {
     case ORACLE_F32: return w_f32((const float *)A, M, N, i, j);
-    case ORACLE_F16: return w_f16((const uint16_t *)A, N, i, j);
+    case ORACLE_F16:
+    case ORACLE_F16X32: return w_f16((const uint16_t *)A, N, i, j);
     case ORACLE_Q8: return w_q8((const int8_t *)A, S, N, i, j);
+    case ORACLE_Q8ROW: return w_q8row((const int8_t *)A, S, N, i, j);
     default: return w_q4((const uint8_t *)A, S, N, i, j);
     }
 }
@@ -184,7 +206,8 @@ static int run_rows(int kind, const void *A, const void *x, const uint16_t *S, i
 {
     if (M < 0 || N < 0 || nrows < 0 || !y || !den) return -1;
     if ((M > 0 && N > 0) && (!A || !x)) return -1;
-    if ((kind == ORACLE_Q8 || kind == ORACLE_Q4) && M > 0 && N > 0 && !S) return -1;
+    if ((kind == ORACLE_Q8 || kind == ORACLE_Q4 || kind == ORACLE_Q8ROW) && M > 0 && N > 0 && !S)
+        return -1;
     if (kind == ORACLE_Q4 && (N % 2)) return -1;
     if (!rows) nrows = M;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -224,6 +247,19 @@ int oracle_gemv_q4(const uint8_t *A, const uint16_t *x, const uint16_t *S, int64
     return run_rows(ORACLE_Q4, A, x, S, M, N, rows, nrows, y, den, threads);
 }
 
+int oracle_gemv_f16_xf32(const uint16_t *A, const float *x, int64_t M, int64_t N,
+                         const int64_t *rows, int64_t nrows, double *y, double *den, int threads)
+{
+    return run_rows(ORACLE_F16X32, A, x, NULL, M, N, rows, nrows, y, den, threads);
+}
+
+int oracle_gemv_q8_rowscale(const int8_t *A, const uint16_t *x, const uint16_t *S, int64_t M,
+                            int64_t N, const int64_t *rows, int64_t nrows, double *y, double *den,
+                            int threads)
+{
+    return run_rows(ORACLE_Q8ROW, A, x, S, M, N, rows, nrows, y, den, threads);
+}
+
 /* ---- dequantised weights (the q*s the reference is computed on) --------- */
 
 int oracle_dequant_q8(const int8_t *A, const uint16_t *S, int64_t M, int64_t N, double *W)
@@ -259,6 +295,8 @@ double oracle_bytes(int kind, int64_t M, int64_t N)
     case ORACLE_F16: return 2.0 * m * n + 2.0 * n + 4.0 * m;
     case ORACLE_Q8: return m * n + 2.0 * m * (double)n_groups(N) + 2.0 * n + 4.0 * m;
     case ORACLE_Q4: return m * n / 2.0 + 2.0 * m * (double)n_groups(N) + 2.0 * n + 4.0 * m;
+    case ORACLE_F16X32: return 2.0 * m * n + 4.0 * n + 4.0 * m;
+    case ORACLE_Q8ROW: return m * n + 2.0 * m + 2.0 * n + 4.0 * m;
     default: return -1.0;
     }
 }

@@ -157,7 +157,7 @@ class Workload:
     """One GEMV problem: dtype, shape, seed and value distributions."""
 
     name: str
-    dtype: str          # "f32" | "f16" | "q8" | "q4"
+    dtype: str          # "f32" | "f16" | "q8" | "q4" | "f16x32" | "q8row"
     M: int
     N: int
     seed: int
@@ -167,7 +167,12 @@ class Workload:
 
     @property
     def quantised(self) -> bool:
-        return self.dtype in ("q8", "q4")
+        return self.dtype in ("q8", "q4", "q8row")
+
+    @property
+    def scale_groups(self) -> int:
+        """FP16 scales per row: one per 128 columns, or one for "q8row"."""
+        return 1 if self.dtype == "q8row" else n_groups(self.N)
 
 
 def _wl(name, dtype, M, N, seed, a, x, s=None) -> Workload:
@@ -207,6 +212,10 @@ WORKLOADS: Dict[str, Workload] = {
     "q8_14336x4096": _wl("q8_14336x4096", "q8", 14336, 4096, 51, Q8D, N1, SCD),
     "q4_4096x14336": _wl("q4_4096x14336", "q4", 4096, 14336, 52, Q4D, N1, SCD),
     "q4_14336x4096": _wl("q4_14336x4096", "q4", 14336, 4096, 53, Q4D, N1, SCD),
+    # format options: FP16 weights with an FP32 hidden state; INT8 with one
+    # FP16 scale per row
+    "f16x32_down_4096x14336": _wl("f16x32_down_4096x14336", "f16x32", 4096, 14336, 61, N002, N1),
+    "q8row_4096x14336": _wl("q8row_4096x14336", "q8row", 4096, 14336, 62, Q8D, N1, SCD),
 }
 
 
@@ -235,9 +244,9 @@ def _draw(dist: Tuple, seed: int, tag: int, start: int, count: int) -> np.ndarra
 def _encode_rows(dtype: str, vals: np.ndarray, nrows: int, N: int) -> np.ndarray:
     if dtype == "f32":
         return vals.astype(np.float32).reshape(nrows, N)
-    if dtype == "f16":
+    if dtype in ("f16", "f16x32"):
         return to_f16_bits(vals).reshape(nrows, N)
-    if dtype == "q8":
+    if dtype in ("q8", "q8row"):
         return vals.astype(np.int8).reshape(nrows, N)
     if dtype == "q4":
         return pack_int4(vals.reshape(nrows, N))
@@ -248,7 +257,7 @@ def weight_rows(w: Workload, row0: int, nrows: int) -> np.ndarray:
     """Rows ``row0 .. row0+nrows-1`` of A in storage format.
 
     f32 -> float32 [n, N]; f16 -> uint16 bits [n, N]; q8 -> int8 [n, N];
-    q4 -> uint8 [n, N/2].
+    q4 -> uint8 [n, N/2]; f16x32 as f16; q8row as q8.
     """
     if w.dtype == "q4" and w.N % 2:
         raise ValueError("int4 rows need an even column count")
@@ -257,16 +266,16 @@ def weight_rows(w: Workload, row0: int, nrows: int) -> np.ndarray:
 
 
 def x_vector(w: Workload) -> np.ndarray:
-    """x in storage format: float32 [N] for f32, FP16 bits uint16 [N] otherwise."""
+    """x in storage format: float32 [N] for f32 and f16x32, FP16 bits uint16 [N] otherwise."""
     vals = _draw(w.x_dist, w.seed, TAG_X, 0, w.N)
-    return vals.astype(np.float32) if w.dtype == "f32" else to_f16_bits(vals)
+    return vals.astype(np.float32) if w.dtype in ("f32", "f16x32") else to_f16_bits(vals)
 
 
 def scale_rows(w: Workload, row0: int, nrows: int) -> np.ndarray:
-    """FP16 bits [nrows, ceil(N/128)] of the group scales."""
+    """FP16 bits [nrows, groups] of the scales (groups = ceil(N/128), or 1 for q8row)."""
     if not w.quantised:
-        raise ValueError("scales exist only for q8/q4")
-    g = n_groups(w.N)
+        raise ValueError("scales exist only for q8/q4/q8row")
+    g = w.scale_groups
     vals = _draw(w.s_dist, w.seed, TAG_SCALES, row0 * g, nrows * g)
     return to_f16_bits(vals).reshape(nrows, g)
 
@@ -292,4 +301,8 @@ def random_case(dtype: str, M: int, N: int, seed: int) -> Workload:
         return _wl(f"case_q8_{M}x{N}", "q8", M, N, seed, Q8D, N1, SCD)
     if dtype == "q4":
         return _wl(f"case_q4_{M}x{N}", "q4", M, N, seed, Q4D, N1, SCD)
+    if dtype == "f16x32":
+        return _wl(f"case_f16x32_{M}x{N}", "f16x32", M, N, seed, N002, N1)
+    if dtype == "q8row":
+        return _wl(f"case_q8row_{M}x{N}", "q8row", M, N, seed, Q8D, N1, SCD)
     raise ValueError(dtype)

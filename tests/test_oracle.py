@@ -127,6 +127,29 @@ def pin_unit_vectors(orc):
             assert np.array_equal(y, expect_w[:, k]), (dt, k)
 
 
+def pin_format_options_unit_vectors(orc):
+    # f16 weights with FP32 x: e_k picks column k exactly, and an FP32 x that
+    # is not a binary16 value (1 + 2^-20) scales it exactly
+    M, N = 4, 200
+    w = synth.random_case("f16x32", M, N, 8)
+    A = synth.weight_rows(w, 0, M)
+    Av = _f16_value(A)
+    for k in (0, 1, 100, 199):
+        e = np.zeros(N, dtype=np.float32)
+        e[k] = 1.0 + 2.0 ** -20
+        y, _ = orc.gemv("f16x32", A, e, M, N)
+        assert np.array_equal(y, Av[:, k] * (1.0 + 2.0 ** -20)), k
+    # one scale per row: row i's weights are s_i * q, whatever the column
+    q = synth.integers(9, 1, 0, M * N, -127, 127).reshape(M, N)
+    s_val = np.ldexp(1.0, np.arange(M) - 3)
+    for k in (0, 127, 128, 199):
+        e = np.zeros(N)
+        e[k] = 1.0
+        y, _ = orc.gemv("q8row", q.astype(np.int8), synth.to_f16_bits(e), M, N,
+                        scales=synth.to_f16_bits(s_val))
+        assert np.array_equal(y, s_val * q[:, k]), k
+
+
 def pin_int4_byte_table(orc):
     # one row, hand-built bytes: low nibble = even column, two's complement
     row = np.array([[0x21, 0x43, 0x8F, 0x7E, 0x09]], dtype=np.uint8)
@@ -167,11 +190,12 @@ def _exact_weights(dt, A, s_bits, M, N):
         for j in range(N):
             if dt == "f32":
                 W[i][j] = Fraction(float(A[i, j]))
-            elif dt == "f16":
+            elif dt in ("f16", "f16x32"):
                 W[i][j] = Fraction(float(np.uint16(A[i, j]).view(np.float16)))
             else:
-                sc = Fraction(float(np.uint16(s_bits[i, j // 128]).view(np.float16)))
-                if dt == "q8":
+                col = 0 if dt == "q8row" else j // 128
+                sc = Fraction(float(np.uint16(s_bits[i, col]).view(np.float16)))
+                if dt in ("q8", "q8row"):
                     code = int(A[i, j])
                 else:
                     byte = int(A[i, j // 2])
@@ -183,7 +207,7 @@ def _exact_weights(dt, A, s_bits, M, N):
 
 def pin_bruteforce_exact(orc):
     shapes = [(1, 1), (2, 3), (4, 8), (9, 33), (5, 130), (3, 257), (2, 64)]
-    for dt in ("f32", "f16", "q8", "q4"):
+    for dt in ("f32", "f16", "q8", "q4", "f16x32", "q8row"):
         for (M, N) in shapes:
             if dt == "q4" and N % 2:
                 continue
@@ -191,7 +215,7 @@ def pin_bruteforce_exact(orc):
             inp = synth.make(w)
             A, x, s = inp["A"], inp["x"], inp.get("scales")
             W = _exact_weights(dt, A, s, M, N)
-            xv = [Fraction(float(v)) for v in (x if dt == "f32" else x.view(np.float16))]
+            xv = [Fraction(float(v)) for v in (x if x.dtype == np.float32 else x.view(np.float16))]
             y, den = orc.gemv(dt, A, x, M, N, scales=s)
             for i in range(M):
                 ex = sum((W[i][j] * xv[j] for j in range(N)), Fraction(0))
@@ -219,6 +243,9 @@ def pin_counts(orc):
     assert int(2 / (0.5 + 2 / 128) * 100) / 100 == g["int4_cap_printed"]
     assert orc.bytes("q8", 4096, 14336) == 4096 * 14336 + 2 * 4096 * 112 + 2 * 14336 + 4 * 4096
     assert orc.flops(0, 5) == 0 and orc.flops(5, 0) == 0
+    # FP32 x: 4 bytes per element of x; one scale per row: 2 bytes per row
+    assert orc.bytes("f16x32", 4096, 14336) == 2 * 4096 * 14336 + 4 * 14336 + 4 * 4096
+    assert orc.bytes("q8row", 4096, 14336) == 4096 * 14336 + 2 * 4096 + 2 * 14336 + 4 * 4096
 
 
 def _f16(vals):
@@ -263,7 +290,7 @@ def pin_softmax_sums_and_brute_force(orc):
 
 
 PINS = [pin_dec16_all_patterns, pin_rowmajor_worked_example, pin_identity, pin_unit_vectors,
-        pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts,
+        pin_format_options_unit_vectors, pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts,
         pin_softmax_closed_forms, pin_softmax_sums_and_brute_force]
 
 
@@ -326,7 +353,8 @@ MUTANTS = {1: "int4 nibble order swapped", 2: "int4 read as offset-8",
            3: "scale group width 64", 4: "A read column-major",
            5: "binary16 subnormals decoded as normals", 6: "last column dropped",
            7: "scale row pitch floor(N/128)", 8: "softmax without the maximum subtracted",
-           9: "softmax sum missing its last term", 10: "softmax normalised by N"}
+           9: "softmax sum missing its last term", 10: "softmax normalised by N",
+           11: "per-row scale taken from row 0", 12: "FP32 x of f16 weights read as binary16"}
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[k] for k in sorted(MUTANTS)])

@@ -49,6 +49,7 @@ def test_workload_inputs_have_storage_shapes():
         assert rows.shape == (2, width), name
         x = synth.x_vector(w)
         assert x.shape == (w.N,)
-        assert x.dtype == (np.float32 if w.dtype == "f32" else np.uint16)
+        assert x.dtype == (np.float32 if w.dtype in ("f32", "f16x32") else np.uint16)
         if w.quantised:
-            assert synth.scale_rows(w, 0, 2).shape == (2, synth.n_groups(w.N))
+            g = 1 if w.dtype == "q8row" else synth.n_groups(w.N)
+            assert synth.scale_rows(w, 0, 2).shape == (2, g)
