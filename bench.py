@@ -51,16 +51,26 @@ ROTATE_MIN_BYTES = 256 << 20
 # ---------------------------------------------------------------------------
 
 def a_bytes(dtype: str, M: int, N: int) -> int:
-    per = {"f32": 4 * N, "f16": 2 * N, "q8": N, "q4": N // 2}[dtype]
+    per = {"f32": 4 * N, "f16": 2 * N, "q8": N, "q4": N // 2, "f16x32": 2 * N, "q8row": N}[dtype]
     return M * per
 
 
 def scale_bytes(dtype: str, M: int, N: int) -> int:
+    if dtype == "q8row":
+        return 2 * M
     return 2 * M * synth.n_groups(N) if dtype in ("q8", "q4") else 0
 
 
 def x_bytes(dtype: str, N: int) -> int:
-    return (4 if dtype == "f32" else 2) * N
+    return (4 if dtype in ("f32", "f16x32") else 2) * N
+
+
+def f16_weights(dtype: str) -> bool:
+    return dtype in ("f16", "f16x32")
+
+
+def f32_x(dtype: str) -> bool:
+    return dtype in ("f32", "f16x32")
 
 
 def algorithmic_bytes(dtype: str, M: int, N: int) -> int:
@@ -349,9 +359,11 @@ def run_ours(args):
             return torch.from_numpy(np.ascontiguousarray(arr).view(np.float16)).to(dev)
         return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
 
-    A0 = to_dev(inp["A"], "f16bits" if w.dtype == "f16" else "raw")
-    x = to_dev(inp["x"], "raw" if w.dtype == "f32" else "f16bits")
+    A0 = to_dev(inp["A"], "f16bits" if f16_weights(w.dtype) else "raw")
+    x = to_dev(inp["x"], "raw" if f32_x(w.dtype) else "f16bits")
     S0 = to_dev(inp["scales"], "f16bits") if w.quantised else None
+    if w.dtype == "q8row":
+        S0 = S0.reshape(-1)  # one scale per row: [M]
     wbytes = a_bytes(w.dtype, w.M, w.N) + scale_bytes(w.dtype, w.M, w.N)
     copies = rotation_copies(wbytes, l2)
     As = [A0] + [A0.clone() for _ in range(copies - 1)]
@@ -705,9 +717,11 @@ def run_profile(args):
     torch.cuda.set_device(0)
     w = synth.WORKLOADS[args.workload]
     inp = synth.make(w)
-    A = torch.from_numpy(inp["A"].view(np.float16) if w.dtype == "f16" else inp["A"]).cuda()
-    x = torch.from_numpy(inp["x"] if w.dtype == "f32" else inp["x"].view(np.float16)).cuda()
+    A = torch.from_numpy(inp["A"].view(np.float16) if f16_weights(w.dtype) else inp["A"]).cuda()
+    x = torch.from_numpy(inp["x"] if f32_x(w.dtype) else inp["x"].view(np.float16)).cuda()
     S = torch.from_numpy(inp["scales"].view(np.float16)).cuda() if w.quantised else None
+    if w.dtype == "q8row":
+        S = S.reshape(-1)
     if args.variant:
         vid = [v["id"] for v in mbg.variants(w.dtype) if v["name"] == args.variant]
         if not vid:

@@ -56,7 +56,13 @@ typedef enum {
 } gemv_status_t;
 
 /* Storage types, used by the variant-introspection calls. */
-typedef enum { GEMV_F32 = 0, GEMV_F16 = 1, GEMV_Q8 = 2, GEMV_Q4 = 3 } gemv_dtype_t;
+typedef enum {
+    GEMV_F32 = 0,
+    GEMV_F16 = 1,
+    GEMV_Q8 = 2,
+    GEMV_Q4 = 3,
+    GEMV_F16_X32 = 4 /* binary16 weights, FP32 x (gemv_f16_xf32) */
+} gemv_dtype_t;
 
 /*
  * FP32 GEMV.  A: float [M][N] row-major, x: float [N], y: float [M].
@@ -100,8 +106,36 @@ gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, 
                       const uint16_t *scales, void *stream);
 
 /*
- * Any of the four GEMVs (dtype: gemv_dtype_t) with launch flags.  scales is
- * ignored for FP32/FP16.
+ * FP16 weights with an FP32 x: A: binary16 [M][N], x: float [N], y: float
+ * [M].  Each weight is widened to FP32 and multiplied by x[j] in FP32.  x must
+ * be 4-byte aligned; the vectorised kernels need A and x 16-byte aligned and
+ * N a multiple of 8.
+ * "llama.cpp GEMV CUDA", implementation note (the hidden state may be kept in
+ * FP32 while the weights are FP16).
+ */
+gemv_status_t gemv_f16_xf32(const uint16_t *A, const float *x, float *y, int64_t M, int64_t N,
+                            void *stream);
+
+/*
+ * INT8 weight-only GEMV with ONE scale per row: y[i] = s[i] * sum_j q[i,j] *
+ * x[j], computed as sum_j (FP32(s[i]) * q[i,j]) * x[j].  A: int8 [M][N];
+ * row_scales: binary16 [M]; x: binary16 [N]; y: float [M].  Same results as
+ * gemv_q8 with every group scale of row i equal to s[i].  The bulk-copy
+ * pipeline is not used for this layout (a row's scales are not a 16-byte
+ * block); the row-tile and warp-per-row kernels are.
+ * "membound", section "The kernel decode actually runs: dequant GEMV" (the
+ * per-row scale of the page's kernel).
+ */
+gemv_status_t gemv_q8_rowscale(const int8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                               const uint16_t *row_scales, void *stream);
+/* gemv_q8_rowscale with the launch flags of gemv_ex (below). */
+gemv_status_t gemv_q8_rowscale_ex(const int8_t *A, const uint16_t *x, float *y, int64_t M,
+                                  int64_t N, const uint16_t *row_scales, unsigned flags,
+                                  void *stream);
+
+/*
+ * Any of the GEMVs above with 128-column scale groups (dtype: gemv_dtype_t)
+ * with launch flags.  scales is ignored for the unquantised types.
  *
  * GEMV_FLAG_OVERLAP_PRECEDING: the caller guarantees that A and scales are
  * not written by the kernel that precedes this call on `stream` (model
@@ -215,6 +249,12 @@ gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *inf
 int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N);
 gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,
                                int64_t M, int64_t N, const uint16_t *scales, void *stream);
+/* The same two calls for gemv_q8_rowscale (variant ids index the INT8 table;
+ * the bulk-copy variants return GEMV_ERR_UNSUPPORTED there). */
+int gemv_q8_rowscale_select_variant(const int8_t *A, const uint16_t *x, int64_t M, int64_t N);
+gemv_status_t gemv_q8_rowscale_run_variant(int variant, const int8_t *A, const uint16_t *x, float *y,
+                                           int64_t M, int64_t N, const uint16_t *row_scales,
+                                           void *stream);
 
 /*
  * Synchronises `stream`, reads and clears this device's status word.

@@ -7,7 +7,7 @@ library's CUDA kernels.  There is no CPU fallback: if the library cannot be
 built or loaded, every call raises.
 
 Function names match the C entry points: ``gemv_f32``, ``gemv_f16``,
-``gemv_q8``, ``gemv_q4``, ``gemv_probe_read``, ``gemv_dequant_q8``,
+``gemv_q8``, ``gemv_q4``, ``gemv_f16_xf32``, ``gemv_q8_rowscale``, ``gemv_probe_read``, ``gemv_dequant_q8``,
 ``gemv_dequant_q4``, ``gemv_run_variant`` ...  ``lib()`` returns the raw
 ctypes handle for callers that want to pass pointers themselves.
 """
@@ -19,8 +19,8 @@ import os
 import threading
 from typing import List, Optional
 
-F32, F16, Q8, Q4 = 0, 1, 2, 3
-DTYPES = {"f32": F32, "f16": F16, "q8": Q8, "q4": Q4}
+F32, F16, Q8, Q4, F16X32 = 0, 1, 2, 3, 4
+DTYPES = {"f32": F32, "f16": F16, "q8": Q8, "q4": Q4, "f16x32": F16X32}
 GROUP = 128
 
 STATUS = {0: "GEMV_OK", 1: "GEMV_ERR_INVALID_VALUE", 2: "GEMV_ERR_MISALIGNED",
@@ -58,6 +58,10 @@ def _declare(L):
         "gemv_f16": [vp, vp, vp, i64, i64, vp],
         "gemv_q8": [vp, vp, vp, i64, i64, vp, vp],
         "gemv_q4": [vp, vp, vp, i64, i64, vp, vp],
+        "gemv_f16_xf32": [vp, vp, vp, i64, i64, vp],
+        "gemv_q8_rowscale": [vp, vp, vp, i64, i64, vp, vp],
+        "gemv_q8_rowscale_run_variant": [i32, vp, vp, vp, i64, i64, vp, vp],
+        "gemv_q8_rowscale_ex": [vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_probe_read": [vp, ctypes.c_size_t, vp, i32, vp],
         "gemv_dequant_q8": [vp, vp, vp, i64, i64, vp],
         "gemv_dequant_q4": [vp, vp, vp, i64, i64, vp],
@@ -81,6 +85,8 @@ def _declare(L):
     L.gemv_variant_count.restype = i32
     L.gemv_select_variant.argtypes = [i32, vp, vp, i64, i64]
     L.gemv_select_variant.restype = i32
+    L.gemv_q8_rowscale_select_variant.argtypes = [vp, vp, i64, i64]
+    L.gemv_q8_rowscale_select_variant.restype = i32
     for name in ("gemv_softmax_variant_count", "gemv_probe_copy_variant_count"):
         getattr(L, name).argtypes = []
         getattr(L, name).restype = i32
@@ -200,6 +206,38 @@ def gemv_f16(A, x, y=None, stream=None):
     return y
 
 
+def gemv_f16_xf32(A, x, y=None, stream=None):
+    """y = A x with FP16 A [M, N] and an FP32 x [N]; FP32 arithmetic and output."""
+    torch = _torch()
+    M, N = _mn(A, F16X32)
+    _check(A, "A", _f16_types(), (M, N))
+    _check(x, "x", (torch.float32,), (N,), A.device)
+    y = _out(y, M, A.device)
+    _raise(lib().gemv_f16_xf32(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, _stream_ptr(stream)),
+           "gemv_f16_xf32")
+    return y
+
+
+def gemv_q8_rowscale(A, x, row_scales, y=None, stream=None, flags: int = 0):
+    """INT8 weights A [M, N] with one FP16 scale per row (row_scales [M]), FP16 x [N].
+
+    ``flags`` as for ``gemv_ex``."""
+    torch = _torch()
+    M, N = _mn(A, Q8)
+    _check(A, "A", (torch.int8,), (M, N))
+    _check(x, "x", _f16_types(), (N,), A.device)
+    _check(row_scales, "row_scales", _f16_types(), (M,), A.device)
+    y = _out(y, M, A.device)
+    if flags:
+        st = lib().gemv_q8_rowscale_ex(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                       row_scales.data_ptr(), flags, _stream_ptr(stream))
+    else:
+        st = lib().gemv_q8_rowscale(A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                    row_scales.data_ptr(), _stream_ptr(stream))
+    _raise(st, "gemv_q8_rowscale")
+    return y
+
+
 def _quant(fn_name, dtype, A, x, scales, y, stream):
     torch = _torch()
     M, N = _mn(A, dtype)
@@ -231,9 +269,10 @@ def gemv_ex(dtype: str, A, x, scales=None, y=None, stream=None, flags: int = 0):
     torch = _torch()
     dt = DTYPES[dtype]
     M, N = _mn(A, dt)
-    a_types = {F32: (torch.float32,), F16: _f16_types(), Q8: (torch.int8,), Q4: (torch.uint8,)}[dt]
+    a_types = {F32: (torch.float32,), F16: _f16_types(), Q8: (torch.int8,), Q4: (torch.uint8,),
+               F16X32: _f16_types()}[dt]
     _check(A, "A", a_types, tuple(A.shape))
-    _check(x, "x", (torch.float32,) if dt == F32 else _f16_types(), (N,), A.device)
+    _check(x, "x", (torch.float32,) if dt in (F32, F16X32) else _f16_types(), (N,), A.device)
     s_ptr = None
     if dt in (Q8, Q4):
         _check(scales, "scales", _f16_types(), (M, (N + GROUP - 1) // GROUP), A.device)
@@ -245,7 +284,12 @@ def gemv_ex(dtype: str, A, x, scales=None, y=None, stream=None, flags: int = 0):
 
 
 def gemv(dtype: str, A, x, scales=None, y=None, stream=None, overlap: bool = False):
-    """Dispatch on the storage type name: 'f32', 'f16', 'q8', 'q4'."""
+    """Dispatch on the storage type name: 'f32', 'f16', 'q8', 'q4', 'f16x32', 'q8row'.
+
+    'q8row' takes one scale per row (``scales`` of shape [M])."""
+    if dtype == "q8row":
+        return gemv_q8_rowscale(A, x, scales, y, stream,
+                                FLAG_OVERLAP_PRECEDING if overlap else 0)
     if overlap:
         return gemv_ex(dtype, A, x, scales, y, stream, FLAG_OVERLAP_PRECEDING)
     if dtype == "f32":
@@ -256,25 +300,37 @@ def gemv(dtype: str, A, x, scales=None, y=None, stream=None, overlap: bool = Fal
         return gemv_q8(A, x, scales, y, stream)
     if dtype == "q4":
         return gemv_q4(A, x, scales, y, stream)
+    if dtype == "f16x32":
+        return gemv_f16_xf32(A, x, y, stream)
     raise ValueError(dtype)
 
 
 def gemv_run_variant(dtype: str, variant: int, A, x, scales=None, y=None, stream=None):
-    """Run one compiled kernel variant (see ``variants``) on tensors."""
-    torch = _torch()
-    dt = DTYPES[dtype]
+    """Run one compiled kernel variant (see ``variants``) on tensors.
+
+    'q8row' (one scale per row) runs a variant of the INT8 table."""
+    dt = _table_dtype(dtype)
     M, N = _mn(A, dt)
     y = _out(y, M, A.device)
     s_ptr = scales.data_ptr() if scales is not None else None
-    _raise(lib().gemv_run_variant(dt, variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
-                                  s_ptr, _stream_ptr(stream)), f"gemv_run_variant({dtype}, {variant})")
-    del torch
+    if dtype == "q8row":
+        st = lib().gemv_q8_rowscale_run_variant(variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                                s_ptr, _stream_ptr(stream))
+    else:
+        st = lib().gemv_run_variant(dt, variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                    s_ptr, _stream_ptr(stream))
+    _raise(st, f"gemv_run_variant({dtype}, {variant})")
     return y
+
+
+def _table_dtype(dtype: str) -> int:
+    """Variant table of a storage type name ('q8row' shares the INT8 table)."""
+    return Q8 if dtype == "q8row" else DTYPES[dtype]
 
 
 def variants(dtype: str) -> List[dict]:
     L = lib()
-    dt = DTYPES[dtype]
+    dt = _table_dtype(dtype)
     out = []
     for k in range(L.gemv_variant_count(dt)):
         info = VariantInfo()
@@ -288,8 +344,10 @@ def variants(dtype: str) -> List[dict]:
 
 
 def select_variant(dtype: str, A, x) -> int:
-    dt = DTYPES[dtype]
+    dt = _table_dtype(dtype)
     M, N = _mn(A, dt)
+    if dtype == "q8row":
+        return lib().gemv_q8_rowscale_select_variant(A.data_ptr(), x.data_ptr(), M, N)
     return lib().gemv_select_variant(dt, A.data_ptr(), x.data_ptr(), M, N)
 
 

@@ -63,6 +63,7 @@ const Variant *table(int dtype, int *count)
     case DT_F16: return variants_f16(count);
     case DT_Q8: return variants_q8(count);
     case DT_Q4: return variants_q4(count);
+    case DT_F16X32: return variants_f16x32(count);
     default: *count = 0; return nullptr;
     }
 }
@@ -107,15 +108,21 @@ int64_t row_bytes_of(int dtype, int64_t N)
 {
     switch (dtype) {
     case DT_F32: return 4 * N;
-    case DT_F16: return 2 * N;
+    case DT_F16:
+    case DT_F16X32: return 2 * N;
     case DT_Q8: return N;
     default: return N / 2;
     }
 }
 
-int a_align(int dtype) { return dtype == DT_F32 ? 4 : dtype == DT_F16 ? 2 : 1; }
-int x_align(int dtype) { return dtype == DT_F32 ? 4 : 2; }
-int x_elem_bytes(int dtype) { return dtype == DT_F32 ? 4 : 2; }
+int a_align(int dtype) { return dtype == DT_F32 ? 4 : (dtype == DT_F16 || dtype == DT_F16X32) ? 2 : 1; }
+int x_align(int dtype) { return (dtype == DT_F32 || dtype == DT_F16X32) ? 4 : 2; }
+int x_elem_bytes(int dtype) { return (dtype == DT_F32 || dtype == DT_F16X32) ? 4 : 2; }
+bool is_quant(int dtype) { return dtype == DT_Q8 || dtype == DT_Q4; }
+
+// Scale grouping: 128 columns per scale, or one scale per row.
+enum { SCALES_GROUP128 = 0, SCALES_PER_ROW = 1 };
+int64_t scale_groups(int64_t N, int mode) { return mode == SCALES_PER_ROW ? 1 : (N + kGroup - 1) / kGroup; }
 
 // Common argument checks.  Returns GEMV_OK when the call may proceed.
 gemv_status_t validate(int dtype, const void *A, const void *x, const float *y, int64_t M,
@@ -140,13 +147,12 @@ gemv_status_t validate(int dtype, const void *A, const void *x, const float *y, 
 }
 
 // Dynamic shared memory of variant v for a row of N columns.
-size_t smem_bytes(const Variant &v, int dtype, int64_t N)
+size_t smem_bytes(const Variant &v, int dtype, int64_t N, int64_t groups)
 {
     if (v.kind == KIND_BULK) {
         const int64_t rb = row_bytes_of(dtype, N);
         const BulkLayout L = bulk_layout(v.stages, v.rows_per_group, v.warps * 32, rb,
-                                         N * x_elem_bytes(dtype), (N + kGroup - 1) / kGroup,
-                                         dtype == DT_Q8 || dtype == DT_Q4);
+                                         N * x_elem_bytes(dtype), groups, is_quant(dtype));
         return static_cast<size_t>(L.total);
     }
     if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)
@@ -157,8 +163,9 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N)
 
 // Can variant v serve this call?
 bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void *A, const void *x,
-                  int64_t M, int64_t N, const uint16_t *scales)
+                  int64_t M, int64_t N, const uint16_t *scales, int smode = SCALES_GROUP128)
 {
+    const int64_t groups = scale_groups(N, smode);
     if (v.xmode == XMODE_ELEM) {
         const int64_t blocks = (M + v.warps - 1) / v.warps;
         return blocks <= INT_MAX;
@@ -166,11 +173,11 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
     const int64_t rb = row_bytes_of(dtype, N);
     if (rb % 16 || !aligned(A, 16) || !aligned(x, 16)) return false;
     if (rb / 16 > INT_MAX / 64) return false;
-    if (static_cast<int64_t>(smem_bytes(v, dtype, N)) > d.max_smem) return false;
+    if (static_cast<int64_t>(smem_bytes(v, dtype, N, groups)) > d.max_smem) return false;
     if (v.kind == KIND_BULK) {
         // one stage (rows + their scales) is one transaction count of an mbarrier
-        const int64_t g = (N + kGroup - 1) / kGroup;
-        const bool quant = dtype == DT_Q8 || dtype == DT_Q4;
+        const int64_t g = groups;
+        const bool quant = is_quant(dtype);
         if (quant && ((2 * g) % 16 || !aligned(scales, 16))) return false;
         const int64_t tx = v.rows_per_group * (rb + (quant ? 2 * g : 0));
         if (tx >= (1 << 20)) return false;
@@ -226,7 +233,7 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
 // - rows too long for a tile, or x too long for shared memory: warp per row
 //   with a rolling buffer.
 int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x, int64_t M,
-                   int64_t N, const uint16_t *scales)
+                   int64_t N, const uint16_t *scales, int smode = SCALES_GROUP128)
 {
     int n = 0;
     const Variant *v = table(dtype, &n);
@@ -240,7 +247,7 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
         while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
         for (int k = 0; k < n; ++k) {
             if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == 8 &&
-                variant_fits(v[k], d, dtype, A, x, M, N, scales))
+                variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
                 return k;
         }
     }
@@ -248,20 +255,20 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
         int g = 1;
         while (static_cast<int64_t>(g) * kTileChunks < chunks) g *= 2;
         const int warps = g > 256 ? g / 32 : 8;
-        const bool via_l1 = (dtype == DT_F32 || dtype == DT_F16) && g >= 128;
+        const bool via_l1 = !is_quant(dtype) && g >= 128;
         int k = find_variant(dtype, g, via_l1 ? XMODE_L1 : XMODE_BULK, KIND_TILE, warps);
-        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales)) return k;
+        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);
-        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales)) return k;
+        if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
     }
     int k = small_x ? find_variant(dtype, 32, XMODE_BULK) : find_variant(dtype, 32, XMODE_L1);
-    if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N, scales))
+    if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
         k = find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     return k;
 }
 
 gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, int64_t M, int64_t N,
-                  const uint16_t *scales, void *stream, unsigned flags = 0)
+                  const uint16_t *scales, void *stream, unsigned flags = 0, int smode = SCALES_GROUP128)
 {
     gemv_status_t st = validate(dtype, A, x, y, M, N, scales);
     if (st != GEMV_OK) return st;
@@ -278,11 +285,11 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     DeviceState *d = current_device();
     if (!d) return GEMV_ERR_CUDA;
     if (vid < 0) {
-        vid = choose_variant(*d, dtype, A, x, M, N, scales);
+        vid = choose_variant(*d, dtype, A, x, M, N, scales, smode);
         if (vid < 0) return GEMV_ERR_UNSUPPORTED;
     }
     const Variant &v = tab[vid];
-    if (!variant_fits(v, *d, dtype, A, x, M, N, scales)) return GEMV_ERR_UNSUPPORTED;
+    if (!variant_fits(v, *d, dtype, A, x, M, N, scales, smode)) return GEMV_ERR_UNSUPPORTED;
 
     GemvArgs a{};
     a.A = A;
@@ -292,7 +299,15 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     a.M = M;
     a.N = N;
     a.row_bytes = row_bytes_of(dtype, N);
-    a.groups = (N + kGroup - 1) / kGroup;
+    a.groups = scale_groups(N, smode);
+    {
+        // chunk / column -> scale group: c >> scale_shift, j >> scale_elem_shift
+        const int epc = dtype == DT_Q4 ? 32 : dtype == DT_Q8 ? 16 : 8;
+        int lg = 0;
+        while ((1 << lg) < kGroup / epc) ++lg;
+        a.scale_shift = smode == SCALES_PER_ROW ? 30 : lg;
+        a.scale_elem_shift = smode == SCALES_PER_ROW ? 62 : 7;
+    }
     a.nchunks = static_cast<int>(a.row_bytes / 16);
     a.err = d->status;
     a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -300,7 +315,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     a.pdl = ((flags & GEMV_FLAG_OVERLAP_PRECEDING) && v.supports_pdl()) ? 1 : 0;
 
     int64_t blocks;
-    const size_t smem = smem_bytes(v, dtype, N);
+    const size_t smem = smem_bytes(v, dtype, N, a.groups);
     if (v.xmode == XMODE_ELEM) {
         blocks = (M + v.warps - 1) / v.warps;
     } else {
@@ -346,6 +361,26 @@ gemv_status_t gemv_q4(const uint8_t *A, const uint16_t *x, float *y, int64_t M, 
     return run(DT_Q4, -1, A, x, y, M, N, scales, stream);
 }
 
+gemv_status_t gemv_f16_xf32(const uint16_t *A, const float *x, float *y, int64_t M, int64_t N,
+                           void *stream)
+{
+    return run(DT_F16X32, -1, A, x, y, M, N, nullptr, stream);
+}
+
+gemv_status_t gemv_q8_rowscale(const int8_t *A, const uint16_t *x, float *y, int64_t M, int64_t N,
+                               const uint16_t *row_scales, void *stream)
+{
+    return run(DT_Q8, -1, A, x, y, M, N, row_scales, stream, 0, SCALES_PER_ROW);
+}
+
+gemv_status_t gemv_q8_rowscale_ex(const int8_t *A, const uint16_t *x, float *y, int64_t M,
+                                  int64_t N, const uint16_t *row_scales, unsigned flags,
+                                  void *stream)
+{
+    if (flags & ~static_cast<unsigned>(GEMV_FLAG_OVERLAP_PRECEDING)) return GEMV_ERR_INVALID_VALUE;
+    return run(DT_Q8, -1, A, x, y, M, N, row_scales, stream, flags, SCALES_PER_ROW);
+}
+
 gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t M, int64_t N,
                       const uint16_t *scales, unsigned flags, void *stream)
 {
@@ -378,14 +413,32 @@ gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *inf
     return GEMV_OK;
 }
 
-int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N)
+static int select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N, int smode)
 {
     if (dtype < 0 || dtype >= DT_COUNT || M <= 0 || N <= 0 || !A || !x) return -1;
     if (dtype == DT_Q4 && (N % 2)) return -1;
     if (!aligned(A, a_align(dtype)) || !aligned(x, x_align(dtype))) return -1;
     DeviceState *d = current_device();
     if (!d) return -1;
-    return choose_variant(*d, dtype, A, x, M, N, nullptr);
+    return choose_variant(*d, dtype, A, x, M, N, nullptr, smode);
+}
+
+int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N)
+{
+    return select_variant(dtype, A, x, M, N, SCALES_GROUP128);
+}
+
+int gemv_q8_rowscale_select_variant(const int8_t *A, const uint16_t *x, int64_t M, int64_t N)
+{
+    return select_variant(DT_Q8, A, x, M, N, SCALES_PER_ROW);
+}
+
+gemv_status_t gemv_q8_rowscale_run_variant(int variant, const int8_t *A, const uint16_t *x, float *y,
+                                           int64_t M, int64_t N, const uint16_t *row_scales,
+                                           void *stream)
+{
+    if (variant < 0) return GEMV_ERR_INVALID_VALUE;
+    return run(DT_Q8, variant, A, x, y, M, N, row_scales, stream, 0, SCALES_PER_ROW);
 }
 
 gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,

@@ -83,6 +83,7 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
         p.N = N;
         p.row_bytes = row_bytes;
         p.groups = groups;
+        p.scale_elem_shift = 7;  // 128 columns per scale
         const unsigned g = grid_for(M * N, 256);
         if (dtype == DT_Q8) dequant_elem_kernel<DT_Q8><<<g, 256, 0, s>>>(p, W);
         else dequant_elem_kernel<DT_Q4><<<g, 256, 0, s>>>(p, W);

@@ -209,6 +209,11 @@ template <> struct Fmt<DT_Q4> {
     static constexpr int XB = 2;
     static constexpr bool QUANT = true;
 };
+template <> struct Fmt<DT_F16X32> {
+    static constexpr int EPC = 8;
+    static constexpr int XB = 4;
+    static constexpr bool QUANT = false;
+};
 
 // Bytes of x that one 16-byte chunk of A multiplies.
 template <int DT> constexpr int x_chunk_bytes() { return Fmt<DT>::EPC * Fmt<DT>::XB; }
@@ -262,11 +267,14 @@ template <int DT>
 __device__ __forceinline__ void x_to_float(const uint4 (&xv)[x_chunk_vecs<DT>()],
                                            float (&xf)[Fmt<DT>::EPC])
 {
-    if constexpr (DT == DT_F32) {
-        xf[0] = __uint_as_float(xv[0].x);
-        xf[1] = __uint_as_float(xv[0].y);
-        xf[2] = __uint_as_float(xv[0].z);
-        xf[3] = __uint_as_float(xv[0].w);
+    if constexpr (Fmt<DT>::XB == 4) {
+#pragma unroll
+        for (int v = 0; v < x_chunk_vecs<DT>(); ++v) {
+            xf[4 * v + 0] = __uint_as_float(xv[v].x);
+            xf[4 * v + 1] = __uint_as_float(xv[v].y);
+            xf[4 * v + 2] = __uint_as_float(xv[v].z);
+            xf[4 * v + 3] = __uint_as_float(xv[v].w);
+        }
     } else {
 #pragma unroll
         for (int v = 0; v < x_chunk_vecs<DT>(); ++v) {
@@ -286,7 +294,7 @@ __device__ __forceinline__ void chunk_to_float(const uint4 a, float (&wf)[Fmt<DT
     if constexpr (DT == DT_F32) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) wf[k] = __uint_as_float(w[k]);
-    } else if constexpr (DT == DT_F16) {
+    } else if constexpr (DT == DT_F16 || DT == DT_F16X32) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) half2_bits_to_float(w[k], wf[2 * k], wf[2 * k + 1]);
     } else if constexpr (DT == DT_Q8) {
@@ -433,7 +441,7 @@ template <int DT>
 __device__ __forceinline__ void chunk_dot_mixed(const uint4 a, const uint4 (&xv)[x_chunk_vecs<DT>()],
                                                 float scale, float (&acc)[NACC])
 {
-    static_assert(DT != DT_F32, "FP32 weights take the FP32 path");
+    static_assert(Fmt<DT>::XB == 2, "an FP32 x takes the FP32 path");
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
     if constexpr (DT == DT_F16) {
         (void)scale;

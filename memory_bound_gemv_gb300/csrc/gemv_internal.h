@@ -7,7 +7,8 @@
 
 namespace mbg {
 
-enum { DT_F32 = 0, DT_F16 = 1, DT_Q8 = 2, DT_Q4 = 3, DT_COUNT = 4 };
+// Storage types.  DT_F16X32: binary16 weights with an FP32 x.
+enum { DT_F32 = 0, DT_F16 = 1, DT_Q8 = 2, DT_Q4 = 3, DT_F16X32 = 4, DT_COUNT = 5 };
 
 enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3 };
 
@@ -44,6 +45,8 @@ struct GemvArgs {
     unsigned int *err;        // device status word
     uint64_t wait_limit_ns;   // bound of every device-side wait
     int skip_x_copy;          // test hook: arm the barrier but issue no copy
+    int scale_shift;          // scale group of 16-byte chunk c: c >> scale_shift
+    int scale_elem_shift;     // scale group of column j: j >> scale_elem_shift
     int pdl;                  // launched with programmatic serialisation: stream the
                               // weights before waiting for the preceding kernel
 };
@@ -105,6 +108,7 @@ const Variant *variants_f32(int *count);
 const Variant *variants_f16(int *count);
 const Variant *variants_q8(int *count);
 const Variant *variants_q4(int *count);
+const Variant *variants_f16x32(int *count);
 
 // Probe kernels (gemv_probe.cu).
 struct ProbeVariant {

@@ -32,7 +32,6 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
     constexpr int GPW = 32 / LPR;
     constexpr int ROWS_PER_WARP = GPW * RPW;
     constexpr int ROWS_PER_BLOCK = WARPS * ROWS_PER_WARP;
-    constexpr int CHUNKS_PER_GROUP = kGroup / EPC;  // chunks sharing one scale
     static_assert(32 % LPR == 0, "lanes per row must divide the warp");
     static_assert(XMODE == XMODE_BULK || XMODE == XMODE_VEC || XMODE == XMODE_L1, "xmode");
 
@@ -87,7 +86,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
                 buf[r][u] = ld_stream16(rowp[r] + static_cast<size_t>(c) * 16);
-                if constexpr (F::QUANT) sbuf[r][u] = ld_half_as_float(srow[r] + c / CHUNKS_PER_GROUP);
+                if constexpr (F::QUANT) sbuf[r][u] = ld_half_as_float(srow[r] + (c >> p.scale_shift));
                 else sbuf[r][u] = 0.f;
             }
         }
@@ -143,7 +142,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
                     for (int r = 0; r < RPW; ++r) {
                         buf[r][u] = ld_stream16(rowp[r] + static_cast<size_t>(cn) * 16);
                         if constexpr (F::QUANT)
-                            sbuf[r][u] = ld_half_as_float(srow[r] + cn / CHUNKS_PER_GROUP);
+                            sbuf[r][u] = ld_half_as_float(srow[r] + (cn >> p.scale_shift));
                     }
                 }
 #pragma unroll
@@ -191,14 +190,13 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     constexpr bool WIDE = G > 32;                   // group spans several warps
     constexpr int GW = WIDE ? G / 32 : 1;           // warps per group
     constexpr int LW = WIDE ? 32 : G;               // shuffle width
-    constexpr int CHUNKS_PER_GROUP = kGroup / EPC;
     constexpr int NW = T / 32;
     constexpr int KB = kTileBatch;                  // tiles per deferred reduction
     constexpr int PART_BYTES = WIDE ? 2 * KB * NW * 4 : 0;
     constexpr int X_OFFSET = (16 + PART_BYTES + 15) / 16 * 16;
     static_assert(T % G == 0 && (G <= 32 ? 32 % G == 0 : G % 32 == 0), "group shape");
     static_assert(XMODE == XMODE_BULK || XMODE == XMODE_L1, "xmode");
-    static_assert(MATH == MATH_F32 || DT != DT_F32, "FP32 weights use FP32 math");
+    static_assert(MATH == MATH_F32 || Fmt<DT>::XB == 2, "an FP32 x uses FP32 math");
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
@@ -249,7 +247,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
             for (int k = 0; k < CPT; ++k) {
                 if (tg + k * G < nchunks) {
                     buf[k] = ld_stream16(rp + k * G * 16);
-                    if constexpr (F::QUANT) sb[k] = ld_half_as_float(sp + (tg + k * G) / CHUNKS_PER_GROUP);
+                    if constexpr (F::QUANT) sb[k] = ld_half_as_float(sp + ((tg + k * G) >> p.scale_shift));
                 }
             }
         }
@@ -384,8 +382,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     constexpr int XCB = x_chunk_bytes<DT>();
     constexpr int XV = x_chunk_vecs<DT>();
     constexpr int NW = T / 32;  // consumer warps
-    constexpr int CPG = kGroup / F::EPC;
-    static_assert(MATH == MATH_F32 || DT != DT_F32, "FP32 weights use FP32 math");
+    static_assert(MATH == MATH_F32 || Fmt<DT>::XB == 2, "an FP32 x uses FP32 math");
     static_assert(NW <= 32, "the producer warp adds one partial per consumer warp");
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -540,7 +537,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
                     const uint4 a = lds128(st + r * rb + c16);
                     float sc = 0.f;
                     if constexpr (F::QUANT)
-                        sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c / CPG));
+                        sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c >> p.scale_shift));
                     if constexpr (MATH == MATH_MIXED) {
                         chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
                     } else {
@@ -576,10 +573,10 @@ __device__ __forceinline__ float elem_weight(const GemvArgs &p, int64_t i, int64
     const unsigned char *row = static_cast<const unsigned char *>(p.A) + i * p.row_bytes;
     if constexpr (DT == DT_F32) {
         return __ldg(reinterpret_cast<const float *>(row) + j);
-    } else if constexpr (DT == DT_F16) {
+    } else if constexpr (DT == DT_F16 || DT == DT_F16X32) {
         return ld_half_as_float(reinterpret_cast<const uint16_t *>(row) + j);
     } else {
-        const float s = ld_half_as_float(p.scales + i * p.groups + j / kGroup);
+        const float s = ld_half_as_float(p.scales + i * p.groups + (j >> p.scale_elem_shift));
         int q;
         if constexpr (DT == DT_Q8) {
             q = static_cast<int>(static_cast<signed char>(__ldg(reinterpret_cast<const char *>(row) + j)));
@@ -595,7 +592,7 @@ __device__ __forceinline__ float elem_weight(const GemvArgs &p, int64_t i, int64
 template <int DT>
 __device__ __forceinline__ float elem_x(const GemvArgs &p, int64_t j)
 {
-    if constexpr (DT == DT_F32) return __ldg(static_cast<const float *>(p.x) + j);
+    if constexpr (Fmt<DT>::XB == 4) return __ldg(static_cast<const float *>(p.x) + j);
     else return ld_half_as_float(static_cast<const uint16_t *>(p.x) + j);
 }
 
@@ -692,9 +689,9 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
     Variant{DT, G, 1, CPT, T / 32, XM, NAME, &launch_tile<DT, G, CPT, T, XM, MATH>,             \
             &smem_limit_tile<DT, G, CPT, T, XM, MATH>, KIND_TILE, tile_x_offset<DT, G, CPT, T>(), \
             &occupancy_tile<DT, G, CPT, T, XM, MATH>, MATH, 0}
-// FP32 weights use FP32 arithmetic; the other types default to the mixed path.
+// An FP32 x uses FP32 arithmetic; binary16 x defaults to the mixed path.
 #define MBG_TILE(DT, G, CPT, T, XM, NAME) \
-    MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
+    MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
 
 template <int DT, int T, int RS, int S, int MATH>
 void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
@@ -721,7 +718,7 @@ cudaError_t occupancy_bulk(int *blocks, size_t smem)
             &smem_limit_bulk<DT, T, RS, S, MATH>, KIND_BULK, 0, &occupancy_bulk<DT, T, RS, S, MATH>, \
             MATH, S}
 #define MBG_BULK(DT, T, RS, S, NAME) \
-    MBG_BULK_M(DT, T, RS, S, ((DT) == DT_F32 ? MATH_F32 : MATH_MIXED), NAME)
+    MBG_BULK_M(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

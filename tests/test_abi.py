@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_four_gemv_entry_points():
     names = declared_functions()
-    for n in ("gemv_f32", "gemv_f16", "gemv_q8", "gemv_q4", "gemv_probe_read"):
+    for n in ("gemv_f32", "gemv_f16", "gemv_q8", "gemv_q4", "gemv_probe_read",
+              "gemv_f16_xf32", "gemv_q8_rowscale"):
         assert n in names
 
 
@@ -48,7 +49,7 @@ def test_status_strings():
 
 
 def test_variant_tables():
-    for dt in ("f32", "f16", "q8", "q4"):
+    for dt in ("f32", "f16", "q8", "q4", "f16x32"):
         vs = mbg.variants(dt)
         assert len(vs) >= 2
         assert any(v["xmode"] == "elem" for v in vs)
@@ -63,7 +64,8 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
 
 
 @pytest.mark.parametrize("fn,extra", [("gemv_f32", []), ("gemv_f16", []),
-                                      ("gemv_q8", [FAKE]), ("gemv_q4", [FAKE])])
+                                      ("gemv_q8", [FAKE]), ("gemv_q4", [FAKE]),
+                                      ("gemv_f16_xf32", []), ("gemv_q8_rowscale", [FAKE])])
 def test_validation_errors_without_device(fn, extra):
     L = mbg.lib()
     f = getattr(L, fn)
@@ -80,7 +82,9 @@ def test_validation_errors_without_device(fn, extra):
     assert f(FAKE, FAKE, FAKE + 2, 4, 8, *extra, None) == mbg.ERR_MISALIGNED
     # x not aligned to its element size
     assert f(FAKE, FAKE + 1, FAKE, 4, 8, *extra, None) == mbg.ERR_MISALIGNED
-    if fn in ("gemv_f32", "gemv_f16"):
+    if fn == "gemv_f16_xf32":
+        assert f(FAKE, FAKE + 2, FAKE, 4, 8, None) == mbg.ERR_MISALIGNED  # FP32 x
+    if fn in ("gemv_f32", "gemv_f16", "gemv_f16_xf32"):
         assert f(FAKE + 1, FAKE, FAKE, 4, 8, None) == mbg.ERR_MISALIGNED
     else:
         assert f(FAKE, FAKE, FAKE, 4, 8, None, None) == mbg.ERR_INVALID_VALUE  # scales NULL

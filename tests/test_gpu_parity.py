@@ -19,7 +19,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU container
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-DTYPES = ("f32", "f16", "q8", "q4")
+DTYPES = ("f32", "f16", "q8", "q4", "f16x32", "q8row")
 
 # (M, N): several tiles, ragged tails, short rows for the multi-row variants,
 # and row pitches that are / are not multiples of 16 bytes.
@@ -101,8 +101,10 @@ def test_edge_sizes(dtype):
     mbg.gemv(dtype, A0, t["x"], t.get("scales")[:0] if "scales" in t else None, y=y[:0])
     # N == 0: y = 0
     L = mbg.lib()
-    dt = mbg.DTYPES[dtype]
-    st = L.gemv_run_variant(dt, 0, 0, 0, y.data_ptr(), 3, 0, None, None)
+    if dtype == "q8row":
+        st = L.gemv_q8_rowscale_run_variant(0, 0, 0, y.data_ptr(), 3, 0, None, None)
+    else:
+        st = L.gemv_run_variant(mbg.DTYPES[dtype], 0, 0, 0, y.data_ptr(), 3, 0, None, None)
     assert st == mbg.OK
     torch.cuda.synchronize()
     assert y.tolist() == [0.0, 0.0, 0.0]
@@ -153,6 +155,8 @@ def _eye_inputs(dtype, n):
     x = synth.normal(3, 2, 0, n, 1.0)
     if dtype == "f32":
         return {"A": eye.astype(np.float32), "x": x.astype(np.float32)}, x.astype(np.float32).astype(np.float64)
+    if dtype == "f16x32":
+        return {"A": synth.to_f16_bits(eye), "x": x.astype(np.float32)}, x.astype(np.float32).astype(np.float64)
     xb = synth.to_f16_bits(x)
     xv = xb.view(np.float16).astype(np.float64)
     ones = np.full((n, synth.n_groups(n)), 0x3C00, dtype=np.uint16)
@@ -160,6 +164,8 @@ def _eye_inputs(dtype, n):
         return {"A": synth.to_f16_bits(eye), "x": xb}, xv
     if dtype == "q8":
         return {"A": eye.astype(np.int8), "x": xb, "scales": ones}, xv
+    if dtype == "q8row":
+        return {"A": eye.astype(np.int8), "x": xb, "scales": ones[:, :1]}, xv
     return {"A": synth.pack_int4(eye.astype(np.int64)), "x": xb, "scales": ones}, xv
 
 
@@ -244,7 +250,9 @@ def test_runs_on_a_side_stream():
 
 
 def test_tolerances_are_the_stated_ones():
-    assert TOL == {"f32": 1e-5, "f16": 2e-3, "q8": 2e-3, "q4": 2e-3}
+    # FP32 arithmetic 1e-5, FP16 / quantised 2e-3; FP16 weights with an FP32 x
+    # are multiplied and summed in FP32, so they take the FP32 bound
+    assert TOL == {"f32": 1e-5, "f16": 2e-3, "q8": 2e-3, "q4": 2e-3, "f16x32": 1e-5, "q8row": 2e-3}
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -309,3 +317,29 @@ def test_overlapped_chain_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert_close("f32", y2.cpu().numpy(), y2_ref, den, "overlapped chain in a graph")
     assert mbg.gemv_get_device_error() == mbg.OK
+
+
+def test_row_scales_equal_broadcast_group_scales():
+    """One scale per row gives the same bits as equal group scales, per variant."""
+    M, N = 300, 4160
+    w = synth.random_case("q8row", M, N, 71)
+    inp = synth.make(w)
+    t = upload("q8row", inp)
+    groups = t["scales"].reshape(M, 1).expand(M, synth.n_groups(N)).contiguous()
+    compared = 0
+    for v in mbg.variants("q8"):
+        try:
+            y_row = mbg.gemv_run_variant("q8row", v["id"], t["A"], t["x"], t["scales"])
+        except mbg.GemvError as e:
+            # the bulk pipeline never takes row scales; the others refuse only
+            # shapes they refuse with group scales too
+            assert e.status == mbg.ERR_UNSUPPORTED, v["name"]
+            if v["kind"] != "bulk":
+                with pytest.raises(mbg.GemvError):
+                    mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
+            continue
+        y_grp = mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
+        torch.cuda.synchronize()
+        assert torch.equal(y_row, y_grp), v["name"]
+        compared += 1
+    assert compared >= 5
