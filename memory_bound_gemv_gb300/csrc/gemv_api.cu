@@ -178,7 +178,8 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
         // one stage (rows + their scales) is one transaction count of an mbarrier
         const int64_t g = groups;
         const bool quant = is_quant(dtype);
-        if (quant && ((2 * g) % 16 || !aligned(scales, 16))) return false;
+        // staged scales: one bulk copy per stage; one scale per row: read directly
+        if (quant && g > 1 && ((2 * g) % 16 || !aligned(scales, 16))) return false;
         const int64_t tx = v.rows_per_group * (rb + (quant ? 2 * g : 0));
         if (tx >= (1 << 20)) return false;
         return true;  // persistent grid
@@ -226,10 +227,12 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
 
 // The automatic choice (measured on GB300 over the workload families):
 // - layouts the vector kernels cannot take: element-wise kernel;
-// - INT8: the bulk-copy pipeline, with about 16 KB of rows per stage;
+// - INT8, and INT4 rows of at least 4 KB: the bulk-copy pipeline, with
+//   8-16 KB of rows per stage;
 // - otherwise row tiles with the narrowest group that requests a whole row at
 //   once; x through L1 for groups of 128 threads or more (FP32/FP16 rows of
-//   at least 8 KB), in shared memory below that;
+//   at least 8 KB), in shared memory below that and for an FP32 x of FP16
+//   weights;
 // - rows too long for a tile, or x too long for shared memory: warp per row
 //   with a rolling buffer.
 int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x, int64_t M,
@@ -242,7 +245,10 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if (!vec_ok) return find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     const int64_t chunks = rb / 16;
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
-    if (dtype == DT_Q8 && small_x) {
+    // the quantised types are bound by instruction issue: the bulk-copy
+    // pipeline (no load instructions for A) wins for INT8, and for INT4 rows
+    // of 4 KB or more; shorter INT4 rows do better in row tiles
+    if ((dtype == DT_Q8 || (dtype == DT_Q4 && rb >= 4096)) && small_x) {
         int rs = 1;
         while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
         for (int k = 0; k < n; ++k) {
@@ -255,7 +261,7 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
         int g = 1;
         while (static_cast<int64_t>(g) * kTileChunks < chunks) g *= 2;
         const int warps = g > 256 ? g / 32 : 8;
-        const bool via_l1 = !is_quant(dtype) && g >= 128;
+        const bool via_l1 = (dtype == DT_F32 || dtype == DT_F16) && g >= 128;
         int k = find_variant(dtype, g, via_l1 ? XMODE_L1 : XMODE_BULK, KIND_TILE, warps);
         if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);

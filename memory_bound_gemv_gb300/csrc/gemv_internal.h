@@ -98,7 +98,8 @@ __host__ __device__ inline BulkLayout bulk_layout(int S, int RS, int T, int64_t 
     L.stage = L.x + round16(x_bytes);
     L.stage_bytes = static_cast<int>(RS * row_bytes);
     L.scale = L.stage + S * L.stage_bytes;
-    L.scale_bytes = quant ? round16(RS * 2 * groups) : 0;
+    // one scale per row (groups == 1) is read from global memory, not staged
+    L.scale_bytes = (quant && groups > 1) ? round16(RS * 2 * groups) : 0;
     L.total = L.scale + S * L.scale_bytes;
     return L;
 }

@@ -19,6 +19,7 @@
 #pragma once
 
 #include "gemv_device.cuh"
+#include <type_traits>
 
 namespace mbg {
 
@@ -406,12 +407,13 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         const int64_t r0 = (blockIdx.x + it * grid) * RS;
         const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
         const uint32_t bytes = static_cast<uint32_t>(rows * p.row_bytes);
-        const uint32_t sbytes = F::QUANT ? static_cast<uint32_t>(rows * 2 * p.groups) : 0u;
+        const bool stage_scales = F::QUANT && p.groups > 1;
+        const uint32_t sbytes = stage_scales ? static_cast<uint32_t>(rows * 2 * p.groups) : 0u;
         const uint32_t b = smem_addr(&full[slot]);
         mbar_arrive_expect_tx(b, bytes + sbytes);
         bulk_copy_g2s(smem_addr(smem + L.stage + slot * L.stage_bytes),
                       static_cast<const unsigned char *>(p.A) + r0 * p.row_bytes, bytes, b);
-        if constexpr (F::QUANT)
+        if (stage_scales)
             bulk_copy_g2s(smem_addr(smem + L.scale + slot * L.scale_bytes), p.scales + r0 * p.groups,
                           sbytes, b);
     };
@@ -523,30 +525,47 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         for (int r = 0; r < RS; ++r)
 #pragma unroll
             for (int k = 0; k < NACC; ++k) acc[r][k] = 0.f;
+        // ROW_SCALE: one scale per row, read once per tile from global memory
+        auto dot_rows = [&](auto row_scale) {
+            constexpr bool ROW_SCALE = decltype(row_scale)::value;
+            float rsc[ROW_SCALE ? RS : 1];
+            if constexpr (ROW_SCALE) {
+#pragma unroll
+                for (int r = 0; r < RS; ++r) rsc[r] = r < rows ? ld_half_as_float(p.scales + r0 + r) : 0.f;
+            }
 #pragma unroll 2
-        for (int c = tid; c < nchunks; c += T) {
-            const uint32_t c16 = static_cast<uint32_t>(c) * 16u;
-            uint4 xv[XV];
+            for (int c = tid; c < nchunks; c += T) {
+                const uint32_t c16 = static_cast<uint32_t>(c) * 16u;
+                uint4 xv[XV];
 #pragma unroll
-            for (int v = 0; v < XV; ++v) xv[v] = lds128(xa + v * xstride + c16);
-            float xf[MATH == MATH_F32 ? F::EPC : 1];
-            if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
+                for (int v = 0; v < XV; ++v) xv[v] = lds128(xa + v * xstride + c16);
+                float xf[MATH == MATH_F32 ? F::EPC : 1];
+                if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
-            for (int r = 0; r < RS; ++r) {
-                if (r < rows) {
-                    const uint4 a = lds128(st + r * rb + c16);
-                    float sc = 0.f;
-                    if constexpr (F::QUANT)
-                        sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c >> p.scale_shift));
-                    if constexpr (MATH == MATH_MIXED) {
-                        chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
-                    } else {
-                        float wf[F::EPC];
-                        chunk_to_float<DT>(a, wf);
-                        chunk_fma<DT>(wf, xf, sc, acc[r]);
+                for (int r = 0; r < RS; ++r) {
+                    if (r < rows) {
+                        const uint4 a = lds128(st + r * rb + c16);
+                        float sc = 0.f;
+                        if constexpr (ROW_SCALE)
+                            sc = rsc[r];
+                        else if constexpr (F::QUANT)
+                            sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c >> p.scale_shift));
+                        if constexpr (MATH == MATH_MIXED) {
+                            chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
+                        } else {
+                            float wf[F::EPC];
+                            chunk_to_float<DT>(a, wf);
+                            chunk_fma<DT>(wf, xf, sc, acc[r]);
+                        }
                     }
                 }
             }
+        };
+        if constexpr (F::QUANT) {
+            if (p.groups == 1) dot_rows(std::true_type{});
+            else dot_rows(std::false_type{});
+        } else {
+            dot_rows(std::false_type{});
         }
         float *pp = part + slot * NW * RS;
 #pragma unroll

@@ -8,8 +8,8 @@ namespace mbg {
 
 static const Variant kTableQ8[] = {
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
-    MBG_BULK(DT_Q8, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),
+    MBG_BULK(DT_Q8, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q8, 512, 1, 4, "bulk_t512_r1_s4"),
     MBG_BULK(DT_Q8, 256, 2, 4, "bulk_t256_r2_s4"),
     MBG_BULK(DT_Q8, 512, 2, 4, "bulk_t512_r2_s4"),

@@ -324,22 +324,29 @@ def test_row_scales_equal_broadcast_group_scales():
     M, N = 300, 4160
     w = synth.random_case("q8row", M, N, 71)
     inp = synth.make(w)
+    y_ref, den = reference("q8row", inp, M, N)
     t = upload("q8row", inp)
     groups = t["scales"].reshape(M, 1).expand(M, synth.n_groups(N)).contiguous()
-    compared = 0
+    compared = bulk = 0
     for v in mbg.variants("q8"):
         try:
             y_row = mbg.gemv_run_variant("q8row", v["id"], t["A"], t["x"], t["scales"])
         except mbg.GemvError as e:
-            # the bulk pipeline never takes row scales; the others refuse only
-            # shapes they refuse with group scales too
+            # a variant refuses row scales only where it refuses the shape
             assert e.status == mbg.ERR_UNSUPPORTED, v["name"]
-            if v["kind"] != "bulk":
-                with pytest.raises(mbg.GemvError):
-                    mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
+            with pytest.raises(mbg.GemvError):
+                mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
             continue
-        y_grp = mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
+        torch.cuda.synchronize()
+        assert_close("q8row", y_row.cpu().numpy(), y_ref, den, v["name"])
+        bulk += v["kind"] == "bulk"
+        try:
+            y_grp = mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], groups)
+        except mbg.GemvError as e:
+            # 33 group scales per row (66 bytes) cannot be bulk-copied
+            assert e.status == mbg.ERR_UNSUPPORTED and v["kind"] == "bulk", v["name"]
+            continue
         torch.cuda.synchronize()
         assert torch.equal(y_row, y_grp), v["name"]
         compared += 1
-    assert compared >= 5
+    assert compared >= 5 and bulk >= 1
