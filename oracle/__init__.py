@@ -21,6 +21,10 @@ the pages it follows in the C file's header:
 * row softmax -- "membound", section "Bonus kernel: online softmax" (the
   oracle is the plain definition; the page's online update reaches the same
   value up to rounding).
+* symmetric INT8 / INT4 weight quantisation and its squared error --
+  "membound", section "The kernel decode actually runs: dequant GEMV" (scale
+  max|w|/127 per row or per 128 columns, max|w|/7 per 128 columns for INT4;
+  FP32 arithmetic, FP16 scales rounded to nearest even).
 
 Every function is pinned by ``tests/test_oracle.py`` against values fixed by
 the pages or by mathematics (worked example, identity, unit vectors, all-ones
@@ -100,6 +104,12 @@ class Oracle:
         L.oracle_mutant_id.restype = i32
         L.oracle_softmax_f16.restype = i32
         L.oracle_softmax_f16.argtypes = [vp, i64, i64, vp, i64, vp, i32]
+        L.oracle_enc16.restype = ctypes.c_uint16
+        L.oracle_enc16.argtypes = [ctypes.c_float]
+        L.oracle_enc16_array.restype = None
+        L.oracle_enc16_array.argtypes = [vp, vp, i64]
+        L.oracle_quantize.restype = i32
+        L.oracle_quantize.argtypes = [i32, i32, i32, vp, i64, i64, vp, vp, vp]
         self._L = L
 
     # -- binary16 --------------------------------------------------------
@@ -109,6 +119,37 @@ class Oracle:
         out = np.empty(b.shape, dtype=np.float64)
         self._L.oracle_dec16_array(b.ctypes.data, out.ctypes.data, b.size)
         return out
+
+    def enc16(self, values) -> np.ndarray:
+        """float32 values -> IEEE binary16 bit patterns, nearest even (own encoder)."""
+        f = np.ascontiguousarray(np.asarray(values, dtype=np.float32))
+        out = np.empty(f.shape, dtype=np.uint16)
+        self._L.oracle_enc16_array(f.ctypes.data, out.ctypes.data, f.size)
+        return out
+
+    # -- quantiser ---------------------------------------------------------
+    def quantize(self, dtype: str, W, M: int, N: int):
+        """Symmetric quantisation of W [M, N] for 'q8', 'q8row' or 'q4'.
+
+        W: float32 values, or uint16 binary16 bit patterns.  Returns (codes,
+        scales, sq_err): int8 [M, N] or packed uint8 [M, N/2]; FP16 bits
+        [M, groups] ([M, 1] for 'q8row'); sum of squared errors (double).
+        """
+        W = np.ascontiguousarray(W)
+        w_kind = 1 if W.dtype == np.uint16 else 0
+        if w_kind == 0 and W.dtype != np.float32:
+            raise ValueError("W must be float32 or binary16 bits")
+        bits = 4 if dtype == "q4" else 8
+        per_row = 1 if dtype == "q8row" else 0
+        groups = 0 if N == 0 else (1 if per_row else (N + 127) // 128)
+        A = np.zeros((M, N // 2 if bits == 4 else N), dtype=np.uint8 if bits == 4 else np.int8)
+        S = np.zeros((M, groups), dtype=np.uint16)
+        err = ctypes.c_double(0.0)
+        rc = self._L.oracle_quantize(bits, per_row, w_kind, W.ctypes.data, M, N, A.ctypes.data,
+                                     S.ctypes.data, ctypes.addressof(err))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments of {dtype} quantize")
+        return A, S, err.value
 
     # -- GEMV --------------------------------------------------------------
     def gemv(self, dtype: str, A, x, M: int, N: int, scales=None,

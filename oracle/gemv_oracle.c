@@ -44,7 +44,8 @@
  * generalised per storage type as bytes(A) + bytes(scales) + bytes(x) + 4M.
  *
  * The file also holds the row softmax of the same pages' second memory-bound
- * decode kernel (see oracle_softmax_f16).
+ * decode kernel (see oracle_softmax_f16) and the symmetric weight quantiser
+ * that produces the INT8 / INT4 operands (see oracle_quantize).
  *
  * Built with ORACLE_MUTANT=k (k > 0) it contains one deliberate mistake; the
  * test-suite builds those variants to show that its pins catch each one.
@@ -52,6 +53,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <string.h>
 
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
@@ -345,6 +347,140 @@ int oracle_softmax_f16(const uint16_t *x, int64_t M, int64_t N, const int64_t *r
 #endif
         for (int64_t j = 0; j < N; ++j) yi[j] = exp(oracle_dec16(xi[j]) - m) / sum;
     }
+    return 0;
+}
+
+/* ---- symmetric weight quantisation -----------------------------------------
+ *
+ * "membound", section "The kernel decode actually runs: dequant GEMV": INT8
+ * weights with a symmetric scale per row, INT4 with a symmetric scale per
+ * group of 128 columns, and the quantisation RMSE of U[-1,1] weights reported
+ * next to the kernels (about 2.3e-3 for INT8, 4.1e-2 for INT4).  Those two
+ * figures fix the scale as max|w| / 127 and max|w| / 7: rounding to the
+ * nearest code leaves a uniform error of RMS s / sqrt(12), i.e.
+ * (1/127)/sqrt(12) = 2.27e-3 and (0.992/7)/sqrt(12) = 4.09e-2 (0.992 being the
+ * expected maximum of 128 uniform magnitudes).
+ *
+ * The page does not state the arithmetic; it is read as FP32 throughout, one
+ * group at a time:
+ *   a   = max |w| over the group                 (exact)
+ *   s   = a / qmax                               (binary32 division, nearest even)
+ *   s16 = binary16(s), nearest even; an overflow to +inf is replaced by 65504
+ *   q   = clamp(rint(w / s16), -qmax, qmax)      (binary32 division; rint ties to even)
+ *         and q = 0 where s16 == 0 or w is NaN
+ * A group is 128 columns of a row (the last one may be shorter) or a whole
+ * row (per_row).  Codes are stored as the GEMV reads them: int8 [M][N], or
+ * int4 two per byte with the even column in the low nibble ([M][N/2]).
+ * scales: binary16 bits [M][groups].  *sq_err = sum over all weights of
+ * (w - s16 * q)^2, in double.
+ */
+
+/* binary32 -> binary16 bit pattern, round to nearest, ties to even, written
+ * from the IEEE 754 definition (10 fraction bits, exponent bias 15,
+ * subnormals with unit 2^-24). */
+uint16_t oracle_enc16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)(sign | 0x7E00u); /* NaN */
+    if ((u & 0x7FFFFFFFu) == 0x7F800000u) return (uint16_t)(sign | 0x7C00u); /* inf */
+    const double v = fabs((double)f);
+    if (v < ldexp(1.0, -14)) {
+        /* subnormal range: integer multiple of 2^-24 (1024 becomes the
+         * smallest normal, whose pattern is the same integer) */
+#if ORACLE_MUTANT == 16
+        const double t = floor(ldexp(v, 24)); /* truncation instead of rounding */
+#else
+        const double t = nearbyint(ldexp(v, 24));
+#endif
+        return (uint16_t)(sign | (uint16_t)t);
+    }
+    int e;
+    frexp(v, &e);       /* v = m * 2^e, m in [0.5, 1) */
+    e -= 1;             /* v = (1.f) * 2^e */
+#if ORACLE_MUTANT == 16
+    double t = floor(ldexp(v, 10 - e));
+#else
+    double t = nearbyint(ldexp(v, 10 - e)); /* in [1024, 2048] */
+#endif
+    if (t >= 2048.0) {
+        t = 1024.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(t - 1024.0));
+}
+
+void oracle_enc16_array(const float *f, uint16_t *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_enc16(f[k]);
+}
+
+/* w_kind: 0 = FP32 weights, 1 = binary16 bit patterns (widened exactly). */
+static float w_in(int w_kind, const void *W, int64_t k)
+{
+    if (w_kind == 0) return ((const float *)W)[k];
+    return (float)oracle_dec16(((const uint16_t *)W)[k]);
+}
+
+int oracle_quantize(int bits, int per_row, int w_kind, const void *W, int64_t M, int64_t N,
+                    void *A, uint16_t *scales, double *sq_err)
+{
+    if ((bits != 8 && bits != 4) || (w_kind != 0 && w_kind != 1) || M < 0 || N < 0) return -1;
+    if (bits == 4 && (per_row || N % 2)) return -1;
+    if (M > 0 && N > 0 && (!W || !A || !scales)) return -1;
+#if ORACLE_MUTANT == 13
+    const float qmax = bits == 8 ? 127.0f : 8.0f; /* INT4 scale by 8 */
+#else
+    const float qmax = bits == 8 ? 127.0f : 7.0f;
+#endif
+#if ORACLE_MUTANT == 15
+    const int64_t width = per_row ? N : 64; /* groups of 64 columns */
+#else
+    const int64_t width = per_row ? N : ORACLE_GROUP;
+#endif
+    const int64_t groups = N == 0 ? 0 : (per_row ? 1 : n_groups(N));
+    double err = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t g = 0; g < groups; ++g) {
+            const int64_t j0 = g * width;
+            const int64_t j1 = j0 + width < N ? j0 + width : N;
+            float a = 0.0f;
+            for (int64_t j = j0; j < j1; ++j) {
+                const float m = fabsf(w_in(w_kind, W, i * N + j));
+                if (m > a) a = m;
+            }
+            const float s = a / qmax;
+            uint16_t s16 = oracle_enc16(s);
+            if (s16 == 0x7C00u) s16 = 0x7BFFu;
+            scales[i * groups + g] = s16;
+            const float sf = (float)oracle_dec16(s16);
+            for (int64_t j = j0; j < j1; ++j) {
+                const float w = w_in(w_kind, W, i * N + j);
+                float q = 0.0f;
+                if (sf != 0.0f && w == w) {
+#if ORACLE_MUTANT == 14
+                    q = truncf(w / sf); /* truncation instead of rounding */
+#else
+                    q = rintf(w / sf);
+#endif
+                    q = q > qmax ? qmax : (q < -qmax ? -qmax : q);
+                }
+                const int code = (int)q;
+                if (bits == 8) {
+                    ((int8_t *)A)[i * N + j] = (int8_t)code;
+                } else {
+                    uint8_t *b = (uint8_t *)A + i * (N / 2) + j / 2;
+                    const uint8_t nib = (uint8_t)(code & 0xF);
+                    *b = (j % 2) ? (uint8_t)((*b & 0x0F) | (nib << 4)) : (uint8_t)((*b & 0xF0) | nib);
+                }
+                const double d = (double)w - (double)sf * (double)code;
+                err += d * d;
+            }
+        }
+    }
+    if (sq_err) *sq_err = err;
     return 0;
 }
 

@@ -289,9 +289,112 @@ def pin_softmax_sums_and_brute_force(orc):
     del w
 
 
+# ---------------------------------------------------------------------------
+# quantiser pins
+# ---------------------------------------------------------------------------
+
+def _f32(v):
+    return np.asarray(v, dtype=np.float32)
+
+
+def pin_enc16_against_numpy(orc):
+    # every binary16 value, the midpoints between neighbours (ties), one
+    # float32 ulp either side of each midpoint, the overflow edge and a random
+    # spread from the subnormal range up
+    h = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    vals = h.view(np.float16).astype(np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2.0
+    m32 = _f32(mids)
+    around = np.concatenate([m32, np.nextafter(m32, np.float32(np.inf)),
+                             np.nextafter(m32, np.float32(0))])
+    rnd = _f32(np.ldexp(synth.uniform(4, 1, 0, 20000, 1.0, 2.0), synth.integers(4, 2, 0, 20000, -30, 16)))
+    edge = _f32([65504.0, 65519.99, 65520.0, 70000.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                 2.0 ** -26, 0.0, -0.0, np.inf, -np.inf])
+    f = np.concatenate([_f32(vals), around, rnd, edge])
+    f = np.concatenate([f, -f])
+    ours = orc.enc16(f)
+    with np.errstate(over="ignore"):
+        ref = f.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+    assert orc.enc16(_f32([np.nan]))[0] & 0x7FFF > 0x7C00
+
+
+def pin_quantize_page_rmse(orc):
+    g = _golden("quantization_rmse.json")
+    M, N = 256, 4096
+    W = _f32(synth.uniform(21, 1, 0, M * N, -1.0, 1.0).reshape(M, N))
+    _, _, e8 = orc.quantize("q8row", W, M, N)
+    _, _, e4 = orc.quantize("q4", W, M, N)
+    r8, r4 = (e8 / W.size) ** 0.5, (e4 / W.size) ** 0.5
+    assert float(f"{r8:.1e}") == g["q8_per_row_rmse"], r8
+    assert float(f"{r4:.1e}") == g["q4_group128_rmse"], r4
+
+
+def pin_quantize_closed_forms(orc):
+    # a group on the code grid: w = k * 0.25 with max 7 * 0.25 -> s = 0.25, codes k, no error
+    k = np.arange(-7, 8)
+    row = np.concatenate([k, np.zeros(128 - k.size)]) * 0.25
+    A, S, e = orc.quantize("q4", _f32([row]), 1, 128)
+    assert S[0, 0] == 0x3400 and e == 0.0  # binary16 0.25
+    W = orc.dequant("q4", A, S, 1, 128)
+    assert np.array_equal(W[0], row)
+    # ties go to the even code: s = 0.5 (max 3.5 = 7 s); 0.25 -> 0, 0.75 -> 2,
+    # 1.25 -> 2, -0.75 -> -2, -1.75 -> -4
+    row = np.zeros(128)
+    row[:6] = [3.5, 0.25, 0.75, 1.25, -0.75, -1.75]
+    A, S, _ = orc.quantize("q4", _f32([row]), 1, 128)
+    assert S[0, 0] == 0x3800
+    assert list(orc.dequant("q4", A, S, 1, 128)[0, :6] / 0.5) == [7, 0, 2, 2, -2, -4]
+    # an all-zero group: scale 0, codes 0; INT8 per row: the largest magnitude maps to +-127
+    W = _f32(synth.uniform(22, 1, 0, 3 * 300, -2.0, 2.0).reshape(3, 300))
+    W[1, 128:256] = 0.0
+    A, S, _ = orc.quantize("q8", W, 3, 300)
+    assert S[1, 1] == 0 and not np.any(A[1, 128:256])
+    A, S, _ = orc.quantize("q8row", W, 3, 300)
+    for i in range(3):
+        assert abs(int(A[i, np.argmax(np.abs(W[i]))])) == 127
+
+
+def pin_quantize_invariants(orc):
+    M, N = 5, 1000
+    W = _f32(synth.normal(23, 1, 0, M * N, 0.05).reshape(M, N))
+    for dt, qmax in (("q8", 127), ("q8row", 127), ("q4", 7)):
+        A, S, e = orc.quantize(dt, W, M, N)
+        width = N if dt == "q8row" else 128
+        # scales: binary16 of (FP32 max|w| / qmax), by numpy's own arithmetic
+        amax = np.array([[np.abs(W[i, g * width:(g + 1) * width]).max() for g in range(S.shape[1])]
+                         for i in range(M)], dtype=np.float32)
+        assert np.array_equal(S, (amax / np.float32(qmax)).astype(np.float16).view(np.uint16)), dt
+        # every weight within half a step of its reconstruction, codes in range
+        s = S.view(np.float16).astype(np.float64)
+        sc = s[:, np.arange(N) // width]
+        if dt == "q4":
+            Wq = orc.dequant("q4", A, S, M, N)
+        else:
+            Wq = A.astype(np.float64) * sc
+        assert np.all(np.abs(W - Wq) <= sc / 2 * (1 + 2.0 ** -10)), dt
+        codes = np.rint(Wq / np.where(sc == 0, 1, sc))
+        assert np.abs(codes).max() == qmax, dt
+        assert abs(e - ((W.astype(np.float64) - Wq) ** 2).sum()) <= 1e-12 * e, dt
+        # scaling a row by 2^3 scales its scales by 2^3 and keeps the codes
+        W2 = W.copy()
+        W2[2] *= 8.0
+        A2, S2, _ = orc.quantize(dt, W2, M, N)
+        assert np.array_equal(A2, A), dt
+        assert np.array_equal(S2[2].view(np.float16).astype(np.float64),
+                              S[2].view(np.float16).astype(np.float64) * 8.0), dt
+        # binary16 weights give the same result as their exact FP32 values
+        Wh = W.astype(np.float16)
+        Ah, Sh, eh = orc.quantize(dt, Wh.view(np.uint16), M, N)
+        Af, Sf, ef = orc.quantize(dt, Wh.astype(np.float32), M, N)
+        assert np.array_equal(Ah, Af) and np.array_equal(Sh, Sf) and eh == ef, dt
+
+
 PINS = [pin_dec16_all_patterns, pin_rowmajor_worked_example, pin_identity, pin_unit_vectors,
         pin_format_options_unit_vectors, pin_int4_byte_table, pin_all_ones, pin_bruteforce_exact, pin_counts,
-        pin_softmax_closed_forms, pin_softmax_sums_and_brute_force]
+        pin_softmax_closed_forms, pin_softmax_sums_and_brute_force,
+        pin_enc16_against_numpy, pin_quantize_page_rmse, pin_quantize_closed_forms,
+        pin_quantize_invariants]
 
 
 @pytest.fixture(scope="module")
@@ -354,7 +457,9 @@ MUTANTS = {1: "int4 nibble order swapped", 2: "int4 read as offset-8",
            5: "binary16 subnormals decoded as normals", 6: "last column dropped",
            7: "scale row pitch floor(N/128)", 8: "softmax without the maximum subtracted",
            9: "softmax sum missing its last term", 10: "softmax normalised by N",
-           11: "per-row scale taken from row 0", 12: "FP32 x of f16 weights read as binary16"}
+           11: "per-row scale taken from row 0", 12: "FP32 x of f16 weights read as binary16",
+           13: "INT4 scale max/8", 14: "codes truncated, not rounded",
+           15: "quantisation groups of 64 columns", 16: "binary16 encoder truncates"}
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[k] for k in sorted(MUTANTS)])
