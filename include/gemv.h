@@ -202,6 +202,30 @@ gemv_status_t gemv_softmax_run_variant(int variant, const uint16_t *x, uint16_t 
                                        int64_t N, void *stream);
 
 /*
+ * Symmetric weight quantisation: produces the A and scales operands of
+ * gemv_q8 (per_row = 0: one scale per 128 columns, scales [M][ceil(N/128)]),
+ * gemv_q8_rowscale (per_row = 1: scales [M]) and gemv_q4 (one scale per 128
+ * columns, A packed as gemv_q4 reads it; N must be even, else
+ * GEMV_ERR_UNSUPPORTED).
+ * W: [M][N] row-major, FP32 (w_dtype = GEMV_F32) or binary16 (GEMV_F16).
+ * Per group, in FP32: a = max|w|; s = a / qmax (qmax 127 for INT8, 7 for
+ * INT4; IEEE division); the stored scale is binary16(s) rounded to nearest
+ * even (an overflow to infinity stores 65504 instead); each code is
+ * q = clamp(rint(w / scale), -qmax, qmax), with q = 0 where the scale is 0 or w
+ * is NaN.  sq_err: NULL, or a device double to which the call ADDS
+ * sum (w - scale*q)^2 over all weights (the caller zeroes it; the order of the
+ * additions varies, so the last bits may differ between runs).  Codes and
+ * scales are deterministic.  W, A and scales must not overlap.
+ * "membound", section "The kernel decode actually runs: dequant GEMV" (INT8
+ * with a symmetric per-row scale, INT4 with symmetric per-128-column scales,
+ * and the quantisation RMSE of U[-1,1] weights: 2.3e-3 and 4.1e-2).
+ */
+gemv_status_t gemv_quantize_q8(const void *W, int w_dtype, int8_t *A, uint16_t *scales, int64_t M,
+                               int64_t N, int per_row, double *sq_err, void *stream);
+gemv_status_t gemv_quantize_q4(const void *W, int w_dtype, uint8_t *A, uint16_t *scales, int64_t M,
+                               int64_t N, double *sq_err, void *stream);
+
+/*
  * Dequantise to FP32: W[i*N + j] = FP32(s[i, j/128]) * q[i,j], using the
  * same unpacking code as the GEMV kernels.  The product is exact, so W must
  * equal the oracle's dequantised weights bit for bit.  Test helper:

@@ -64,6 +64,8 @@ def _declare(L):
         "gemv_q8_rowscale_ex": [vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_probe_read": [vp, ctypes.c_size_t, vp, i32, vp],
         "gemv_dequant_q8": [vp, vp, vp, i64, i64, vp],
+        "gemv_quantize_q8": [vp, i32, vp, vp, i64, i64, i32, vp, vp],
+        "gemv_quantize_q4": [vp, i32, vp, vp, i64, i64, vp, vp],
         "gemv_dequant_q4": [vp, vp, vp, i64, i64, vp],
         "gemv_variant_info": [i32, i32, ctypes.POINTER(VariantInfo)],
         "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
@@ -349,6 +351,41 @@ def select_variant(dtype: str, A, x) -> int:
     if dtype == "q8row":
         return lib().gemv_q8_rowscale_select_variant(A.data_ptr(), x.data_ptr(), M, N)
     return lib().gemv_select_variant(dt, A.data_ptr(), x.data_ptr(), M, N)
+
+
+def quantize(W, dtype: str, sq_err=None, stream=None):
+    """Symmetric quantisation of W (float32 or float16 [M, N]) on the GPU.
+
+    dtype 'q8' (one scale per 128 columns), 'q8row' (one per row) or 'q4'.
+    Returns (A, scales) in the layouts gemv_q8 / gemv_q8_rowscale / gemv_q4
+    take.  ``sq_err``: optional float64 CUDA tensor of one element to which the
+    sum of squared quantisation errors is added."""
+    torch = _torch()
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D")
+    M, N = W.shape
+    _check(W, "W", (torch.float32, torch.float16), (M, N))
+    w_dt = F32 if W.dtype == torch.float32 else F16
+    e_ptr = None
+    if sq_err is not None:
+        _check(sq_err, "sq_err", (torch.float64,), (1,), W.device)
+        e_ptr = sq_err.data_ptr()
+    if dtype == "q4":
+        A = torch.empty(M, N // 2, dtype=torch.uint8, device=W.device)
+        S = torch.empty(M, (N + GROUP - 1) // GROUP, dtype=torch.float16, device=W.device)
+        st = lib().gemv_quantize_q4(W.data_ptr(), w_dt, A.data_ptr(), S.data_ptr(), M, N, e_ptr,
+                                    _stream_ptr(stream))
+    elif dtype in ("q8", "q8row"):
+        per_row = dtype == "q8row"
+        A = torch.empty(M, N, dtype=torch.int8, device=W.device)
+        S = torch.empty((M,) if per_row else (M, (N + GROUP - 1) // GROUP), dtype=torch.float16,
+                        device=W.device)
+        st = lib().gemv_quantize_q8(W.data_ptr(), w_dt, A.data_ptr(), S.data_ptr(), M, N,
+                                    1 if per_row else 0, e_ptr, _stream_ptr(stream))
+    else:
+        raise ValueError(dtype)
+    _raise(st, f"quantize({dtype})")
+    return A, S
 
 
 def gemv_dequant_q8(A, scales, W=None, stream=None):

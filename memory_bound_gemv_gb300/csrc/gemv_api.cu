@@ -502,6 +502,38 @@ static gemv_status_t dequant(int dtype, const void *A, const uint16_t *scales, f
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
 }
 
+static gemv_status_t quantize(int bits, bool per_row, const void *W, int w_dtype, void *A,
+                              uint16_t *scales, int64_t M, int64_t N, double *sq_err, void *stream)
+{
+    if (M < 0 || N < 0) return GEMV_ERR_INVALID_VALUE;
+    if (w_dtype != DT_F32 && w_dtype != DT_F16) return GEMV_ERR_INVALID_VALUE;
+    if (bits == 4 && (N % 2)) return GEMV_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return GEMV_OK;
+    if (!W || !A || !scales) return GEMV_ERR_INVALID_VALUE;
+    if (!aligned(W, w_dtype == DT_F32 ? 4 : 2) || !aligned(scales, 2) ||
+        (sq_err && !aligned(sq_err, 8)))
+        return GEMV_ERR_MISALIGNED;
+    if (M > INT64_MAX / (4 * N)) return GEMV_ERR_UNSUPPORTED;
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    launch_quantize(bits, per_row, w_dtype == DT_F16, W, A, scales, sq_err, M, N, d->sm_count,
+                    static_cast<cudaStream_t>(stream));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+gemv_status_t gemv_quantize_q8(const void *W, int w_dtype, int8_t *A, uint16_t *scales, int64_t M,
+                               int64_t N, int per_row, double *sq_err, void *stream)
+{
+    return quantize(8, per_row != 0, W, w_dtype, A, scales, M, N, sq_err, stream);
+}
+
+gemv_status_t gemv_quantize_q4(const void *W, int w_dtype, uint8_t *A, uint16_t *scales, int64_t M,
+                               int64_t N, double *sq_err, void *stream)
+{
+    return quantize(4, false, W, w_dtype, A, scales, M, N, sq_err, stream);
+}
+
 gemv_status_t gemv_dequant_q8(const int8_t *A, const uint16_t *scales, float *W, int64_t M,
                               int64_t N, void *stream)
 {

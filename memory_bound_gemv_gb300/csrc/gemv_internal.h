@@ -130,6 +130,11 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
 // N == 0: y = 0.
 void launch_fill_zero(float *y, int64_t M, cudaStream_t s);
 
+// Symmetric quantisation (gemv_quantize.cu): bits 8 or 4; one scale per row
+// or per 128 columns; FP32 or binary16 weights.
+void launch_quantize(int bits, bool per_row, bool f16in, const void *W, void *A, uint16_t *scales,
+                     double *sq_err, int64_t M, int64_t N, int sm_count, cudaStream_t s);
+
 // Row softmax (gemv_softmax.cu).  variant < 0 chooses; cudaErrorNotSupported
 // when the variant cannot serve the shape or alignment.
 cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,

@@ -151,3 +151,21 @@ def test_softmax_and_copy_validation():
     assert L.gemv_probe_copy(FAKE, FAKE, 4096, -1, None) == mbg.ERR_INVALID_VALUE
     assert L.gemv_probe_copy(FAKE, FAKE + 8, 4096, 0, None) == mbg.ERR_MISALIGNED
     assert len(mbg.softmax_variants()) >= 2 and len(mbg.copy_probe_variants()) >= 1
+
+
+def test_quantize_validation():
+    L = mbg.lib()
+    E = FAKE
+    # (W, w_dtype, A, scales, M, N, [per_row], sq_err, stream)
+    q8 = lambda *a: L.gemv_quantize_q8(*a)
+    assert q8(E, mbg.F32, E, E, -1, 4, 0, None, None) == mbg.ERR_INVALID_VALUE
+    assert q8(E, mbg.Q8, E, E, 4, 4, 0, None, None) == mbg.ERR_INVALID_VALUE  # weights must be F32/F16
+    assert q8(None, mbg.F32, None, None, 0, 4, 0, None, None) == mbg.OK
+    assert q8(None, mbg.F32, E, E, 4, 4, 0, None, None) == mbg.ERR_INVALID_VALUE
+    assert q8(E, mbg.F32, E, None, 4, 4, 0, None, None) == mbg.ERR_INVALID_VALUE
+    assert q8(E + 2, mbg.F32, E, E, 4, 4, 0, None, None) == mbg.ERR_MISALIGNED
+    assert q8(E + 1, mbg.F16, E, E, 4, 4, 0, None, None) == mbg.ERR_MISALIGNED
+    assert q8(E, mbg.F32, E, E + 1, 4, 4, 1, None, None) == mbg.ERR_MISALIGNED
+    assert q8(E, mbg.F32, E, E, 4, 4, 0, E + 4, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_quantize_q4(E, mbg.F32, E, E, 4, 7, None, None) == mbg.ERR_UNSUPPORTED
+    assert L.gemv_quantize_q4(E, mbg.F32, E, E, -4, 8, None, None) == mbg.ERR_INVALID_VALUE
