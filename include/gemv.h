@@ -157,6 +157,32 @@ gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t
                       const uint16_t *scales, unsigned flags, void *stream);
 
 /*
+ * gemv_ex with x and y in HOST memory: one call per decode step that takes
+ * the input vector from, and returns the output to, page-locked host buffers.
+ * x_host: page-locked host memory (cudaHostAlloc / cudaHostRegister / a
+ * pinned torch tensor), N elements of x's type; else GEMV_ERR_INVALID_VALUE.
+ * x_dev: device buffer of the same size that receives x (the caller owns it;
+ * 16-byte aligned for the vectorised kernels).  y_host: page-locked host
+ * memory (device memory is accepted too) of M floats, written by the GEMV
+ * kernel directly; read it after synchronising `stream`.  A, scales and dtype
+ * as for gemv_ex.
+ * The copy of x is a small kernel that reads the host buffer over the
+ * CPU-GPU link, and the GEMV is launched with programmatic dependent launch
+ * after it, so the GEMV streams its weights while x is still being fetched.
+ * GEMV_FLAG_OVERLAP_PRECEDING: additionally, the kernel that precedes the
+ * call on `stream` writes neither A, scales nor x_host (a previous call of
+ * this function qualifies); the copy then reads x_host before that kernel has
+ * finished and writes x_dev only after it.  x_host must not change until the
+ * call has run on the stream.
+ * Same results as gemv_ex on device copies of x (bit for bit).
+ * The pages time device-resident operands only; this call has no
+ * counterpart there.
+ */
+gemv_status_t gemv_ex_host(int dtype, const void *A, const void *x_host, void *x_dev, float *y_host,
+                           int64_t M, int64_t N, const uint16_t *scales, unsigned flags,
+                           void *stream);
+
+/*
  * Pure-read bandwidth probe: streams buf[0..bytes) once with the same
  * 16-byte read-only loads the GEMV kernels use and folds every word into
  * *sink with XOR (so no load is dead code).  bytes must be a multiple of 16

@@ -71,6 +71,7 @@ def _declare(L):
         "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
         "gemv_get_device_error": [vp],
         "gemv_ex": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
+        "gemv_ex_host": [i32, vp, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_softmax_f16": [vp, vp, i64, i64, vp],
         "gemv_softmax_run_variant": [i32, vp, vp, i64, i64, vp],
         "gemv_probe_copy": [vp, vp, ctypes.c_size_t, i32, vp],
@@ -116,6 +117,8 @@ def library_path() -> str:
 def lib(build_if_stale: bool = True):
     """The ctypes handle of libmbgemv.so (built in-tree on first use if stale)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             from . import build as _b
@@ -140,7 +143,12 @@ def _torch():
 def _stream_ptr(stream) -> Optional[int]:
     torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
+        # the current stream's handle without building a Stream object (this
+        # runs once per call, on the host's critical path in a decode loop)
+        try:
+            return torch._C._cuda_getCurrentRawStream(torch._C._cuda_getDevice())
+        except AttributeError:  # pragma: no cover - other torch builds
+            stream = torch.cuda.current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -283,6 +291,43 @@ def gemv_ex(dtype: str, A, x, scales=None, y=None, stream=None, flags: int = 0):
     _raise(lib().gemv_ex(dt, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, s_ptr, flags,
                          _stream_ptr(stream)), "gemv_ex")
     return y
+
+
+def gemv_host(dtype: str, A, x_host, x_dev, scales=None, y_host=None, stream=None,
+              overlap: bool = False):
+    """GEMV with x and y in page-locked host memory (``gemv_ex_host``).
+
+    x_host: pinned CPU tensor [N]; x_dev: CUDA tensor like it that receives
+    x; y_host: pinned CPU float32 [M] (allocated pinned when None), written
+    by the kernel -- synchronise the stream before reading it.  ``overlap``:
+    the kernel before this call on the stream writes neither A, scales nor
+    x_host (a previous gemv_host call qualifies)."""
+    torch = _torch()
+    dt = DTYPES[dtype]
+    M, N = _mn(A, dt)
+    a_types = {F32: (torch.float32,), F16: _f16_types(), Q8: (torch.int8,), Q4: (torch.uint8,),
+               F16X32: _f16_types()}[dt]
+    x_types = (torch.float32,) if dt in (F32, F16X32) else _f16_types()
+    _check(A, "A", a_types, tuple(A.shape))
+    _check(x_dev, "x_dev", x_types, (N,), A.device)
+    # page-locking is checked by the library (GEMV_ERR_INVALID_VALUE otherwise)
+    if not isinstance(x_host, torch.Tensor) or x_host.device.type != "cpu":
+        raise ValueError("x_host must be a pinned CPU tensor")
+    if x_host.dtype not in x_types or tuple(x_host.shape) != (N,) or not x_host.is_contiguous():
+        raise ValueError(f"x_host must be a contiguous [{N}] tensor of {x_types}")
+    if y_host is None:
+        y_host = torch.empty(M, dtype=torch.float32).pin_memory()
+    elif (not isinstance(y_host, torch.Tensor) or y_host.device.type != "cpu"
+          or y_host.dtype != torch.float32 or tuple(y_host.shape) != (M,) or not y_host.is_contiguous()):
+        raise ValueError(f"y_host must be a pinned contiguous float32 [{M}] CPU tensor")
+    s_ptr = None
+    if dt in (Q8, Q4):
+        _check(scales, "scales", _f16_types(), (M, (N + GROUP - 1) // GROUP), A.device)
+        s_ptr = scales.data_ptr()
+    flags = FLAG_OVERLAP_PRECEDING if overlap else 0
+    _raise(lib().gemv_ex_host(dt, A.data_ptr(), x_host.data_ptr(), x_dev.data_ptr(), y_host.data_ptr(),
+                              M, N, s_ptr, flags, _stream_ptr(stream)), "gemv_ex_host")
+    return y_host
 
 
 def gemv(dtype: str, A, x, scales=None, y=None, stream=None, overlap: bool = False):

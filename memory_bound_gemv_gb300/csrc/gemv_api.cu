@@ -387,6 +387,45 @@ gemv_status_t gemv_q8_rowscale_ex(const int8_t *A, const uint16_t *x, float *y, 
     return run(DT_Q8, -1, A, x, y, M, N, row_scales, stream, flags, SCALES_PER_ROW);
 }
 
+// Address through which kernels reach p: page-locked host memory (and, when
+// allow_device, device or managed memory); nullptr for anything else.
+static void *device_view(const void *p, bool allow_device)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    if (allow_device && (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged))
+        return const_cast<void *>(p);
+    return nullptr;
+}
+
+gemv_status_t gemv_ex_host(int dtype, const void *A, const void *x_host, void *x_dev, float *y_host,
+                           int64_t M, int64_t N, const uint16_t *scales, unsigned flags,
+                           void *stream)
+{
+    if (flags & ~static_cast<unsigned>(GEMV_FLAG_OVERLAP_PRECEDING)) return GEMV_ERR_INVALID_VALUE;
+    gemv_status_t st = validate(dtype, A, x_dev, y_host, M, N, scales);
+    if (st != GEMV_OK || M == 0) return st;
+    float *y = static_cast<float *>(device_view(y_host, true));
+    if (!y) return GEMV_ERR_INVALID_VALUE;
+    if (N == 0) return run(dtype, -1, A, x_dev, y, M, N, scales, stream);
+    if (!x_host) return GEMV_ERR_INVALID_VALUE;
+    if (!aligned(x_host, x_align(dtype))) return GEMV_ERR_MISALIGNED;
+    const void *xh = device_view(x_host, false);
+    if (!xh) return GEMV_ERR_INVALID_VALUE;
+    if (!current_device()) return GEMV_ERR_CUDA;
+    launch_copy_in(xh, x_dev, N * x_elem_bytes(dtype), (flags & GEMV_FLAG_OVERLAP_PRECEDING) != 0,
+                   static_cast<cudaStream_t>(stream));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_LAUNCH);
+    // the GEMV never writes what the copy reads, and reads x only after the
+    // copy has completed (griddepcontrol.wait): it may always overlap it
+    return run(dtype, -1, A, x_dev, y, M, N, scales, stream, GEMV_FLAG_OVERLAP_PRECEDING);
+}
+
 gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t M, int64_t N,
                       const uint16_t *scales, unsigned flags, void *stream)
 {
