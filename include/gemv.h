@@ -183,6 +183,32 @@ gemv_status_t gemv_ex_host(int dtype, const void *A, const void *x_host, void *x
                            void *stream);
 
 /*
+ * gemv_ex_host for callers that cannot allocate device memory: the same
+ * computation and results, with the device copy of x kept in a fixed array
+ * inside the library instead of a caller-provided x_dev.  Meant for code
+ * that may not allocate once it is running (real-time or certified loops
+ * that allocate only at start-up), plug-ins whose host program owns the
+ * device allocator, and callers that have only this C ABI.  The other
+ * arguments are those of gemv_ex_host.
+ * Limit: x may take at most GEMV_NOALLOC_X_MAX_BYTES bytes (N <= 131072
+ * binary16 values or 65536 FP32 values); a longer x returns
+ * GEMV_ERR_UNSUPPORTED before anything is launched.  Every GPU that loads the
+ * library holds this array (256 KiB) until the process exits; nothing is
+ * allocated by the call.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the one array and leave the last x in it; it
+ * is fully rewritten before each use, so nothing needs clearing.  Calls that
+ * can run at the same time on the GPU (different streams, or other threads
+ * without ordering) race on it: issue them on one stream.
+ * The pages have no counterpart to this entry point.
+ */
+#define GEMV_NOALLOC_X_MAX_BYTES 262144
+gemv_status_t gemv_ex_host_noalloc(int dtype, const void *A, const void *x_host, float *y_host,
+                                   int64_t M, int64_t N, const uint16_t *scales, unsigned flags,
+                                   void *stream);
+
+/*
  * Pure-read bandwidth probe: streams buf[0..bytes) once with the same
  * 16-byte read-only loads the GEMV kernels use and folds every word into
  * *sink with XOR (so no load is dead code).  bytes must be a multiple of 16

@@ -72,6 +72,7 @@ def _declare(L):
         "gemv_get_device_error": [vp],
         "gemv_ex": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_ex_host": [i32, vp, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
+        "gemv_ex_host_noalloc": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_softmax_f16": [vp, vp, i64, i64, vp],
         "gemv_softmax_run_variant": [i32, vp, vp, i64, i64, vp],
         "gemv_probe_copy": [vp, vp, ctypes.c_size_t, i32, vp],
