@@ -713,7 +713,8 @@ def run_softmax(args):
                        "launch": f"CUDA graph of {batch} back-to-back launches"},
             "mbu": {"copy_probe_gbs": ceiling, "mbu_copy_pct": 100.0 * value / ceiling, "probes": best},
             "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
-                         "frac": value / peak, "peak_kind": peak_kind, "traffic": None},
+                         "frac": value / peak, "peak_kind": peak_kind,
+                         "traffic": recorded_traffic(w.name, "auto")},
             "parity_rows_max_rel_err": err, "gpu_launches": steps}
     print(json.dumps(line), flush=True)
     if args.json_out:
@@ -752,6 +753,22 @@ def run_profile(args):
     return 0
 
 
+def run_profile_softmax(args):
+    """One launch of the row softmax (for an ncu capture)."""
+    import numpy as np
+    import torch
+
+    import memory_bound_gemv_gb300 as mbg
+
+    torch.cuda.set_device(0)
+    w = synth.SOFTMAX_WORKLOADS[args.workload]
+    x = torch.from_numpy(synth.weight_rows(w, 0, w.M).view(np.float16)).cuda()
+    y = mbg.gemv_softmax_f16(x)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": w.name, "y00": float(y[0, 0].item())}))
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -783,6 +800,8 @@ def main(argv=None):
     if args.op == "softmax":
         if args.workload not in synth.SOFTMAX_WORKLOADS:
             p.error("--op softmax needs a softmax_* workload")
+        if args.profile:
+            return run_profile_softmax(args)
         return run_softmax(args)
     if args.workload not in synth.WORKLOADS:
         p.error("GEMV workloads: " + ", ".join(sorted(synth.WORKLOADS)))
