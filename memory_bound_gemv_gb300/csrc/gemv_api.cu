@@ -594,8 +594,11 @@ static gemv_status_t softmax_run(const uint16_t *x, uint16_t *y, int64_t M, int6
     if (!x || !y) return GEMV_ERR_INVALID_VALUE;
     if (!aligned(x, 2) || !aligned(y, 2)) return GEMV_ERR_MISALIGNED;
     if (M > INT64_MAX / N) return GEMV_ERR_UNSUPPORTED;
-    if (!current_device()) return GEMV_ERR_CUDA;
-    const cudaError_t e = launch_softmax(x, y, M, N, variant, static_cast<cudaStream_t>(stream));
+    DeviceState *d = current_device();
+    if (!d) return GEMV_ERR_CUDA;
+    const cudaError_t e = launch_softmax(x, y, M, N, variant, d->status,
+                                         g_wait_limit_ns.load(std::memory_order_relaxed),
+                                         static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return GEMV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
 }

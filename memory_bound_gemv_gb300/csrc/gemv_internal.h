@@ -142,7 +142,7 @@ void launch_quantize(int bits, bool per_row, bool f16in, const void *W, void *A,
 // Row softmax (gemv_softmax.cu).  variant < 0 chooses; cudaErrorNotSupported
 // when the variant cannot serve the shape or alignment.
 cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
-                           cudaStream_t s);
+                           unsigned int *err, uint64_t wait_limit_ns, cudaStream_t s);
 int softmax_variant_count();
 const char *softmax_variant_name(int v);
 

@@ -12,6 +12,14 @@
 // read and one write per element (the page's version re-reads the row through
 // L2 for a second pass; with the row in registers there is no second read).
 //
+// softmax_bulk_kernel: the same single read and write, with the row segments
+// staged by bulk async copies into a ring of shared-memory buffers instead of
+// register prefetch, so a persistent grid of blocks (or clusters) keeps the
+// next rows in flight without spending registers on them.  Each thread keeps
+// exp(x - m_t) for its own maximum; the (max, sum) pairs meet in one
+// exchange per row (one barrier of the block or cluster), which also frees
+// the row's buffer for the next copy.
+//
 // softmax_elem_kernel: any layout or length.  One block per row, the page's
 // two passes: the online update over the row, then exp(x - m) / d re-reading
 // the row.
@@ -187,6 +195,244 @@ __global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint1
     }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy staged rows
+// ---------------------------------------------------------------------------
+
+// Max or sum of one value per thread over the block (C == 1) or the cluster:
+// warp butterfly, then lane 0 of each warp writes its value into slot
+// [rank * NW + warp] of every block of the cluster, one barrier, and every
+// warp reduces the C * NW slots in the same order (all blocks get the same
+// bits).
+template <int T, int C, bool MAX>
+__device__ __forceinline__ float row_reduce(float v, float *slots, int rank)
+{
+    constexpr int NW = T / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = MAX ? fmaxf(v, o) : v + o;
+    }
+    if (lane == 0) {
+        if constexpr (C == 1) {
+            slots[warp] = v;
+        } else {
+            cg::cluster_group cluster = cg::this_cluster();
+#pragma unroll
+            for (int r = 0; r < C; ++r) *cluster.map_shared_rank(&slots[rank * NW + warp], r) = v;
+        }
+    }
+    if constexpr (C == 1) __syncthreads();
+    else cg::this_cluster().sync();
+    float w = MAX ? -INFINITY : 0.f;
+    for (int i = lane; i < C * NW; i += 32) w = MAX ? fmaxf(w, slots[i]) : w + slots[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, w, off);
+        w = MAX ? fmaxf(w, o) : w + o;
+    }
+    return w;
+}
+
+// (max, sum) of the row from one pair per thread: inside a warp the maximum
+// first, then the sums rescaled to it; lane 0 of each warp writes the warp's
+// pair into slot [rank * NW + warp] of every block of the cluster; one barrier
+// (of the block, or of the cluster); then every warp combines the C * NW pairs
+// in the same order, so all blocks of a cluster get the same bits.  A side
+// with no elements has m = -inf and d = 0.
+template <int T, int C>
+__device__ __forceinline__ MaxSum row_exchange(MaxSum v, float2 *slots, int rank)
+{
+    constexpr int NW = T / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float m = v.m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float d = (v.m == -INFINITY) ? 0.f : v.d * __expf(v.m - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) {
+        const float2 pr = make_float2(m, d);
+        if constexpr (C == 1) {
+            slots[warp] = pr;
+        } else {
+            cg::cluster_group cluster = cg::this_cluster();
+#pragma unroll
+            for (int r = 0; r < C; ++r) *cluster.map_shared_rank(&slots[rank * NW + warp], r) = pr;
+        }
+    }
+    if constexpr (C == 1) __syncthreads();
+    else cg::this_cluster().sync();
+    constexpr int PER = (C * NW + 31) / 32;
+    float2 e[PER];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int idx = lane + 32 * k;
+        e[k] = idx < C * NW ? slots[idx] : make_float2(-INFINITY, 0.f);
+        M = fmaxf(M, e[k].x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float D = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+        if (e[k].x != -INFINITY) D += e[k].y * __expf(e[k].x - M);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) D += __shfl_xor_sync(0xffffffffu, D, off);
+    return {M, D};
+}
+
+__host__ __device__ constexpr int softmax_bulk_smem(int T, int EPT, int C, int NB)
+{
+    // NB row-segment buffers, NB mbarriers + the abort flag, slots [2 rows][C * T/32] of
+    // (max, sum) pairs (or of a max and a sum)
+    return NB * T * EPT * 2 + NB * 8 + 16 + 2 * C * (T / 32) * 8;
+}
+
+// C blocks (a cluster) per row, T threads per block, EPT elements per thread,
+// NB staged rows per block.  PAIR: one exchange of (max, sum) pairs per row;
+// else the row maximum first, then the sum of exp(x - max) (two barriers, but
+// fewer live registers across them).  Requires N % 8 == 0, 16-byte aligned x and y and
+// N <= C * T * EPT.  Cluster k handles rows k, k + nclusters, ...; its blocks
+// walk the same rows and meet the same barriers.  A wait that gives up sets
+// the status word and the block's abort flag; the block then runs on without
+// writing y, so that the barriers of the cluster still match.
+template <int T, int EPT, int C, int NB, bool PAIR>
+__global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N,
+                                                         unsigned int *err, uint64_t wait_limit_ns)
+{
+    constexpr int VPT = EPT / 8;
+    constexpr int NW = T / 32;
+    constexpr int SEGE = T * EPT;  // elements of a block's segment
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *bufs = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NB * SEGE * 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + NB);
+    float2 *slots = reinterpret_cast<float2 *>(smem + NB * SEGE * 2 + NB * 8 + 16);
+
+    const int tid = threadIdx.x;
+    const int rank = C > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+    const int64_t cid = blockIdx.x / C;
+    const int64_t ncl = gridDim.x / C;
+    const int seg0 = rank * SEGE;
+    const int segn = N - seg0 < 0 ? 0 : (N - seg0 < SEGE ? N - seg0 : SEGE);
+    const uint32_t seg_bytes = static_cast<uint32_t>(segn) * 2u;
+
+    if (tid == 0) {
+        for (int b = 0; b < NB; ++b) mbar_init(smem_addr(&full[b]), 1);
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    if constexpr (C > 1) cg::this_cluster().sync();  // every block of the cluster has started
+
+    // thread 0 issues the copies and remembers, per buffer, the phase of a
+    // copy not yet waited for (only needed when the block gives up)
+    uint32_t issued[NB], pending[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) issued[b] = pending[b] = 0;
+    auto issue = [&](int64_t row, int b) {
+        const uint32_t bar = smem_addr(&full[b]);
+        mbar_arrive_expect_tx(bar, seg_bytes);
+        bulk_copy_g2s(smem_addr(bufs + b * SEGE * 2), x + row * N + seg0, seg_bytes, bar);
+        ++issued[b];
+        pending[b] = 1;
+    };
+    if (tid == 0 && seg_bytes) {
+        for (int b = 0; b < NB; ++b) {
+            const int64_t row = cid + b * ncl;
+            if (row < M) issue(row, b);
+        }
+    }
+
+    int64_t i = 0;
+    for (int64_t row = cid; row < M; row += ncl, ++i) {
+        const int b = static_cast<int>(i % NB);
+        if (seg_bytes && !*abort_flag) {
+            if (mbar_wait_bounded(smem_addr(&full[b]), static_cast<uint32_t>((i / NB) & 1), wait_limit_ns)) {
+                if (tid == 0) pending[b] = 0;
+            } else {
+                report_error(err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        // this block's segment into registers; -inf beyond the row end
+        uint4 raw[VPT];
+        const uint32_t bb = smem_addr(bufs + b * SEGE * 2);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int e0 = seg0 + 8 * (k * T + tid);
+            raw[k] = e0 < N ? lds128(bb + (k * T + tid) * 16) : make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
+        }
+        if constexpr (!PAIR) {
+            // every thread has read buffer b: refill it with a later row
+            __syncthreads();
+            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b);
+        }
+        // this thread's maximum (on binary16 pairs, then one conversion)
+        __half2 hm = __halves2half2(__ushort_as_half(0xFC00u), __ushort_as_half(0xFC00u));
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            hm = __hmax2(hm, *reinterpret_cast<const __half2 *>(&raw[k].x));
+            hm = __hmax2(hm, *reinterpret_cast<const __half2 *>(&raw[k].y));
+            hm = __hmax2(hm, *reinterpret_cast<const __half2 *>(&raw[k].z));
+            hm = __hmax2(hm, *reinterpret_cast<const __half2 *>(&raw[k].w));
+        }
+        const float mt = fmaxf(__low2float(hm), __high2float(hm));
+        float *sl = reinterpret_cast<float *>(slots + static_cast<int>(i & 1) * (C * NW));
+        float m = mt;  // the maximum the exponentials are taken against
+        if constexpr (!PAIR) m = row_reduce<T, C, true>(mt, sl, rank);
+
+        // exp(x - m) kept for the output, and its sum
+        float e[EPT];
+        float d = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            half2_bits_to_float(raw[k].x, e[8 * k + 0], e[8 * k + 1]);
+            half2_bits_to_float(raw[k].y, e[8 * k + 2], e[8 * k + 3]);
+            half2_bits_to_float(raw[k].z, e[8 * k + 4], e[8 * k + 5]);
+            half2_bits_to_float(raw[k].w, e[8 * k + 6], e[8 * k + 7]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                e[8 * k + j] = PAIR && m == -INFINITY ? 0.f : __expf(e[8 * k + j] - m);
+                d += e[8 * k + j];
+            }
+        }
+        float inv;
+        if constexpr (PAIR) {
+            // one exchange per row; after it every thread has read buffer b
+            const MaxSum tot = row_exchange<T, C>(MaxSum{mt, d}, slots + static_cast<int>(i & 1) * (C * NW), rank);
+            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b);
+            inv = (mt == -INFINITY) ? 0.f : __expf(mt - tot.m) / tot.d;
+        } else {
+            inv = 1.f / row_reduce<T, C, false>(d, sl + C * NW, rank);
+        }
+        const bool aborted = *abort_flag != 0;
+        if (!aborted) {
+            uint16_t *yr = y + row * N;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int e0 = seg0 + 8 * (k * T + tid);
+                if (e0 < N) {
+                    uint4 o;
+                    o.x = pack_half2(e[8 * k + 0] * inv, e[8 * k + 1] * inv);
+                    o.y = pack_half2(e[8 * k + 2] * inv, e[8 * k + 3] * inv);
+                    o.z = pack_half2(e[8 * k + 4] * inv, e[8 * k + 5] * inv);
+                    o.w = pack_half2(e[8 * k + 6] * inv, e[8 * k + 7] * inv);
+                    st_stream16(yr + e0, o);
+                }
+            }
+        }
+    }
+    if (tid == 0 && *abort_flag) {
+        // copies issued for rows this block did not take may still land
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            if (pending[b]) mbar_wait_bounded(smem_addr(&full[b]), (issued[b] - 1) & 1u, wait_limit_ns);
+    }
+}
+
 // Any layout, any length: one block per row, two passes over the row.
 template <int T>
 __global__ void __launch_bounds__(T) softmax_elem_kernel(const uint16_t *x, uint16_t *y, int64_t N)
@@ -301,26 +547,104 @@ cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N,
     }
 }
 
+// Persistent grid of the bulk-staged kernel: resident clusters (of C
+// blocks), at most one per row.
+template <int T, int EPT, int C, int NB, bool PAIR>
+cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N, unsigned int *err,
+                                uint64_t wait_limit_ns, cudaStream_t s)
+{
+    constexpr int SMEM = softmax_bulk_smem(T, EPT, C, NB);
+    static const int resident = [] {
+        // raise the dynamic shared memory limit once, then ask for the occupancy
+        if (cudaFuncSetAttribute(softmax_bulk_kernel<T, EPT, C, NB, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+            return 0;
+        int dev = 0, sms = 0, n = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if constexpr (C == 1) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, softmax_bulk_kernel<T, EPT, 1, NB, PAIR>, T,
+                                                              SMEM) != cudaSuccess)
+                return 0;
+            return n * sms;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(C * sms);
+            cfg.blockDim = dim3(T);
+            cfg.dynamicSmemBytes = SMEM;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, softmax_bulk_kernel<T, EPT, C, NB, PAIR>, &cfg) != cudaSuccess)
+                return 0;
+            return n;
+        }
+    }();
+    if (resident <= 0) return cudaErrorNotSupported;
+    const int64_t clusters = M < resident ? M : resident;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * C));
+    cfg.blockDim = dim3(T);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = C > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, softmax_bulk_kernel<T, EPT, C, NB, PAIR>, x, y, M, N, err, wait_limit_ns);
+}
+
+template <int T, int EPT, int C>
+cudaError_t launch_softmax_vec_v(const uint16_t *x, uint16_t *y, int64_t M, int N, unsigned int *,
+                                 uint64_t, cudaStream_t s)
+{
+    return launch_softmax_vec<T, EPT, C>(x, y, M, N, s);
+}
+
 struct SoftmaxVariant {
     int threads, ept, cluster;
     const char *name;
-    cudaError_t (*launch)(const uint16_t *, uint16_t *, int64_t, int, cudaStream_t);
+    cudaError_t (*launch)(const uint16_t *, uint16_t *, int64_t, int, unsigned int *, uint64_t,
+                          cudaStream_t);
     int capacity() const { return threads * ept * cluster; }
 };
 
-// The automatic choice is the first entry whose capacity covers the row;
-// the T = 256 cluster entries after it are alternatives for comparison.
+// The automatic choice is the first entry whose capacity covers the row.
 static const SoftmaxVariant kSoftmax[] = {
-    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec<128, 8, 1>},
-    {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec<256, 16, 1>},
-    {256, 32, 1, "sm_t256_e32_c1", &launch_softmax_vec<256, 32, 1>},
-    {512, 32, 1, "sm_t512_e32_c1", &launch_softmax_vec<512, 32, 1>},
-    {512, 32, 2, "sm_t512_e32_c2", &launch_softmax_vec<512, 32, 2>},
-    {512, 32, 4, "sm_t512_e32_c4", &launch_softmax_vec<512, 32, 4>},
-    {512, 32, 8, "sm_t512_e32_c8", &launch_softmax_vec<512, 32, 8>},
-    {256, 32, 2, "sm_t256_e32_c2", &launch_softmax_vec<256, 32, 2>},
-    {256, 32, 4, "sm_t256_e32_c4", &launch_softmax_vec<256, 32, 4>},
-    {256, 32, 8, "sm_t256_e32_c8", &launch_softmax_vec<256, 32, 8>},
+    // the automatic choice, by capacity (measured fastest for each width):
+    // bulk-staged rows smb_t<threads>_e<elements per thread>_c<cluster>_b<staged rows>,
+    // _p: one (max, sum) exchange per row instead of a max then a sum
+    {128, 8, 1, "smb_t128_e8_c1_b3", &launch_softmax_bulk<128, 8, 1, 3, false>},
+    {256, 16, 1, "smb_t256_e16_c1_b3", &launch_softmax_bulk<256, 16, 1, 3, false>},
+    {256, 32, 1, "smb_t256_e32_c1_b3", &launch_softmax_bulk<256, 32, 1, 3, false>},
+    {512, 32, 1, "smb_t512_e32_c1_b2", &launch_softmax_bulk<512, 32, 1, 2, false>},
+    {256, 32, 4, "smb_t256_e32_c4_b2_p", &launch_softmax_bulk<256, 32, 4, 2, true>},
+    {512, 32, 4, "smb_t512_e32_c4_b2_p", &launch_softmax_bulk<512, 32, 4, 2, true>},
+    {512, 32, 8, "smb_t512_e32_c8_b2", &launch_softmax_bulk<512, 32, 8, 2, false>},
+    // alternatives
+    {256, 32, 1, "smb_t256_e32_c1_b2", &launch_softmax_bulk<256, 32, 1, 2, false>},
+    {256, 32, 1, "smb_t256_e32_c1_b2_p", &launch_softmax_bulk<256, 32, 1, 2, true>},
+    {512, 32, 2, "smb_t512_e32_c2_b2", &launch_softmax_bulk<512, 32, 2, 2, false>},
+    {512, 32, 2, "smb_t512_e32_c2_b2_p", &launch_softmax_bulk<512, 32, 2, 2, true>},
+    {256, 32, 4, "smb_t256_e32_c4_b2", &launch_softmax_bulk<256, 32, 4, 2, false>},
+    {512, 32, 8, "smb_t512_e32_c8_b2_p", &launch_softmax_bulk<512, 32, 8, 2, true>},
+    {512, 32, 8, "smb_t512_e32_c8_b3_p", &launch_softmax_bulk<512, 32, 8, 3, true>},
+    // rows held in registers, register prefetch of the next row (single-block rows)
+    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec_v<128, 8, 1>},
+    {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec_v<256, 16, 1>},
+    {256, 32, 1, "sm_t256_e32_c1", &launch_softmax_vec_v<256, 32, 1>},
+    {512, 32, 1, "sm_t512_e32_c1", &launch_softmax_vec_v<512, 32, 1>},
+    {512, 32, 2, "sm_t512_e32_c2", &launch_softmax_vec_v<512, 32, 2>},
+    {512, 32, 4, "sm_t512_e32_c4", &launch_softmax_vec_v<512, 32, 4>},
+    {512, 32, 8, "sm_t512_e32_c8", &launch_softmax_vec_v<512, 32, 8>},
+    {256, 32, 4, "sm_t256_e32_c4", &launch_softmax_vec_v<256, 32, 4>},
 };
 constexpr int kSoftmaxVariants = static_cast<int>(sizeof(kSoftmax) / sizeof(kSoftmax[0]));
 
@@ -335,7 +659,7 @@ const char *softmax_variant_name(int v)
 // Chooses (variant < 0) or runs a given variant; returns a CUDA error, or
 // cudaErrorNotSupported when the variant cannot serve the shape.
 cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
-                           cudaStream_t s)
+                           unsigned int *err, uint64_t wait_limit_ns, cudaStream_t s)
 {
     const bool vec_ok = N % 8 == 0 && N <= (1 << 30) &&
                         (reinterpret_cast<uintptr_t>(x) % 16) == 0 &&
@@ -354,7 +678,7 @@ cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N,
     if (variant < kSoftmaxVariants) {
         const SoftmaxVariant &v = kSoftmax[variant];
         if (!vec_ok || N > v.capacity()) return cudaErrorNotSupported;
-        return v.launch(x, y, M, static_cast<int>(N), s);
+        return v.launch(x, y, M, static_cast<int>(N), err, wait_limit_ns, s);
     }
     if (M > 0x7fffffffLL) return cudaErrorNotSupported;
     softmax_elem_kernel<256><<<static_cast<unsigned>(M), 256, 0, s>>>(x, y, N);
