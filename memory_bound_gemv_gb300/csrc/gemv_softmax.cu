@@ -32,6 +32,17 @@ namespace cg = cooperative_groups;
 
 namespace mbg {
 
+// e^t computed as 2^(t log2 e) by the ex2.approx instruction (PTX ISA: at
+// most 2^-22 relative error; results below the FP32 normal range flush to
+// zero, far below anything a binary16 output can hold).  t = x - m is formed
+// first, so the scaling never multiplies a large |m| on its own.
+__device__ __forceinline__ float exp_approx(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t * 1.4426950408889634f));
+    return r;
+}
+
 // (m, d) pairs: running maximum and sum of exp(x - m).  An empty side has
 // m = -inf and d = 0.
 struct MaxSum {
@@ -43,7 +54,7 @@ __device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b)
     if (a.m == -INFINITY) return b;
     if (b.m == -INFINITY) return a;
     const float m = fmaxf(a.m, b.m);
-    return {m, a.d * __expf(a.m - m) + b.d * __expf(b.m - m)};
+    return {m, a.d * exp_approx(a.m - m) + b.d * exp_approx(b.m - m)};
 }
 
 __device__ __forceinline__ MaxSum warp_combine(MaxSum v)
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint1
             const int e0 = seg + 8 * (k * T + tid);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                v[8 * k + e] = e0 < N ? __expf(v[8 * k + e] - m) : 0.f;
+                v[8 * k + e] = e0 < N ? exp_approx(v[8 * k + e] - m) : 0.f;
                 d += v[8 * k + e];
             }
         }
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint1
             tot = all;
         }
 
-        const float scale = (mine.m == -INFINITY) ? 0.f : __expf(mine.m - tot.m) / tot.d;
+        const float scale = (mine.m == -INFINITY) ? 0.f : exp_approx(mine.m - tot.m) / tot.d;
         uint16_t *yr = y + row * N;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -249,7 +260,7 @@ __device__ __forceinline__ MaxSum row_exchange(MaxSum v, float2 *slots, int rank
     float m = v.m;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float d = (v.m == -INFINITY) ? 0.f : v.d * __expf(v.m - m);
+    float d = (v.m == -INFINITY) ? 0.f : v.d * exp_approx(v.m - m);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     if (lane == 0) {
@@ -278,7 +289,7 @@ __device__ __forceinline__ MaxSum row_exchange(MaxSum v, float2 *slots, int rank
     float D = 0.f;
 #pragma unroll
     for (int k = 0; k < PER; ++k)
-        if (e[k].x != -INFINITY) D += e[k].y * __expf(e[k].x - M);
+        if (e[k].x != -INFINITY) D += e[k].y * exp_approx(e[k].x - M);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) D += __shfl_xor_sync(0xffffffffu, D, off);
     return {M, D};
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
             half2_bits_to_float(raw[k].w, e[8 * k + 6], e[8 * k + 7]);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                e[8 * k + j] = PAIR && m == -INFINITY ? 0.f : __expf(e[8 * k + j] - m);
+                e[8 * k + j] = PAIR && m == -INFINITY ? 0.f : exp_approx(e[8 * k + j] - m);
                 d += e[8 * k + j];
             }
         }
@@ -404,7 +415,7 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
             // one exchange per row; after it every thread has read buffer b
             const MaxSum tot = row_exchange<T, C>(MaxSum{mt, d}, slots + static_cast<int>(i & 1) * (C * NW), rank);
             if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b);
-            inv = (mt == -INFINITY) ? 0.f : __expf(mt - tot.m) / tot.d;
+            inv = (mt == -INFINITY) ? 0.f : exp_approx(mt - tot.m) / tot.d;
         } else {
             inv = 1.f / row_reduce<T, C, false>(d, sl + C * NW, rank);
         }
@@ -446,17 +457,17 @@ __global__ void __launch_bounds__(T) softmax_elem_kernel(const uint16_t *x, uint
         const float v = ld_half_as_float(xr + j);
         if (v == -INFINITY) continue;  // contributes exp(-inf) = 0
         if (v > acc.m) {
-            acc.d = acc.d * __expf(acc.m - v) + 1.f;  // acc.m = -inf gives 0 * 0
+            acc.d = acc.d * exp_approx(acc.m - v) + 1.f;  // acc.m = -inf gives 0 * 0
             acc.m = v;
         } else {
-            acc.d += __expf(v - acc.m);
+            acc.d += exp_approx(v - acc.m);
         }
     }
     const MaxSum tot = block_combine<T>(acc, red);
     const float inv = 1.f / tot.d;
     for (int64_t j = threadIdx.x; j < N; j += T) {
         const float v = ld_half_as_float(xr + j);
-        reinterpret_cast<__half *>(yr)[j] = __float2half_rn(__expf(v - tot.m) * inv);
+        reinterpret_cast<__half *>(yr)[j] = __float2half_rn(exp_approx(v - tot.m) * inv);
     }
 }
 
@@ -618,33 +629,28 @@ struct SoftmaxVariant {
 
 // The automatic choice is the first entry whose capacity covers the row.
 static const SoftmaxVariant kSoftmax[] = {
-    // the automatic choice, by capacity (measured fastest for each width):
-    // bulk-staged rows smb_t<threads>_e<elements per thread>_c<cluster>_b<staged rows>,
-    // _p: one (max, sum) exchange per row instead of a max then a sum
+    // the automatic choice, by capacity (each measured fastest for its widths);
+    // smb_: rows staged by bulk copies, t<threads>_e<elements per thread>_c<cluster>
+    // _b<staged rows>, _p: one (max, sum) exchange per row instead of a max then a sum;
+    // sm_: rows held in registers with a register prefetch of the next row
     {128, 8, 1, "smb_t128_e8_c1_b3", &launch_softmax_bulk<128, 8, 1, 3, false>},
-    {256, 16, 1, "smb_t256_e16_c1_b3", &launch_softmax_bulk<256, 16, 1, 3, false>},
-    {256, 32, 1, "smb_t256_e32_c1_b3", &launch_softmax_bulk<256, 32, 1, 3, false>},
-    {512, 32, 1, "smb_t512_e32_c1_b2", &launch_softmax_bulk<512, 32, 1, 2, false>},
-    {256, 32, 4, "smb_t256_e32_c4_b2_p", &launch_softmax_bulk<256, 32, 4, 2, true>},
-    {512, 32, 4, "smb_t512_e32_c4_b2_p", &launch_softmax_bulk<512, 32, 4, 2, true>},
-    {512, 32, 8, "smb_t512_e32_c8_b2", &launch_softmax_bulk<512, 32, 8, 2, false>},
-    // alternatives
-    {256, 32, 1, "smb_t256_e32_c1_b2", &launch_softmax_bulk<256, 32, 1, 2, false>},
-    {256, 32, 1, "smb_t256_e32_c1_b2_p", &launch_softmax_bulk<256, 32, 1, 2, true>},
-    {512, 32, 2, "smb_t512_e32_c2_b2", &launch_softmax_bulk<512, 32, 2, 2, false>},
-    {512, 32, 2, "smb_t512_e32_c2_b2_p", &launch_softmax_bulk<512, 32, 2, 2, true>},
-    {256, 32, 4, "smb_t256_e32_c4_b2", &launch_softmax_bulk<256, 32, 4, 2, false>},
-    {512, 32, 8, "smb_t512_e32_c8_b2_p", &launch_softmax_bulk<512, 32, 8, 2, true>},
-    {512, 32, 8, "smb_t512_e32_c8_b3_p", &launch_softmax_bulk<512, 32, 8, 3, true>},
-    // rows held in registers, register prefetch of the next row (single-block rows)
-    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec_v<128, 8, 1>},
     {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec_v<256, 16, 1>},
     {256, 32, 1, "sm_t256_e32_c1", &launch_softmax_vec_v<256, 32, 1>},
     {512, 32, 1, "sm_t512_e32_c1", &launch_softmax_vec_v<512, 32, 1>},
+    {512, 32, 2, "smb_t512_e32_c2_b2_p", &launch_softmax_bulk<512, 32, 2, 2, true>},
+    {512, 32, 4, "smb_t512_e32_c4_b2_p", &launch_softmax_bulk<512, 32, 4, 2, true>},
+    {512, 32, 8, "smb_t512_e32_c8_b2_p", &launch_softmax_bulk<512, 32, 8, 2, true>},
+    // alternatives
+    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec_v<128, 8, 1>},
+    {256, 16, 1, "smb_t256_e16_c1_b3", &launch_softmax_bulk<256, 16, 1, 3, false>},
+    {256, 32, 1, "smb_t256_e32_c1_b2", &launch_softmax_bulk<256, 32, 1, 2, false>},
+    {256, 32, 1, "smb_t256_e32_c1_b2_p", &launch_softmax_bulk<256, 32, 1, 2, true>},
+    {512, 32, 1, "smb_t512_e32_c1_b2", &launch_softmax_bulk<512, 32, 1, 2, false>},
+    {256, 32, 4, "smb_t256_e32_c4_b2_p", &launch_softmax_bulk<256, 32, 4, 2, true>},
+    {512, 32, 8, "smb_t512_e32_c8_b2", &launch_softmax_bulk<512, 32, 8, 2, false>},
+    {512, 32, 8, "smb_t512_e32_c8_b3_p", &launch_softmax_bulk<512, 32, 8, 3, true>},
     {512, 32, 2, "sm_t512_e32_c2", &launch_softmax_vec_v<512, 32, 2>},
-    {512, 32, 4, "sm_t512_e32_c4", &launch_softmax_vec_v<512, 32, 4>},
     {512, 32, 8, "sm_t512_e32_c8", &launch_softmax_vec_v<512, 32, 8>},
-    {256, 32, 4, "sm_t256_e32_c4", &launch_softmax_vec_v<256, 32, 4>},
 };
 constexpr int kSoftmaxVariants = static_cast<int>(sizeof(kSoftmax) / sizeof(kSoftmax[0]));
 
