@@ -251,8 +251,10 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if ((dtype == DT_Q8 || (dtype == DT_Q4 && rb >= 4096)) && small_x) {
         int rs = 1;
         while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
+        // INT8 with four rows per stage: four consumer warps with more chunks each
+        const int warps = (dtype == DT_Q8 && rs == 4) ? 4 : 8;
         for (int k = 0; k < n; ++k) {
-            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == 8 &&
+            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == warps &&
                 variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
                 return k;
         }
