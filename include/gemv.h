@@ -167,8 +167,10 @@ gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t
  * kernel directly; read it after synchronising `stream`.  A, scales and dtype
  * as for gemv_ex.
  * The copy of x is a small kernel that reads the host buffer over the
- * CPU-GPU link, and the GEMV is launched with programmatic dependent launch
- * after it, so the GEMV streams its weights while x is still being fetched.
+ * CPU-GPU link; it is launched with programmatic dependent launch (its blocks
+ * are scheduled while the preceding kernel drains) and reads x only after
+ * that kernel has completed.  The GEMV is launched the same way after it, so
+ * it streams its weights while x is still being fetched.
  * GEMV_FLAG_OVERLAP_PRECEDING: additionally, the kernel that precedes the
  * call on `stream` writes neither A, scales nor x_host (a previous call of
  * this function qualifies); the copy then reads x_host before that kernel has

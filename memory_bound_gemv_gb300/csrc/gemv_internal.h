@@ -130,9 +130,10 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
 // N == 0: y = 0.
 void launch_fill_zero(float *y, int64_t M, cudaStream_t s);
 
-// Copy of x from page-locked host memory by a kernel (gemv_host.cu); with
-// pdl, launched with programmatic stream serialisation.
-void launch_copy_in(const void *src, void *dst, int64_t bytes, bool pdl, cudaStream_t s);
+// Copy of x from page-locked host memory by a kernel (gemv_host.cu), launched
+// with programmatic stream serialisation; early: x is read before the wait
+// for the preceding kernel.
+void launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, cudaStream_t s);
 
 // Symmetric quantisation (gemv_quantize.cu): bits 8 or 4; one scale per row
 // or per 128 columns; FP32 or binary16 weights.
