@@ -334,7 +334,10 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
             if (blocks > resident) blocks = resident;
         }
     }
-    v.launch(a, static_cast<unsigned>(blocks), smem, s, a.pdl != 0);
+    // the kernel families that support it are always launched with
+    // programmatic serialisation; without the flag they wait for the
+    // preceding kernel before touching memory (same ordering as a plain launch)
+    v.launch(a, static_cast<unsigned>(blocks), smem, s, v.supports_pdl());
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
 }

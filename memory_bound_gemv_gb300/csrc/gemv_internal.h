@@ -47,8 +47,10 @@ struct GemvArgs {
     int skip_x_copy;          // test hook: arm the barrier but issue no copy
     int scale_shift;          // scale group of 16-byte chunk c: c >> scale_shift
     int scale_elem_shift;     // scale group of column j: j >> scale_elem_shift
-    int pdl;                  // launched with programmatic serialisation: stream the
-                              // weights before waiting for the preceding kernel
+    int pdl;                  // stream the weights before waiting for the preceding
+                              // kernel (kernels with PDL support are always launched
+                              // with programmatic serialisation; without this flag they
+                              // wait before touching memory)
 };
 
 struct Variant {

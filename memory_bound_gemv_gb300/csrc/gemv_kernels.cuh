@@ -217,11 +217,14 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     // (one vector per chunk), a cooperative transposing load otherwise.
     constexpr bool XBULK = XMODE == XMODE_BULK && XV == 1;
     constexpr bool XCOOP = XMODE == XMODE_BULK && XV > 1;
-    // With programmatic dependent launch the first tile of weights is
-    // requested before waiting for the preceding kernel; x is read and y
-    // written only after that wait.
+    // The kernel is always launched with programmatic stream serialisation.
+    // With p.pdl the first tile of weights is requested before waiting for
+    // the preceding kernel (x is read and y written only after that wait);
+    // without it the kernel waits before it touches any memory, so only its
+    // scheduling overlaps the preceding kernel's drain.
     pdl_trigger();
     const bool pdl = p.pdl != 0;
+    if (!pdl) pdl_wait();
     auto stage_x_bulk = [&]() {
         if (tid == 0) {
             const uint32_t b = smem_addr(bar);
@@ -423,6 +426,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     };
 
     pdl_trigger();
+    if (!p.pdl) pdl_wait();  // see the row-tile kernel
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
