@@ -141,6 +141,27 @@ def test_gemv_ex_rejects_unknown_flags():
     assert L.gemv_ex(9, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
 
 
+def test_host_buffer_and_option_validation():
+    L = mbg.lib()
+    # gemv_ex_host(dtype, A, x_host, x_dev, y_host, M, N, scales, flags, stream):
+    # argument checks come before any device call
+    assert L.gemv_ex_host(mbg.F16, FAKE, FAKE, FAKE, FAKE, 4, 8, None, 2, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex_host(mbg.F16, FAKE, FAKE, FAKE, FAKE, -1, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex_host(9, FAKE, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex_host(mbg.F16, FAKE, FAKE, None, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex_host(mbg.F16, FAKE, FAKE, FAKE + 1, FAKE, 4, 8, None, 0, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_ex_host(mbg.F16, FAKE, FAKE, FAKE, FAKE + 2, 4, 8, None, 0, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_ex_host(mbg.Q4, FAKE, FAKE, FAKE, FAKE, 4, 7, FAKE, 0, None) == mbg.ERR_UNSUPPORTED
+    assert L.gemv_ex_host(mbg.F16, None, None, None, None, 0, 8, None, 0, None) == mbg.OK
+    # the no-allocation variant refuses x beyond its array before anything else
+    assert L.gemv_ex_host_noalloc(mbg.F32, FAKE, FAKE, FAKE, 4, 1 << 20, None, 0, None) == mbg.ERR_UNSUPPORTED
+    # per-row INT8 with flags, FP16 weights with FP32 x
+    assert L.gemv_q8_rowscale_ex(FAKE, FAKE, FAKE, 4, 8, FAKE, 2, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_q8_rowscale_ex(FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_q8_rowscale_run_variant(-1, FAKE, FAKE, FAKE, 4, 8, FAKE, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_ex(mbg.F16X32, FAKE, FAKE + 2, FAKE, 4, 8, None, 0, None) == mbg.ERR_MISALIGNED
+
+
 def test_softmax_and_copy_validation():
     L = mbg.lib()
     assert L.gemv_softmax_f16(FAKE, FAKE, -1, 8, None) == mbg.ERR_INVALID_VALUE
