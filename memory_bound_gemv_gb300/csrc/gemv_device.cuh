@@ -235,7 +235,11 @@ __device__ __forceinline__ const uint4 *x_smem_vec(const unsigned char *xs, int 
 // t = 0 .. nt-1 (reads are coalesced in x's own order).  Loads are issued in
 // batches of eight per thread before any of them is stored, so staging costs
 // one memory round trip per batch instead of one per vector.
-template <int DT>
+// PAIRED (INT4 with the mixed-precision products): each 16-byte vector of x
+// is stored re-paired four columns apart, (x0,x4) (x1,x5) (x2,x6) (x3,x7),
+// the order in which q4_codes_h2 yields the codes, so that every product
+// takes the same half of its two operands.
+template <int DT, bool PAIRED = false>
 __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x, int nchunks, int t,
                                                int nt)
 {
@@ -256,7 +260,15 @@ __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x,
             if (i < n) {
                 const int c = i / XV;
                 const int v = i - c * XV;
-                *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = r[j];
+                uint4 w = r[j];
+                if constexpr (PAIRED) {
+                    const uint4 u = w;
+                    w.x = __byte_perm(u.x, u.z, 0x5410);
+                    w.y = __byte_perm(u.x, u.z, 0x7632);
+                    w.z = __byte_perm(u.y, u.w, 0x5410);
+                    w.w = __byte_perm(u.y, u.w, 0x7632);
+                }
+                *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = w;
             }
         }
     }
@@ -437,7 +449,7 @@ __device__ __forceinline__ void q4_codes_h2(uint32_t w, uint32_t (&h)[4])
 // One 16-byte chunk of A times its x chunk (binary16), accumulated in FP32.
 // Quantised chunks are summed into partials and scaled once per chunk
 // (the chunk lies inside one 128-column group).
-template <int DT>
+template <int DT, bool PAIRED = false>
 __device__ __forceinline__ void chunk_dot_mixed(const uint4 a, const uint4 (&xv)[x_chunk_vecs<DT>()],
                                                 float scale, float (&acc)[NACC])
 {
@@ -469,11 +481,20 @@ __device__ __forceinline__ void chunk_dot_mixed(const uint4 a, const uint4 (&xv)
         for (int k = 0; k < 4; ++k) {
             uint32_t h[4];
             q4_codes_h2(w[k], h);
-            const uint4 &x = xv[k];  // x words (x0,x1) (x2,x3) (x4,x5) (x6,x7)
-            mfma_cross_lo(h[0], x.x, x.z, p[0], p[1]);  // q0*x0, q4*x4
-            mfma_cross_hi(h[1], x.x, x.z, p[2], p[3]);  // q1*x1, q5*x5
-            mfma_cross_lo(h[2], x.y, x.w, p[0], p[1]);  // q2*x2, q6*x6
-            mfma_cross_hi(h[3], x.y, x.w, p[2], p[3]);  // q3*x3, q7*x7
+            const uint4 &x = xv[k];
+            if constexpr (PAIRED) {
+                // x words (x0,x4) (x1,x5) (x2,x6) (x3,x7): same halves as the codes
+                mfma_pair(h[0], x.x, p[0], p[1]);
+                mfma_pair(h[1], x.y, p[2], p[3]);
+                mfma_pair(h[2], x.z, p[0], p[1]);
+                mfma_pair(h[3], x.w, p[2], p[3]);
+            } else {
+                // x words (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+                mfma_cross_lo(h[0], x.x, x.z, p[0], p[1]);  // q0*x0, q4*x4
+                mfma_cross_hi(h[1], x.x, x.z, p[2], p[3]);  // q1*x1, q5*x5
+                mfma_cross_lo(h[2], x.y, x.w, p[0], p[1]);  // q2*x2, q6*x6
+                mfma_cross_hi(h[3], x.y, x.w, p[2], p[3]);  // q3*x3, q7*x7
+            }
         }
 #pragma unroll
         for (int k = 0; k < NACC; ++k) acc[k] = fmaf(scale, p[k], acc[k]);

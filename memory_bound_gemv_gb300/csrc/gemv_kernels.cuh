@@ -217,6 +217,8 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     // (one vector per chunk), a cooperative transposing load otherwise.
     constexpr bool XBULK = XMODE == XMODE_BULK && XV == 1;
     constexpr bool XCOOP = XMODE == XMODE_BULK && XV > 1;
+    // INT4 x staged for the mixed-precision products: paired layout
+    constexpr bool PAIRED = DT == DT_Q4 && MATH == MATH_MIXED && XCOOP;
     // The kernel is always launched with programmatic stream serialisation.
     // With p.pdl the first tile of weights is requested before waiting for
     // the preceding kernel (x is read and y written only after that wait);
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
         if constexpr (XBULK) stage_x_bulk();
     }
 
-    if constexpr (XCOOP) stage_x_vmajor<DT>(xs, p.x, nchunks, tid, T);
+    if constexpr (XCOOP) stage_x_vmajor<DT, PAIRED>(xs, p.x, nchunks, tid, T);
     if constexpr (XMODE == XMODE_BULK) __syncthreads();
     if constexpr (XBULK) {
         if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
                             xv[v] = lds128(xb[v] + k * G * 16);
                     }
                     if constexpr (MATH == MATH_MIXED) {
-                        chunk_dot_mixed<DT>(cur[k], xv, F::QUANT ? scur[k] : 0.f, acc);
+                        chunk_dot_mixed<DT, PAIRED>(cur[k], xv, F::QUANT ? scur[k] : 0.f, acc);
                     } else {
                         float xf[EPC];
                         x_to_float<DT>(xv, xf);
@@ -388,6 +390,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     constexpr int NW = T / 32;  // consumer warps
     static_assert(MATH == MATH_F32 || Fmt<DT>::XB == 2, "an FP32 x uses FP32 math");
     static_assert(NW <= 32, "the producer warp adds one partial per consumer warp");
+    constexpr bool PAIRED = DT == DT_Q4 && MATH == MATH_MIXED;  // see stage_x_vmajor
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     } else {
         // several vectors of x per chunk: transpose x into shared memory,
         // then a named barrier of the consumer warps only
-        stage_x_vmajor<DT>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T);
+        stage_x_vmajor<DT, PAIRED>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T);
         asm volatile("bar.sync 1, %0;" ::"r"(T) : "memory");
     }
     for (int64_t it = 0; it < iters; ++it) {
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
                         else if constexpr (F::QUANT)
                             sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c >> p.scale_shift));
                         if constexpr (MATH == MATH_MIXED) {
-                            chunk_dot_mixed<DT>(a, xv, sc, acc[r]);
+                            chunk_dot_mixed<DT, PAIRED>(a, xv, sc, acc[r]);
                         } else {
                             float wf[F::EPC];
                             chunk_to_float<DT>(a, wf);
