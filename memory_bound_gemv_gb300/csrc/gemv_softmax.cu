@@ -26,6 +26,8 @@
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "gemv_device.cuh"
 
 namespace cg = cooperative_groups;
@@ -498,14 +500,24 @@ __global__ void __launch_bounds__(THREADS) probe_copy_kernel(const uint4 *src, u
 // Launch glue
 // ---------------------------------------------------------------------------
 
-// Resident clusters (of C blocks) for this kernel: the persistent grid size.
-template <int T, int EPT, int C>
-int resident_clusters()
+// A value computed once per device (with that device current): launch set-up
+// such as shared-memory limits and persistent grid sizes, which belong to the
+// device's context.  0 when the device index is out of range.
+constexpr int kSoftmaxMaxDevices = 64;
+
+template <typename F>
+int per_device_once(std::once_flag (&once)[kSoftmaxMaxDevices], int (&val)[kSoftmaxMaxDevices], F compute)
 {
-    static int cached = -1;  // a kernel's occupancy does not change during the process
-    if (cached >= 0) return cached;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSoftmaxMaxDevices) return 0;
+    std::call_once(once[dev], [&] { val[dev] = compute(dev); });
+    return val[dev];
+}
+
+template <int T, int EPT, int C>
+int count_resident_clusters(int dev)
+{
+    int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int n = 0;
     if constexpr (C == 1) {
@@ -526,8 +538,16 @@ int resident_clusters()
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&n, softmax_vec_kernel<T, EPT, C>, &cfg) != cudaSuccess) n = 0;
     }
-    cached = n > 0 ? n : sms;
-    return cached;
+    return n > 0 ? n : sms;
+}
+
+// Resident clusters (of C blocks) for this kernel: the persistent grid size.
+template <int T, int EPT, int C>
+int resident_clusters()
+{
+    static std::once_flag once[kSoftmaxMaxDevices];
+    static int val[kSoftmaxMaxDevices];
+    return per_device_once(once, val, [](int dev) { return count_resident_clusters<T, EPT, C>(dev); });
 }
 
 template <int T, int EPT, int C>
@@ -565,13 +585,14 @@ cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N
                                 uint64_t wait_limit_ns, cudaStream_t s)
 {
     constexpr int SMEM = softmax_bulk_smem(T, EPT, C, NB);
-    static const int resident = [] {
-        // raise the dynamic shared memory limit once, then ask for the occupancy
+    static std::once_flag once[kSoftmaxMaxDevices];
+    static int val[kSoftmaxMaxDevices];
+    const int resident = per_device_once(once, val, [](int dev) {
+        // raise the dynamic shared memory limit once per device, then ask for the occupancy
         if (cudaFuncSetAttribute(softmax_bulk_kernel<T, EPT, C, NB, PAIR>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
             return 0;
-        int dev = 0, sms = 0, n = 0;
-        cudaGetDevice(&dev);
+        int sms = 0, n = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if constexpr (C == 1) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, softmax_bulk_kernel<T, EPT, 1, NB, PAIR>, T,
@@ -594,7 +615,7 @@ cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N
                 return 0;
             return n;
         }
-    }();
+    });
     if (resident <= 0) return cudaErrorNotSupported;
     const int64_t clusters = M < resident ? M : resident;
     cudaLaunchConfig_t cfg = {};
