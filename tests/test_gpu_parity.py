@@ -350,3 +350,40 @@ def test_row_scales_equal_broadcast_group_scales():
         assert torch.equal(y_row, y_grp), v["name"]
         compared += 1
     assert compared >= 5 and bulk >= 1
+
+
+def test_concurrent_calls_from_threads_and_streams():
+    """Entry points called from several host threads, each on its own stream,
+    at the same time (the per-device state and the variant caches are shared)."""
+    import threading
+    cases = [("f16", 300, 4160), ("q4", 129, 4160), ("q8", 257, 4096), ("f32", 64, 1000)]
+    prepared = []
+    for dtype, M, N in cases:
+        inp = synth.make(synth.random_case(dtype, M, N, 880 + M))
+        y_ref, den = reference(dtype, inp, M, N)
+        prepared.append((dtype, upload(dtype, inp), y_ref, den))
+    results = [None] * len(prepared)
+    errors = []
+
+    def work(k):
+        try:
+            dtype, t, _, _ = prepared[k]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                ys = [mbg.gemv(dtype, t["A"], t["x"], t.get("scales")) for _ in range(20)]
+            s.synchronize()
+            results[k] = [y.cpu().numpy() for y in ys]
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(len(prepared))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for (dtype, _, y_ref, den), ys in zip(prepared, results):
+        for y in ys:
+            assert_close(dtype, y, y_ref, den, f"{dtype} concurrent")
+        assert all(np.array_equal(ys[0], y) for y in ys[1:])
+    assert mbg.gemv_get_device_error() == mbg.OK
