@@ -251,12 +251,21 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if ((dtype == DT_Q8 || (dtype == DT_Q4 && rb >= 4096)) && small_x) {
         int rs = 1;
         while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
-        // INT8 with four rows per stage: four consumer warps with more chunks each
-        const int warps = (dtype == DT_Q8 && rs == 4) ? 4 : 8;
-        for (int k = 0; k < n; ++k) {
-            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == warps &&
-                variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
-                return k;
+        // consumer warps: INT8 with four rows per stage takes four (more chunks
+        // each); INT4 takes seven when 224 consumers split the row's chunks more
+        // evenly than 256 (every consumer then takes the same number of chunks;
+        // measured +9 % at 14336 columns, within noise for INT8)
+        int warps = 8;
+        if (dtype == DT_Q8 && rs == 4)
+            warps = 4;
+        else if (dtype == DT_Q4 && (chunks + 223) / 224 * 224 < (chunks + 255) / 256 * 256)
+            warps = 7;
+        for (int attempt = 0; attempt < 2; ++attempt, warps = 8) {
+            for (int k = 0; k < n; ++k) {
+                if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == warps &&
+                    variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
+                    return k;
+            }
         }
     }
     if (small_x && chunks <= static_cast<int64_t>(kTileMaxThreads) * kTileChunks) {

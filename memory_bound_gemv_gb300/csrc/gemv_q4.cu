@@ -17,6 +17,7 @@ static const Variant kTableQ4[] = {
     MBG_BULK(DT_Q4, 512, 4, 4, "bulk_t512_r4_s4"),
     MBG_BULK(DT_Q4, 256, 8, 3, "bulk_t256_r8_s3"),
     MBG_BULK(DT_Q4, 512, 8, 4, "bulk_t512_r8_s4"),
+    MBG_BULK(DT_Q4, 224, 2, 3, "bulk_t224_r2_s3"),
     // row tiles (the automatic choice for rows up to 512 * 8 * 16 bytes)
     MBG_TILE(DT_Q4, 1, 8, 256, XMODE_BULK, "tile_g1_c8_t256_bulk"),
     MBG_TILE(DT_Q4, 2, 8, 256, XMODE_BULK, "tile_g2_c8_t256_bulk"),
