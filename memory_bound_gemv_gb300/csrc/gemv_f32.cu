@@ -39,6 +39,12 @@ static const Variant kTableF32[] = {
     MBG_TILE(DT_F32, 256, 8, 256, XMODE_L1, "tile_g256_c8_t256_l1"),
     MBG_TILE(DT_F32, 512, 8, 512, XMODE_L1, "tile_g512_c8_t512_l1"),
     // rows of a warp (or of part of one) with a rolling buffer of loads
+    // 128-thread blocks (finer tiles, more blocks per SM)
+    MBG_TILE(DT_F32, 16, 8, 128, XMODE_BULK, "tile_g16_c8_t128_bulk"),
+    MBG_TILE(DT_F32, 32, 8, 128, XMODE_BULK, "tile_g32_c8_t128_bulk"),
+    MBG_TILE(DT_F32, 32, 8, 128, XMODE_L1, "tile_g32_c8_t128_l1"),
+    MBG_TILE(DT_F32, 64, 8, 128, XMODE_L1, "tile_g64_c8_t128_l1"),
+    MBG_TILE(DT_F32, 128, 8, 128, XMODE_L1, "tile_g128_c8_t128_l1"),
     MBG_VEC(DT_F32, 32, 1, 8, 4, XMODE_BULK, "w32_r1_u8_w4_bulk"),
     MBG_VEC(DT_F32, 32, 1, 4, 8, XMODE_BULK, "w32_r1_u4_w8_bulk"),
     MBG_VEC(DT_F32, 32, 2, 4, 4, XMODE_BULK, "w32_r2_u4_w4_bulk"),
