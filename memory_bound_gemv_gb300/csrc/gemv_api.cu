@@ -214,13 +214,13 @@ int resident_blocks(DeviceState &d, int dtype, int vid, const Variant &v, size_t
     return total;
 }
 
-int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps = 0)
+int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps = 0, int unroll = 0)
 {
     int n = 0;
     const Variant *v = table(dtype, &n);
     for (int k = 0; k < n; ++k)
         if (v[k].lanes_per_row == lpr && v[k].xmode == xmode && v[k].kind == kind &&
-            (warps == 0 || v[k].warps == warps))
+            (warps == 0 || v[k].warps == warps) && (unroll == 0 || v[k].unroll == unroll))
             return k;
     return -1;
 }
@@ -275,8 +275,11 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
         const bool via_l1 = (dtype == DT_F32 || dtype == DT_F16) && g >= 128;
         if ((dtype == DT_F32 || dtype == DT_F16) && g >= 32 && g <= 128) {
             // rows of 2-16 KB: 128-thread blocks (finer tiles, more blocks per
-            // SM) with x through L1 (measured +5-18 % on 1024-8192 columns)
-            const int k = find_variant(dtype, g, XMODE_L1, KIND_TILE, 4);
+            // SM) with x through L1 (measured +5-18 % on 1024-8192 columns);
+            // rows of 4-8 KB as one row per block with four chunks per thread
+            int k = g == 64 ? find_variant(dtype, 128, XMODE_L1, KIND_TILE, 4, 4) : -1;
+            if (k < 0 || !variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
+                k = find_variant(dtype, g, XMODE_L1, KIND_TILE, 4, kTileChunks);
             if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         }
         int k = find_variant(dtype, g, via_l1 ? XMODE_L1 : XMODE_BULK, KIND_TILE, warps);

@@ -45,6 +45,7 @@ static const Variant kTableF16[] = {
     MBG_TILE(DT_F16, 64, 8, 128, XMODE_L1, "tile_g64_c8_t128_l1"),
     MBG_TILE(DT_F16, 64, 8, 128, XMODE_BULK, "tile_g64_c8_t128_bulk"),
     MBG_TILE(DT_F16, 128, 8, 128, XMODE_L1, "tile_g128_c8_t128_l1"),
+    MBG_TILE(DT_F16, 128, 4, 128, XMODE_L1, "tile_g128_c4_t128_l1"),
     // row tiles with operands converted to FP32 (for comparison)
     MBG_TILE_M(DT_F16, 64, 8, 256, XMODE_BULK, MATH_F32, "tile_g64_c8_t256_bulk_f32math"),
     MBG_TILE_M(DT_F16, 256, 8, 256, XMODE_BULK, MATH_F32, "tile_g256_c8_t256_bulk_f32math"),

@@ -45,6 +45,7 @@ static const Variant kTableF32[] = {
     MBG_TILE(DT_F32, 32, 8, 128, XMODE_L1, "tile_g32_c8_t128_l1"),
     MBG_TILE(DT_F32, 64, 8, 128, XMODE_L1, "tile_g64_c8_t128_l1"),
     MBG_TILE(DT_F32, 128, 8, 128, XMODE_L1, "tile_g128_c8_t128_l1"),
+    MBG_TILE(DT_F32, 128, 4, 128, XMODE_L1, "tile_g128_c4_t128_l1"),
     MBG_VEC(DT_F32, 32, 1, 8, 4, XMODE_BULK, "w32_r1_u8_w4_bulk"),
     MBG_VEC(DT_F32, 32, 1, 4, 8, XMODE_BULK, "w32_r1_u4_w8_bulk"),
     MBG_VEC(DT_F32, 32, 2, 4, 4, XMODE_BULK, "w32_r2_u4_w4_bulk"),
