@@ -282,6 +282,12 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
                 k = find_variant(dtype, g, XMODE_L1, KIND_TILE, 4, kTileChunks);
             if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         }
+        if (dtype == DT_Q4 && g == 16) {
+            // INT4 rows of 1-2 KB: one row per 128-thread block, four chunks per
+            // thread (measured +6 % at 4096 columns)
+            const int k = find_variant(dtype, 32, XMODE_BULK, KIND_TILE, 4, 4);
+            if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
+        }
         int k = find_variant(dtype, g, via_l1 ? XMODE_L1 : XMODE_BULK, KIND_TILE, warps);
         if (k >= 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         k = find_variant(dtype, g, XMODE_BULK, KIND_TILE, warps);

@@ -35,6 +35,7 @@ static const Variant kTableQ4[] = {
     MBG_TILE(DT_Q4, 256, 8, 512, XMODE_BULK, "tile_g256_c8_t512_bulk"),
     MBG_TILE(DT_Q4, 512, 4, 512, XMODE_BULK, "tile_g512_c4_t512_bulk"),
     MBG_TILE(DT_Q4, 256, 4, 256, XMODE_BULK, "tile_g256_c4_t256_bulk"),
+    MBG_TILE(DT_Q4, 32, 4, 128, XMODE_BULK, "tile_g32_c4_t128_bulk"),
     MBG_TILE(DT_Q4, 64, 8, 256, XMODE_L1, "tile_g64_c8_t256_l1"),
     MBG_TILE(DT_Q4, 128, 8, 256, XMODE_L1, "tile_g128_c8_t256_l1"),
     MBG_TILE(DT_Q4, 256, 8, 256, XMODE_L1, "tile_g256_c8_t256_l1"),
