@@ -59,16 +59,18 @@ __device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b)
     return {m, a.d * exp_approx(a.m - m) + b.d * exp_approx(b.m - m)};
 }
 
+// (max, sum) over a warp: the maximum first, then every lane's sum rescaled
+// to it once and added up (one exponential per lane instead of one per
+// butterfly level).
 __device__ __forceinline__ MaxSum warp_combine(MaxSum v)
 {
+    float m = v.m;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        MaxSum o;
-        o.m = __shfl_xor_sync(0xffffffffu, v.m, off);
-        o.d = __shfl_xor_sync(0xffffffffu, v.d, off);
-        v = combine(v, o);
-    }
-    return v;
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float d = (v.m == -INFINITY) ? 0.f : v.d * exp_approx(v.m - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    return {m, d};
 }
 
 // Combine over the block; every thread receives the result.  `red` holds at
@@ -654,7 +656,7 @@ static const SoftmaxVariant kSoftmax[] = {
     // smb_: rows staged by bulk copies, t<threads>_e<elements per thread>_c<cluster>
     // _b<staged rows>, _p: one (max, sum) exchange per row instead of a max then a sum;
     // sm_: rows held in registers with a register prefetch of the next row
-    {128, 8, 1, "smb_t128_e8_c1_b3", &launch_softmax_bulk<128, 8, 1, 3, false>},
+    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec_v<128, 8, 1>},
     {256, 16, 1, "sm_t256_e16_c1", &launch_softmax_vec_v<256, 16, 1>},
     {256, 32, 1, "sm_t256_e32_c1", &launch_softmax_vec_v<256, 32, 1>},
     {512, 32, 1, "sm_t512_e32_c1", &launch_softmax_vec_v<512, 32, 1>},
@@ -662,7 +664,7 @@ static const SoftmaxVariant kSoftmax[] = {
     {512, 32, 4, "smb_t512_e32_c4_b2_p", &launch_softmax_bulk<512, 32, 4, 2, true>},
     {512, 32, 8, "smb_t512_e32_c8_b2_p", &launch_softmax_bulk<512, 32, 8, 2, true>},
     // alternatives
-    {128, 8, 1, "sm_t128_e8_c1", &launch_softmax_vec_v<128, 8, 1>},
+    {128, 8, 1, "smb_t128_e8_c1_b3", &launch_softmax_bulk<128, 8, 1, 3, false>},
     {256, 16, 1, "smb_t256_e16_c1_b3", &launch_softmax_bulk<256, 16, 1, 3, false>},
     {256, 32, 1, "smb_t256_e32_c1_b2", &launch_softmax_bulk<256, 32, 1, 2, false>},
     {256, 32, 1, "smb_t256_e32_c1_b2_p", &launch_softmax_bulk<256, 32, 1, 2, true>},
