@@ -532,9 +532,11 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         for (int r = 0; r < RS; ++r)
 #pragma unroll
             for (int k = 0; k < NACC; ++k) acc[r][k] = 0.f;
-        // ROW_SCALE: one scale per row, read once per tile from global memory
-        auto dot_rows = [&](auto row_scale) {
+        // ROW_SCALE: one scale per row, read once per tile from global memory;
+        // FULL: all RS rows of the tile exist (no per-row checks in the loop)
+        auto dot_rows = [&](auto row_scale, auto full_tile) {
             constexpr bool ROW_SCALE = decltype(row_scale)::value;
+            constexpr bool FULL = decltype(full_tile)::value;
             float rsc[ROW_SCALE ? RS : 1];
             if constexpr (ROW_SCALE) {
 #pragma unroll
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
                 if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
                 for (int r = 0; r < RS; ++r) {
-                    if (r < rows) {
+                    if (FULL || r < rows) {
                         const uint4 a = lds128(st + r * rb + c16);
                         float sc = 0.f;
                         if constexpr (ROW_SCALE)
@@ -569,10 +571,11 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
             }
         };
         if constexpr (F::QUANT) {
-            if (p.groups == 1) dot_rows(std::true_type{});
-            else dot_rows(std::false_type{});
+            if (p.groups == 1) dot_rows(std::true_type{}, std::false_type{});
+            else if (rows == RS) dot_rows(std::false_type{}, std::true_type{});
+            else dot_rows(std::false_type{}, std::false_type{});
         } else {
-            dot_rows(std::false_type{});
+            dot_rows(std::false_type{}, std::false_type{});
         }
         float *pp = part + slot * NW * RS;
 #pragma unroll
