@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
         fill = 0;
     };
 
+    const bool full_slots = tg + (CPT - 1) * G < nchunks;
     for (; tile < ntiles; tile += gridDim.x) {
         const int64_t next = tile + gridDim.x;
         if (next < ntiles) load_tile(next, nxt, snxt);
@@ -310,11 +311,13 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
         const int64_t row = tile * RT + grp;
         const bool valid = row < p.M;
         float acc[NACC] = {0.f, 0.f, 0.f, 0.f};
-        if (valid) {
+        // FULL: every chunk slot of this thread lies inside the row (no checks)
+        auto dot = [&](auto full) {
+            constexpr bool FULL = decltype(full)::value;
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
                 const int c = tg + k * G;
-                if (c < nchunks) {
+                if (FULL || c < nchunks) {
                     uint4 xv[XV];
 #pragma unroll
                     for (int v = 0; v < XV; ++v) {
@@ -333,6 +336,16 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
                         chunk_fma<DT>(wf, xf, F::QUANT ? scur[k] : 0.f, acc);
                     }
                 }
+            }
+        };
+        if (valid) {
+            // the check-free copy pays for the instruction-bound quantised
+            // types; for the others the second copy only costs registers
+            if constexpr (F::QUANT) {
+                if (full_slots) dot(std::true_type{});
+                else dot(std::false_type{});
+            } else {
+                dot(std::false_type{});
             }
         }
         float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
