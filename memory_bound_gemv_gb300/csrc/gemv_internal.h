@@ -96,7 +96,7 @@ __host__ __device__ inline BulkLayout bulk_layout(int S, int RS, int T, int64_t 
 {
     BulkLayout L;
     L.part = round16(8 * (2 * S + 1) + 4);
-    L.x = L.part + round16(static_cast<int64_t>(S) * (T / 32) * RS * 4);
+    L.x = L.part + round16(static_cast<int64_t>(S) * T * RS * 4);  // one partial per thread and row
     L.stage = L.x + round16(x_bytes);
     L.stage_bytes = static_cast<int>(RS * row_bytes);
     L.scale = L.stage + S * L.stage_bytes;

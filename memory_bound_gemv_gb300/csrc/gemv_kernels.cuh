@@ -381,11 +381,11 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 //
 // Warp roles.  T/32 consumer warps wait on a stage's "full" barrier, read the
 // tile from shared memory (thread t takes chunks t, t+T, ... of every row of
-// the tile and loads each x chunk once for all RS rows), reduce their partial
-// sums per row with an XOR butterfly, store one partial per warp and row, and
-// arrive on the stage's "reduced" barrier.  One producer warp waits on
-// "reduced", adds the warp partials of each row, writes y and refills the
-// stage with the tile S positions ahead.  No block-wide barrier sits in the
+// the tile and loads each x chunk once for all RS rows), store one partial sum
+// per thread and row, and arrive on the stage's "reduced" barrier.  One
+// producer warp waits on "reduced", adds the partials of each row (a fixed
+// order, then an XOR butterfly), writes y and refills the stage with the tile
+// S positions ahead.  No block-wide barrier sits in the
 // loop, so consumer warps never wait for one another.  Quantised tiles bring
 // their rows' scales along in a second bulk copy on the same barrier.
 //
@@ -483,10 +483,14 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
             }
             const int64_t r0 = (blockIdx.x + done * grid) * RS;
             const int rows = static_cast<int>(min(static_cast<int64_t>(RS), p.M - r0));
-            const float *pp = part + slot * NW * RS;
+            // one partial per consumer thread and row: each lane adds T/32 of
+            // them (in a fixed order), then the warp butterfly
+            const float *pp = part + slot * T * RS;
 #pragma unroll
             for (int r = 0; r < RS; ++r) {
-                float v = lane < NW ? pp[lane * RS + r] : 0.f;
+                float v = 0.f;
+#pragma unroll
+                for (int i = lane; i < T; i += 32) v += pp[r * T + i];
                 v = group_sum<32>(v);
                 if (lane == 0 && r < rows) p.y[r0 + r] = v;
             }
@@ -590,13 +594,12 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         } else {
             dot_rows(std::false_type{}, std::false_type{});
         }
-        float *pp = part + slot * NW * RS;
+        // each thread leaves its row sums for the producer warp to add up
+        // (no butterfly in the consumer warps)
+        float *pp = part + slot * T * RS;
 #pragma unroll
-        for (int r = 0; r < RS; ++r) {
-            float v = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
-            v = group_sum<32>(v);
-            if (lane == 0) pp[warp * RS + r] = v;
-        }
+        for (int r = 0; r < RS; ++r) pp[r * T + tid] = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+        __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&red[slot]));
     }
 }
