@@ -311,7 +311,10 @@ typedef struct {
     int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1),
                             the consumer threads of the block (family 3) */
     int rows_per_group;  /* rows one lane group streams together (family 0, x reuse) */
-    int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread */
+    int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread;
+                            family 3: chunks per consumer thread and row when the variant is
+                            specialised for rows of exactly unroll * threads_per_row chunks
+                            (0: any row length) */
     int warps;           /* warps per block */
     int math;            /* 0: operands converted to FP32; 1: binary16 operands into
                             mixed-precision FMAs with FP32 accumulation */

@@ -175,6 +175,8 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
     if (rb / 16 > INT_MAX / 64) return false;
     if (static_cast<int64_t>(smem_bytes(v, dtype, N, groups)) > d.max_smem) return false;
     if (v.kind == KIND_BULK) {
+        // a fixed chunk count per consumer thread must match the row exactly
+        if (v.unroll > 0 && rb / 16 != static_cast<int64_t>(v.unroll) * v.lanes_per_row) return false;
         // one stage (rows + their scales) is one transaction count of an mbarrier
         const int64_t g = groups;
         const bool quant = is_quant(dtype);
@@ -260,10 +262,17 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
             warps = 4;
         else if (dtype == DT_Q4 && (chunks + 223) / 224 * 224 < (chunks + 255) / 256 * 256)
             warps = 7;
+        // a variant with a fixed chunk count per consumer thread that covers
+        // this row length exactly comes first (table order), then the general ones
+        for (int k = 0; k < n; ++k) {
+            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].unroll > 0 &&
+                variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
+                return k;
+        }
         for (int attempt = 0; attempt < 2; ++attempt, warps = 8) {
             for (int k = 0; k < n; ++k) {
                 if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == warps &&
-                    variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
+                    v[k].unroll == 0 && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
                     return k;
             }
         }

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 // (each decision made warp-uniform first), and the producer first waits
 // (bounded) for the copies it still has in flight, so no copy can land in
 // shared memory after the block has exited.
-template <int DT, int T, int RS, int S, int MATH>
+template <int DT, int T, int RS, int S, int MATH, int CF>
 __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
@@ -526,6 +526,18 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         stage_x_vmajor<DT, PAIRED>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T);
         asm volatile("bar.sync 1, %0;" ::"r"(T) : "memory");
     }
+    // x plane bases (vector-major x), and with a fixed chunk count this
+    // thread's x addresses and scale offsets
+    const uint32_t t16 = static_cast<uint32_t>(tid) * 16u;
+    uint32_t xbase[XV], xthr[XV];
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+        xbase[v] = smem_addr(xs) + static_cast<uint32_t>(v) * static_cast<uint32_t>(nchunks) * 16u;
+        xthr[v] = xbase[v] + t16;
+    }
+    uint32_t sgrp[CF > 0 ? CF : 1];
+#pragma unroll
+    for (int j = 0; j < (CF > 0 ? CF : 1); ++j) sgrp[j] = 2u * static_cast<uint32_t>((tid + j * T) >> p.scale_shift);
     for (int64_t it = 0; it < iters; ++it) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
         const int slot = static_cast<int>(it % S);
@@ -540,8 +552,6 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         // 32-bit shared-space addresses, per-row offsets hoisted out of the loop
         const uint32_t st = smem_addr(smem + L.stage + slot * L.stage_bytes);
         const uint32_t ss = smem_addr(smem + L.scale + slot * L.scale_bytes);
-        const uint32_t xa = smem_addr(xs);
-        const uint32_t xstride = static_cast<uint32_t>(nchunks) * 16u;
         const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
         const uint32_t gb = static_cast<uint32_t>(2 * p.groups);
         float acc[RS][NACC];
@@ -559,23 +569,24 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 #pragma unroll
                 for (int r = 0; r < RS; ++r) rsc[r] = r < rows ? ld_half_as_float(p.scales + r0 + r) : 0.f;
             }
-#pragma unroll 2
-            for (int c = tid; c < nchunks; c += T) {
-                const uint32_t c16 = static_cast<uint32_t>(c) * 16u;
+            // one chunk of every row of the tile: x vectors at xrow[v] + off,
+            // row r of the stage at arow[r] + off, its scale at srow[r] + soff
+            auto chunk = [&](const uint32_t (&xrow)[XV], const uint32_t (&arow)[RS],
+                             const uint32_t (&srow)[RS], uint32_t off, uint32_t soff) {
                 uint4 xv[XV];
 #pragma unroll
-                for (int v = 0; v < XV; ++v) xv[v] = lds128(xa + v * xstride + c16);
+                for (int v = 0; v < XV; ++v) xv[v] = lds128(xrow[v] + off);
                 float xf[MATH == MATH_F32 ? F::EPC : 1];
                 if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
                 for (int r = 0; r < RS; ++r) {
                     if (FULL || r < rows) {
-                        const uint4 a = lds128(st + r * rb + c16);
+                        const uint4 a = lds128(arow[r] + off);
                         float sc = 0.f;
                         if constexpr (ROW_SCALE)
                             sc = rsc[r];
                         else if constexpr (F::QUANT)
-                            sc = lds_half_as_float(ss + r * gb + 2u * static_cast<uint32_t>(c >> p.scale_shift));
+                            sc = lds_half_as_float(srow[r] + soff);
                         if constexpr (MATH == MATH_MIXED) {
                             chunk_dot_mixed<DT, PAIRED>(a, xv, sc, acc[r]);
                         } else {
@@ -585,6 +596,25 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
                         }
                     }
                 }
+            };
+            uint32_t arow[RS], srow[RS];
+#pragma unroll
+            for (int r = 0; r < RS; ++r) {
+                arow[r] = st + r * rb;
+                srow[r] = ss + r * gb;
+            }
+            if constexpr (CF > 0) {
+                // exactly CF chunks per thread and row: fixed offsets from
+                // per-thread bases (no address arithmetic in the loop)
+#pragma unroll
+                for (int r = 0; r < RS; ++r) arow[r] += t16;
+#pragma unroll
+                for (int j = 0; j < CF; ++j) chunk(xthr, arow, srow, j * T * 16u, sgrp[j]);
+            } else {
+#pragma unroll 2
+                for (int c = tid; c < nchunks; c += T)
+                    chunk(xbase, arow, srow, static_cast<uint32_t>(c) * 16u,
+                          2u * static_cast<uint32_t>(c >> p.scale_shift));
             }
         };
         if constexpr (F::QUANT) {
@@ -738,32 +768,36 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
 #define MBG_TILE(DT, G, CPT, T, XM, NAME) \
     MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
 
-template <int DT, int T, int RS, int S, int MATH>
+template <int DT, int T, int RS, int S, int MATH, int CF>
 void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH>, a, grid, T + 32, smem, s, pdl);
+    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH, CF>, a, grid, T + 32, smem, s, pdl);
 }
 
-template <int DT, int T, int RS, int S, int MATH>
+template <int DT, int T, int RS, int S, int MATH, int CF>
 cudaError_t smem_limit_bulk(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH>,
+    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH, CF>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DT, int T, int RS, int S, int MATH>
+template <int DT, int T, int RS, int S, int MATH, int CF>
 cudaError_t occupancy_bulk(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH, CF>,
                                                          T + 32, smem);
 }
 
-#define MBG_BULK_M(DT, T, RS, S, MATH, NAME)                                                    \
-    Variant{DT, T, RS, 1, T / 32, XMODE_BULK, NAME, &launch_bulk<DT, T, RS, S, MATH>,            \
-            &smem_limit_bulk<DT, T, RS, S, MATH>, KIND_BULK, 0, &occupancy_bulk<DT, T, RS, S, MATH>, \
-            MATH, S}
+// unroll = CF: chunks per consumer thread and row when fixed (0: any row length)
+#define MBG_BULK_MF(DT, T, RS, S, MATH, CF, NAME)                                                 \
+    Variant{DT, T, RS, CF, T / 32, XMODE_BULK, NAME, &launch_bulk<DT, T, RS, S, MATH, CF>,         \
+            &smem_limit_bulk<DT, T, RS, S, MATH, CF>, KIND_BULK, 0,                                 \
+            &occupancy_bulk<DT, T, RS, S, MATH, CF>, MATH, S}
+#define MBG_BULK_M(DT, T, RS, S, MATH, NAME) MBG_BULK_MF(DT, T, RS, S, MATH, 0, NAME)
 #define MBG_BULK(DT, T, RS, S, NAME) \
     MBG_BULK_M(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
+#define MBG_BULK_F(DT, T, RS, S, CF, NAME) \
+    MBG_BULK_MF(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), CF, NAME)
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -387,3 +387,25 @@ def test_concurrent_calls_from_threads_and_streams():
             assert_close(dtype, y, y_ref, den, f"{dtype} concurrent")
         assert all(np.array_equal(ys[0], y) for y in ys[1:])
     assert mbg.gemv_get_device_error() == mbg.OK
+
+
+def test_fixed_chunk_bulk_variants_with_ragged_rows():
+    """Bulk variants specialised for an exact chunk count per thread, on row
+    counts that leave a partial last tile."""
+    checked = 0
+    for dtype, M, N in (("q4", 37, 14336), ("q8", 37, 4096), ("q4", 3, 14336)):
+        inp = synth.make(synth.random_case(dtype, M, N, 4000 + M))
+        y_ref, den = reference(dtype, inp, M, N)
+        t = upload(dtype, inp)
+        for v in mbg.variants(dtype):
+            if v["kind"] != "bulk" or v["unroll"] == 0:
+                continue
+            try:
+                y = mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], t.get("scales"))
+            except mbg.GemvError as e:
+                assert e.status == mbg.ERR_UNSUPPORTED
+                continue
+            torch.cuda.synchronize()
+            assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} {v['name']} {M}x{N}")
+            checked += 1
+    assert checked >= 2
