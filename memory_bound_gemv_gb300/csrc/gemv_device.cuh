@@ -30,6 +30,17 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
 }
 
 // 16-byte read-only load that may allocate in L1 (x, when it is not staged).
+// An ordinary 16-byte load cached in L2 only (not the read-only path).
+__device__ __forceinline__ uint4 ld_l2_16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p)
+        : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint4 ld_cached16(const void *p)
 {
     uint4 v;
@@ -235,25 +246,34 @@ __device__ __forceinline__ const uint4 *x_smem_vec(const unsigned char *xs, int 
 // t = 0 .. nt-1 (reads are coalesced in x's own order).  Loads are issued in
 // batches of eight per thread before any of them is stored, so staging costs
 // one memory round trip per batch instead of one per vector.
+// ORDERED: the loads are ordinary (not read-only-path) loads, which the
+// compiler keeps ahead of a barrier arrive that follows them, and
+// after_issue() runs once in every thread, at the same point in all of them,
+// as soon as the first batch has been issued (before any of it is used).
 // PAIRED (INT4 with the mixed-precision products): each 16-byte vector of x
 // is stored re-paired four columns apart, (x0,x4) (x1,x5) (x2,x6) (x3,x7),
 // the order in which q4_codes_h2 yields the codes, so that every product
 // takes the same half of its two operands.
-template <int DT, bool PAIRED = false>
+struct NoOp {
+    __device__ void operator()() const {}
+};
+
+template <int DT, bool PAIRED = false, bool ORDERED = false, typename AfterIssue = NoOp>
 __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x, int nchunks, int t,
-                                               int nt)
+                                               int nt, AfterIssue after_issue = AfterIssue{})
 {
     constexpr int XV = x_chunk_vecs<DT>();
     constexpr int B = 8;
     const uint4 *src = static_cast<const uint4 *>(x);
     const int n = nchunks * XV;
-    for (int base = t; base < n; base += B * nt) {
+    auto batch = [&](int base, auto first) {
         uint4 r[B];
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             const int i = base + j * nt;
-            if (i < n) r[j] = ld_cached16(src + i);
+            if (i < n) r[j] = ORDERED ? ld_l2_16(src + i) : ld_cached16(src + i);
         }
+        if constexpr (decltype(first)::value) after_issue();
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             const int i = base + j * nt;
@@ -271,6 +291,12 @@ __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x,
                 *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = w;
             }
         }
+    };
+    if constexpr (ORDERED) {
+        batch(t, std::true_type{});
+        for (int base = t + B * nt; base < n; base += B * nt) batch(base, std::false_type{});
+    } else {
+        for (int base = t; base < n; base += B * nt) batch(base, std::false_type{});
     }
 }
 

@@ -456,21 +456,29 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     if (warp == NW) {
         // ---------------- producer warp ----------------
         int64_t issued = 0;
-        if (lane == 0) {
-            // with programmatic dependent launch the weights stream in before
-            // the wait for the preceding kernel; x only after it
-            if (p.pdl) {
+        // with programmatic dependent launch the weights stream in before the
+        // wait for the preceding kernel; x only after it
+        if (p.pdl) {
+            if (lane == 0)
                 for (; issued < S && issued < iters; ++issued) issue(issued);
-                pdl_wait();
-            }
-            if constexpr (XV == 1) {
+            pdl_wait();  // the whole producer warp writes y only after the wait
+        }
+        if constexpr (XV == 1) {
+            if (lane == 0) {
                 mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
                 if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
             }
-            for (; issued < S && issued < iters; ++issued) issue(issued);
+        } else {
+            // the consumer warps load x: the first stage goes out at once, the
+            // other stages only once the x loads have been issued (queued
+            // behind a burst of S stages from every block, x would arrive only
+            // when the whole burst has, and no consumer can start before it)
+            if (lane == 0 && issued == 0 && iters > 0) issue(issued++);
+            asm volatile("bar.sync 2, %0;" ::"r"(T + 32) : "memory");
         }
+        if (lane == 0)
+            for (; issued < S && issued < iters; ++issued) issue(issued);
         issued = __shfl_sync(0xffffffffu, issued, 0);
-        if (p.pdl) pdl_wait();  // the whole producer warp writes y only after the wait
         int64_t done = 0;
         for (; done < iters; ++done) {
             const int slot = static_cast<int>(done % S);
@@ -523,7 +531,11 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     } else {
         // several vectors of x per chunk: transpose x into shared memory,
         // then a named barrier of the consumer warps only
-        stage_x_vmajor<DT, PAIRED>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T);
+        // (every consumer warp arrives on barrier 2 once its first x loads
+        // are out; the producer warp waits there before copying weights)
+        stage_x_vmajor<DT, PAIRED, true>(const_cast<unsigned char *>(xs), p.x, nchunks, tid, T, [] {
+            asm volatile("bar.arrive 2, %0;" ::"r"(T + 32) : "memory");
+        });
         asm volatile("bar.sync 1, %0;" ::"r"(T) : "memory");
     }
     // x plane bases (vector-major x), and with a fixed chunk count this
