@@ -248,8 +248,18 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     const int64_t chunks = rb / 16;
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
     // the quantised types are bound by instruction issue: the bulk-copy
-    // pipeline (no load instructions for A) wins for INT8, and for INT4 rows
-    // of 4 KB or more; shorter INT4 rows do better in row tiles
+    // pipeline (no load instructions for A) wins.  A variant specialised for
+    // exactly this row length (a fixed chunk count per consumer thread) comes
+    // first, in table order (measured best first); otherwise the general
+    // pipelines for INT8 and for INT4 rows of 4 KB or more, and row tiles for
+    // shorter INT4 rows
+    if ((dtype == DT_Q8 || dtype == DT_Q4) && small_x) {
+        for (int k = 0; k < n; ++k) {
+            if (v[k].kind == KIND_BULK && v[k].unroll > 0 &&
+                variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
+                return k;
+        }
+    }
     if ((dtype == DT_Q8 || (dtype == DT_Q4 && rb >= 4096)) && small_x) {
         int rs = 1;
         while (rs < 8 && 2 * rs * rb <= 16 * 1024) rs *= 2;
@@ -262,13 +272,6 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
             warps = 4;
         else if (dtype == DT_Q4 && (chunks + 223) / 224 * 224 < (chunks + 255) / 256 * 256)
             warps = 7;
-        // a variant with a fixed chunk count per consumer thread that covers
-        // this row length exactly comes first (table order), then the general ones
-        for (int k = 0; k < n; ++k) {
-            if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].unroll > 0 &&
-                variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
-                return k;
-        }
         for (int attempt = 0; attempt < 2; ++attempt, warps = 8) {
             for (int k = 0; k < n; ++k) {
                 if (v[k].kind == KIND_BULK && v[k].rows_per_group == rs && v[k].warps == warps &&

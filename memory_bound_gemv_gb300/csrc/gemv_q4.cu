@@ -8,8 +8,10 @@ namespace mbg {
 
 static const Variant kTableQ4[] = {
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
-    // fixed chunks per consumer thread (rows of exactly f * t chunks)
+    // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
+    // given row length the first that fits is the automatic choice
     MBG_BULK_F(DT_Q4, 224, 2, 3, 2, "bulk_t224_r2_s3_f2"),
+    MBG_BULK_F(DT_Q4, 128, 4, 3, 1, "bulk_t128_r4_s3_f1"),
     MBG_BULK(DT_Q4, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q4, 256, 1, 3, "bulk_t256_r1_s3"),
     MBG_BULK(DT_Q4, 512, 1, 4, "bulk_t512_r1_s4"),

@@ -9,9 +9,11 @@ namespace mbg {
 static const Variant kTableQ8[] = {
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),
-    // fixed chunks per consumer thread (rows of exactly f * t chunks)
-    MBG_BULK_F(DT_Q8, 128, 4, 2, 2, "bulk_t128_r4_s2_f2"),
+    // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
+    // given row length the first that fits is the automatic choice
+    MBG_BULK_F(DT_Q8, 128, 4, 3, 2, "bulk_t128_r4_s3_f2"),
     MBG_BULK_F(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4"),
+    MBG_BULK_F(DT_Q8, 128, 4, 2, 2, "bulk_t128_r4_s2_f2"),
     MBG_BULK(DT_Q8, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q8, 512, 1, 4, "bulk_t512_r1_s4"),
     MBG_BULK(DT_Q8, 256, 2, 4, "bulk_t256_r2_s4"),

@@ -392,8 +392,9 @@ def test_concurrent_calls_from_threads_and_streams():
 def test_fixed_chunk_bulk_variants_with_ragged_rows():
     """Bulk variants specialised for an exact chunk count per thread, on row
     counts that leave a partial last tile."""
-    checked = 0
-    for dtype, M, N in (("q4", 37, 14336), ("q8", 37, 4096), ("q4", 3, 14336)):
+    checked = set()
+    for dtype, M, N in (("q4", 37, 14336), ("q4", 37, 4096), ("q8", 37, 4096), ("q8", 37, 14336),
+                        ("q4", 3, 14336), ("q4", 2, 4096)):
         inp = synth.make(synth.random_case(dtype, M, N, 4000 + M))
         y_ref, den = reference(dtype, inp, M, N)
         t = upload(dtype, inp)
@@ -407,5 +408,7 @@ def test_fixed_chunk_bulk_variants_with_ragged_rows():
                 continue
             torch.cuda.synchronize()
             assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} {v['name']} {M}x{N}")
-            checked += 1
-    assert checked >= 2
+            checked.add((dtype, v["name"]))
+    every = {(d, v["name"]) for d in ("q4", "q8") for v in mbg.variants(d)
+             if v["kind"] == "bulk" and v["unroll"] > 0}
+    assert checked == every, f"not exercised: {sorted(every - checked)}"
