@@ -118,6 +118,7 @@ int64_t row_bytes_of(int dtype, int64_t N)
 int a_align(int dtype) { return dtype == DT_F32 ? 4 : (dtype == DT_F16 || dtype == DT_F16X32) ? 2 : 1; }
 int x_align(int dtype) { return (dtype == DT_F32 || dtype == DT_F16X32) ? 4 : 2; }
 int x_elem_bytes(int dtype) { return (dtype == DT_F32 || dtype == DT_F16X32) ? 4 : 2; }
+
 bool is_quant(int dtype) { return dtype == DT_Q8 || dtype == DT_Q4; }
 
 // Scale grouping: 128 columns per scale, or one scale per row.
@@ -151,8 +152,9 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N, int64_t groups)
 {
     if (v.kind == KIND_BULK) {
         const int64_t rb = row_bytes_of(dtype, N);
-        const BulkLayout L = bulk_layout(v.stages, v.rows_per_group, v.warps * 32, rb,
-                                         N * x_elem_bytes(dtype), groups, is_quant(dtype));
+        const int64_t xb = v.x_regs ? 0 : N * x_elem_bytes(dtype);
+        const BulkLayout L = bulk_layout(v.stages, v.rows_per_group, v.warps * 32, rb, xb, groups,
+                                         is_quant(dtype));
         return static_cast<size_t>(L.total);
     }
     if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)

@@ -254,6 +254,17 @@ __device__ __forceinline__ const uint4 *x_smem_vec(const unsigned char *xs, int 
 // is stored re-paired four columns apart, (x0,x4) (x1,x5) (x2,x6) (x3,x7),
 // the order in which q4_codes_h2 yields the codes, so that every product
 // takes the same half of its two operands.
+// One 16-byte vector of x re-paired four columns apart (the PAIRED layout).
+__device__ __forceinline__ uint4 pair_x_vec(const uint4 u)
+{
+    uint4 w;
+    w.x = __byte_perm(u.x, u.z, 0x5410);
+    w.y = __byte_perm(u.x, u.z, 0x7632);
+    w.z = __byte_perm(u.y, u.w, 0x5410);
+    w.w = __byte_perm(u.y, u.w, 0x7632);
+    return w;
+}
+
 struct NoOp {
     __device__ void operator()() const {}
 };
@@ -281,13 +292,7 @@ __device__ __forceinline__ void stage_x_vmajor(unsigned char *xs, const void *x,
                 const int c = i / XV;
                 const int v = i - c * XV;
                 uint4 w = r[j];
-                if constexpr (PAIRED) {
-                    const uint4 u = w;
-                    w.x = __byte_perm(u.x, u.z, 0x5410);
-                    w.y = __byte_perm(u.x, u.z, 0x7632);
-                    w.z = __byte_perm(u.y, u.w, 0x5410);
-                    w.w = __byte_perm(u.y, u.w, 0x7632);
-                }
+                if constexpr (PAIRED) w = pair_x_vec(w);
                 *reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(v) * nchunks + c) * 16) = w;
             }
         }

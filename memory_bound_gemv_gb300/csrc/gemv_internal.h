@@ -71,6 +71,7 @@ struct Variant {
     cudaError_t (*occupancy)(int *blocks, size_t smem);
     int math;            // MATH_F32 or MATH_MIXED
     int stages;          // bulk-pipeline depth (KIND_BULK)
+    bool x_regs = false; // bulk pipeline keeps x in registers, not in shared memory
     bool supports_pdl() const { return kind == KIND_TILE || kind == KIND_BULK; }
     int rows_per_block() const
     {

@@ -394,7 +394,10 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 // (each decision made warp-uniform first), and the producer first waits
 // (bounded) for the copies it still has in flight, so no copy can land in
 // shared memory after the block has exited.
-template <int DT, int T, int RS, int S, int MATH, int CF>
+// XR: with a fixed chunk count per consumer thread, consumer thread t only
+// ever reads the x of chunks t, t + T, ...; XR keeps those vectors in its
+// registers (loaded once), so x takes no shared memory and no staging barrier.
+template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
@@ -404,12 +407,14 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     static_assert(MATH == MATH_F32 || Fmt<DT>::XB == 2, "an FP32 x uses FP32 math");
     static_assert(NW <= 32, "the producer warp adds one partial per consumer warp");
     constexpr bool PAIRED = DT == DT_Q4 && MATH == MATH_MIXED;  // see stage_x_vmajor
+    constexpr bool XREG = XR;
+    static_assert(!XR || (CF > 0 && XV > 1), "x in registers: fixed chunk count, several x vectors");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunks = p.nchunks;
     const uint32_t xbytes = static_cast<uint32_t>(nchunks) * XCB;
-    const BulkLayout L = bulk_layout(S, RS, T, p.row_bytes, xbytes, p.groups, F::QUANT);
+    const BulkLayout L = bulk_layout(S, RS, T, p.row_bytes, XREG ? 0u : xbytes, p.groups, F::QUANT);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *red = full + S;
     uint64_t *xbar = red + S;
@@ -523,10 +528,27 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     // ---------------- consumer warps ----------------
     // (every exit decision is made warp-uniform before the warp's shuffles)
     if (p.pdl) pdl_wait();
+    // XREG: this thread's x vectors (chunks tid + j T), loaded with ordinary
+    // loads that go out before the barrier arrive (see stage_x_vmajor), and
+    // re-paired for INT4 once they have arrived
+    uint4 xr[XREG ? CF : 1][XV];
     if constexpr (XV == 1) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns))) {
             if (lane == 0) fail();
             return;
+        }
+    } else if constexpr (XREG) {
+        const uint4 *src = static_cast<const uint4 *>(p.x);
+#pragma unroll
+        for (int j = 0; j < CF; ++j)
+#pragma unroll
+            for (int v = 0; v < XV; ++v) xr[j][v] = ld_l2_16(src + (tid + j * T) * XV + v);
+        asm volatile("bar.arrive 2, %0;" ::"r"(T + 32) : "memory");
+        if constexpr (PAIRED) {
+#pragma unroll
+            for (int j = 0; j < CF; ++j)
+#pragma unroll
+                for (int v = 0; v < XV; ++v) xr[j][v] = pair_x_vec(xr[j][v]);
         }
     } else {
         // several vectors of x per chunk: transpose x into shared memory,
@@ -581,14 +603,11 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 #pragma unroll
                 for (int r = 0; r < RS; ++r) rsc[r] = r < rows ? ld_half_as_float(p.scales + r0 + r) : 0.f;
             }
-            // one chunk of every row of the tile: x vectors at xrow[v] + off,
-            // row r of the stage at arow[r] + off, its scale at srow[r] + soff
-            auto chunk = [&](const uint32_t (&xrow)[XV], const uint32_t (&arow)[RS],
-                             const uint32_t (&srow)[RS], uint32_t off, uint32_t soff) {
-                uint4 xv[XV];
-#pragma unroll
-                for (int v = 0; v < XV; ++v) xv[v] = lds128(xrow[v] + off);
-                float xf[MATH == MATH_F32 ? F::EPC : 1];
+            // one chunk of every row of the tile: x vectors xv, row r of the
+            // stage at arow[r] + off, its scale at srow[r] + soff
+            auto chunk_x = [&](const uint4 (&xv)[XV], const uint32_t (&arow)[RS],
+                               const uint32_t (&srow)[RS], uint32_t off, uint32_t soff) {
+                [[maybe_unused]] float xf[MATH == MATH_F32 ? F::EPC : 1];
                 if constexpr (MATH == MATH_F32) x_to_float<DT>(xv, xf);
 #pragma unroll
                 for (int r = 0; r < RS; ++r) {
@@ -609,6 +628,14 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
                     }
                 }
             };
+            // the same with the x vectors at xrow[v] + off in shared memory
+            auto chunk = [&](const uint32_t (&xrow)[XV], const uint32_t (&arow)[RS],
+                             const uint32_t (&srow)[RS], uint32_t off, uint32_t soff) {
+                uint4 xv[XV];
+#pragma unroll
+                for (int v = 0; v < XV; ++v) xv[v] = lds128(xrow[v] + off);
+                chunk_x(xv, arow, srow, off, soff);
+            };
             uint32_t arow[RS], srow[RS];
 #pragma unroll
             for (int r = 0; r < RS; ++r) {
@@ -621,7 +648,10 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
 #pragma unroll
                 for (int r = 0; r < RS; ++r) arow[r] += t16;
 #pragma unroll
-                for (int j = 0; j < CF; ++j) chunk(xthr, arow, srow, j * T * 16u, sgrp[j]);
+                for (int j = 0; j < CF; ++j) {
+                    if constexpr (XREG) chunk_x(xr[j], arow, srow, j * T * 16u, sgrp[j]);
+                    else chunk(xthr, arow, srow, j * T * 16u, sgrp[j]);
+                }
             } else {
 #pragma unroll 2
                 for (int c = tid; c < nchunks; c += T)
@@ -780,36 +810,39 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
 #define MBG_TILE(DT, G, CPT, T, XM, NAME) \
     MBG_TILE_M(DT, G, CPT, T, XM, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
 
-template <int DT, int T, int RS, int S, int MATH, int CF>
+template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH, CF>, a, grid, T + 32, smem, s, pdl);
+    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>, a, grid, T + 32, smem, s, pdl);
 }
 
-template <int DT, int T, int RS, int S, int MATH, int CF>
+template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 cudaError_t smem_limit_bulk(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH, CF>,
+    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DT, int T, int RS, int S, int MATH, int CF>
+template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 cudaError_t occupancy_bulk(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH, CF>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>,
                                                          T + 32, smem);
 }
 
-// unroll = CF: chunks per consumer thread and row when fixed (0: any row length)
-#define MBG_BULK_MF(DT, T, RS, S, MATH, CF, NAME)                                                 \
-    Variant{DT, T, RS, CF, T / 32, XMODE_BULK, NAME, &launch_bulk<DT, T, RS, S, MATH, CF>,         \
-            &smem_limit_bulk<DT, T, RS, S, MATH, CF>, KIND_BULK, 0,                                 \
-            &occupancy_bulk<DT, T, RS, S, MATH, CF>, MATH, S}
+// unroll = CF: chunks per consumer thread and row when fixed (0: any row
+// length); XR: x in registers (MBG_BULK_FX)
+#define MBG_BULK_MFX(DT, T, RS, S, MATH, CF, XR, NAME)                                             \
+    Variant{DT, T, RS, CF, T / 32, XMODE_BULK, NAME, &launch_bulk<DT, T, RS, S, MATH, CF, XR>,     \
+            &smem_limit_bulk<DT, T, RS, S, MATH, CF, XR>, KIND_BULK, 0,                             \
+            &occupancy_bulk<DT, T, RS, S, MATH, CF, XR>, MATH, S, XR}
+#define MBG_BULK_MF(DT, T, RS, S, MATH, CF, NAME) MBG_BULK_MFX(DT, T, RS, S, MATH, CF, false, NAME)
 #define MBG_BULK_M(DT, T, RS, S, MATH, NAME) MBG_BULK_MF(DT, T, RS, S, MATH, 0, NAME)
 #define MBG_BULK(DT, T, RS, S, NAME) \
     MBG_BULK_M(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), NAME)
 #define MBG_BULK_F(DT, T, RS, S, CF, NAME) \
     MBG_BULK_MF(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), CF, NAME)
+#define MBG_BULK_FX(DT, T, RS, S, CF, NAME) MBG_BULK_MFX(DT, T, RS, S, MATH_MIXED, CF, true, NAME)
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -12,6 +12,8 @@ static const Variant kTableQ8[] = {
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
     // given row length the first that fits is the automatic choice
     MBG_BULK_F(DT_Q8, 128, 4, 3, 2, "bulk_t128_r4_s3_f2"),
+    // x in registers (_xr): measured +5 % at 14336 columns, slower for 4096
+    MBG_BULK_FX(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4_xr"),
     MBG_BULK_F(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4"),
     MBG_BULK_F(DT_Q8, 128, 4, 2, 2, "bulk_t128_r4_s2_f2"),
     MBG_BULK(DT_Q8, 256, 1, 4, "bulk_t256_r1_s4"),
