@@ -63,6 +63,15 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Asks L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16 bytes).
+// A prefetch is only a hint: it changes no value that a later load returns,
+// so it may be issued before the wait for a preceding kernel that could
+// still write the range (L2 is where that kernel's writes land).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel on
 // the stream (if it was launched with programmatic serialisation) start its
 // blocks while this grid still runs; wait blocks until the preceding grid has

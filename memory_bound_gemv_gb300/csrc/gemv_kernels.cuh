@@ -226,7 +226,18 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     // scheduling overlaps the preceding kernel's drain.
     pdl_trigger();
     const bool pdl = p.pdl != 0;
-    if (!pdl) pdl_wait();
+    if (!pdl) {
+        // this block's first two tiles into L2 while the preceding kernel
+        // drains (a hint only: the loads of the tiles come after the wait;
+        // measured: one tile +3-12 %, the second +6 % more at 4096x14336)
+        for (int k = 0; k < 2; ++k) {
+            const int64_t row0 = (static_cast<int64_t>(blockIdx.x) + k * static_cast<int64_t>(gridDim.x)) * RT + grp;
+            if (tg == 0 && row0 < p.M)
+                prefetch_l2(static_cast<const unsigned char *>(p.A) + row0 * p.row_bytes,
+                            static_cast<uint32_t>(p.row_bytes));
+        }
+        pdl_wait();
+    }
     auto stage_x_bulk = [&]() {
         if (tid == 0) {
             const uint32_t b = smem_addr(bar);
@@ -447,7 +458,19 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     };
 
     pdl_trigger();
-    if (!p.pdl) pdl_wait();  // see the row-tile kernel
+    if (!p.pdl) {
+        // the first tile into L2 while the preceding kernel drains (a hint
+        // only; see the row-tile kernel).  Only the first: the x loads that
+        // follow the wait would queue behind a larger burst (measured: S
+        // tiles cost INT8 at 14336 columns 9 %, one tile gains 4-9 %)
+        if (tid == 0 && iters > 0) {
+            const int64_t r0 = static_cast<int64_t>(blockIdx.x) * RS;
+            const int64_t rows = min(static_cast<int64_t>(RS), p.M - r0);
+            prefetch_l2(static_cast<const unsigned char *>(p.A) + r0 * p.row_bytes,
+                        static_cast<uint32_t>(rows * p.row_bytes));
+        }
+        pdl_wait();
+    }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
