@@ -10,7 +10,10 @@
 //   stride:  blocks walk tiles of THREADS*U vectors in grid-stride order;
 //   tile:    the row-tile GEMV's pattern: a persistent grid walks tiles of
 //            THREADS*U vectors in grid-stride order and requests the next tile
-//            before folding the current one.
+//            before folding the current one;
+//   bulk:    bulk async copies (cp.async.bulk) of large chunks into
+//            shared-memory rings -- the bulk pipeline's way of reading weights
+//            (measured a little above the load-based patterns).
 // Every loaded word is XOR-folded; each warp XORs its fold into *sink, so no
 // load can be dropped as dead code.
 #include "gemv_device.cuh"
@@ -100,6 +103,80 @@ __global__ void __launch_bounds__(THREADS) probe_tile_kernel(const uint4 *buf, s
     if ((threadIdx.x & 31) == 0 && fold) atomicXor(sink, static_cast<unsigned long long>(fold));
 }
 
+// Bulk-copy read probe: one warp per block streams chunks of B bytes (grid-
+// stride order) through an S-deep ring of shared-memory stages with
+// cp.async.bulk, waits on each stage's mbarrier (bounded), and XOR-folds the
+// chunk before the stage is refilled.  On a timeout it waits (bounded) for the
+// copies still in flight and sets bit 63 of *sink.
+template <int B, int S>
+__global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t n16,
+                                                        unsigned long long *sink)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *ring = smem + 128;
+    const int lane = threadIdx.x & 31;
+    const size_t nbytes = n16 * 16;
+    const size_t nchunks = (nbytes + B - 1) / B;
+    const size_t grid = gridDim.x;
+    const size_t iters = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / grid + 1 : 0;
+    constexpr uint64_t kLimitNs = 1000000000ull;
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(&bar[s]), 1);
+    __syncwarp();
+    auto chunk_bytes = [&](size_t k) {
+        const size_t off = (blockIdx.x + k * grid) * static_cast<size_t>(B);
+        return static_cast<uint32_t>(nbytes - off < static_cast<size_t>(B) ? nbytes - off : B);
+    };
+    auto issue = [&](size_t k) {
+        if (lane == 0) {
+            const uint32_t b = smem_addr(&bar[k % S]);
+            const uint32_t n = chunk_bytes(k);
+            mbar_arrive_expect_tx(b, n);
+            bulk_copy_g2s(smem_addr(ring + (k % S) * B),
+                          reinterpret_cast<const unsigned char *>(buf) + (blockIdx.x + k * grid) * static_cast<size_t>(B),
+                          n, b);
+        }
+    };
+    size_t issued = 0;
+    for (; issued < S && issued < iters; ++issued) issue(issued);
+    uint32_t fold = 0;
+    bool ok = true;
+    size_t k = 0;
+    for (; k < iters; ++k) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(smem_addr(&bar[k % S]), static_cast<uint32_t>((k / S) & 1), kLimitNs));
+        if (!ok) break;
+        const uint4 *r = reinterpret_cast<const uint4 *>(ring + (k % S) * B);
+        const uint32_t n = chunk_bytes(k) / 16;
+        for (uint32_t i = lane; i < n; i += 32) {
+            const uint4 v = r[i];
+            fold ^= v.x ^ v.y ^ v.z ^ v.w;
+        }
+        __syncwarp();  // every lane has read the stage before it is refilled
+        if (issued < iters) issue(issued++);
+    }
+    if (!ok) {
+        if (lane == 0)
+            for (size_t j = k; j < issued; ++j)
+                mbar_wait_bounded(smem_addr(&bar[j % S]), static_cast<uint32_t>((j / S) & 1), kLimitNs);
+        if (lane == 0) atomicOr(sink, 1ull << 63);
+        return;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) fold ^= __shfl_xor_sync(0xffffffffu, fold, off);
+    if (lane == 0 && fold) atomicXor(sink, static_cast<unsigned long long>(fold));
+}
+
+template <int B, int S>
+void launch_probe_bulk(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
+                       cudaStream_t s)
+{
+    const int smem = 128 + S * B;
+    cudaFuncSetAttribute(probe_bulk_kernel<B, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    probe_bulk_kernel<B, S><<<grid, 32, smem, s>>>(static_cast<const uint4 *>(buf), n16, sink);
+}
+
 template <int THREADS, int U>
 void launch_probe_tile(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
                        cudaStream_t s)
@@ -115,6 +192,8 @@ void launch_probe(const void *buf, size_t n16, unsigned long long *sink, unsigne
         <<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
 }
 
+// pattern field: 0 grid-stride tiles, 1 one segment per warp, 2 tiles with
+// the next requested early, 3 bulk copies (threads 32, unroll = stages)
 static const ProbeVariant kProbes[] = {
     {"segment_t128_u8_b8", 128, 8, 8, 1, &launch_probe<128, 8, 1>},
     {"segment_t256_u8_b4", 256, 8, 4, 1, &launch_probe<256, 8, 1>},
@@ -126,6 +205,9 @@ static const ProbeVariant kProbes[] = {
     {"tile_t512_u4_b2", 512, 4, 2, 2, &launch_probe_tile<512, 4>},
     {"tile_t256_u8_b4", 256, 8, 4, 2, &launch_probe_tile<256, 8>},
     {"tile_t512_u8_b1", 512, 8, 1, 2, &launch_probe_tile<512, 8>},
+    {"bulk_b32k_s2_x2", 32, 2, 2, 3, &launch_probe_bulk<32768, 2>},
+    {"bulk_b32k_s4_x1", 32, 4, 1, 3, &launch_probe_bulk<32768, 4>},
+    {"bulk_b16k_s4_x2", 32, 4, 2, 3, &launch_probe_bulk<16384, 4>},
 };
 
 const ProbeVariant *probe_variants(int *count)
