@@ -211,11 +211,13 @@ gemv_status_t gemv_ex_host_noalloc(int dtype, const void *A, const void *x_host,
                                    void *stream);
 
 /*
- * Pure-read bandwidth probe: streams buf[0..bytes) once with the same
- * 16-byte read-only loads the GEMV kernels use and folds every word into
- * *sink with XOR (so no load is dead code).  bytes must be a multiple of 16
- * and buf 16-byte aligned.  `variant` selects the read pattern
- * (0 .. gemv_probe_variant_count()-1).  Achieved bytes / time is the
+ * Pure-read bandwidth probe: streams buf[0..bytes) once, either with the
+ * same 16-byte read-only loads the GEMV kernels use or (the "bulk_" patterns)
+ * with bulk asynchronous copies into shared-memory rings, and folds every
+ * word into the low 32 bits of *sink with XOR (so no read is dead code).
+ * bytes must be a multiple of 16 and buf 16-byte aligned.  `variant` selects
+ * the read pattern (0 .. gemv_probe_variant_count()-1).  A bulk pattern whose
+ * bounded wait gives up sets bit 63 of *sink.  Achieved bytes / time is the
  * measured read ceiling that memory-bandwidth utilisation is quoted against.
  * "membound", section "Why GEMV, and why MBU" (pure-read probe as the
  * denominator for a read-dominated kernel).
