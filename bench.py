@@ -406,6 +406,9 @@ def run_ours(args):
                 e1.record(stream)
                 e1.synchronize()
                 res[name] = gbs(reps * probe_bytes, e0.elapsed_time(e1) * 1e-3)
+        # bit 63 of the sink: a bulk-copy probe gave up waiting (its time means nothing)
+        if (int(sink.item()) >> 63) & 1:
+            raise SystemExit("a bulk-copy probe timed out; no MBU denominator")
         return res
 
     probe_before = run_probes()
