@@ -9,10 +9,23 @@ pure-read ceiling measured in the same run ("membound", sections "Results" and
 One step = one GEMV launch over the whole workload: choose the kernel, stage
 x, stream A, accumulate, reduce, write y.  Weights rotate through enough
 copies (at least max(256 MiB, 4 x L2)) that every launch reads A cold from
-HBM ("membound", gotcha 1); x stays resident.  Steps are replayed from CUDA
-graphs of back-to-back launches and timed with CUDA events on the launching
-stream.  Algorithmic bytes per step = A + scales + x read once, y written
-once ("Making GEMV Fast", section "Memory Access").
+HBM ("membound", gotcha 1); x stays resident.  The K timed steps are one CUDA
+graph of exactly K back-to-back launches (or replays of a graph of B launches
+plus one graph of the remainder), each graph replayed during warm-up; before
+the timed region L2 is flushed and a short spin kernel is queued so that the
+host's submission of the graph is not inside the timed region.  Time comes
+from CUDA events on the launching stream.  Algorithmic bytes per step = A +
+scales + x read once, y written once ("Making GEMV Fast", section "Memory
+Access").
+
+Besides the headline the line carries, unless --no-configs: every workload of
+the five families (FP32 1024^2, FP16 4096^2, the FP16 decode shapes, the
+square sweep in FP32 and FP16, INT8/INT4 at both decode shapes) with its
+automatic kernel, time per launch in a chain of plain launches and in an
+overlapped chain, GB/s, MBU against the probe and the 8 TB/s spec, and the
+parity error over every row against the CPU oracle; plus FP16, INT8 and INT4
+at each decode shape timed in interleaved rounds (best round per kernel) with
+their speed-up over FP16 ("membound", "dequant GEMV").
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (the reference arm: there is no runnable upstream
@@ -22,6 +35,7 @@ code).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -44,6 +58,20 @@ SPEC_HBM_GBS = 8000.0           # HBM3e nominal
 FALLBACK_HBM_GBS = 6800.0       # used only if MEASURED_PEAKS.json is absent
 PUBLISHED = {"f16_down_4096x14336": (417.0, "membound page, RTX 4080 Laptop (Ada sm_89): context only")}
 ROTATE_MIN_BYTES = 256 << 20
+GATE_CYCLES = 400_000           # spin kernel ahead of a timed region (~0.2 ms)
+GRAPH_MAX = 1000                # launches per captured graph
+
+KERNEL_NAMES = {"vec": "mbg_warprow_kernel", "tile": "mbg_rowtile_kernel", "bulk": "mbg_bulkpipe_kernel",
+                "band": "mbg_rowband_kernel", "elem": "mbg_elem_kernel"}
+
+# the five workload families, in the order they are reported
+CONFIG_WORKLOADS = ["f32_1024", "f16_4096", "f16_up_14336x4096", "f16_down_4096x14336",
+                    "sweep_f32_2048", "sweep_f32_4096", "sweep_f32_8192", "sweep_f32_16384",
+                    "sweep_f16_2048", "sweep_f16_4096", "sweep_f16_8192", "sweep_f16_16384",
+                    "q8_4096x14336", "q8_14336x4096", "q4_4096x14336", "q4_14336x4096"]
+# FP16 / INT8 / INT4 at one shape, timed in interleaved rounds
+INTERLEAVED = {"4096x14336": ("f16_down_4096x14336", "q8_4096x14336", "q4_4096x14336"),
+               "14336x4096": ("f16_up_14336x4096", "q8_14336x4096", "q4_14336x4096")}
 
 
 # ---------------------------------------------------------------------------
@@ -91,6 +119,23 @@ def split_steps(steps: int, batch: int):
     """(full graph replays, tail launches) for exactly `steps` launches."""
     batch = max(1, batch)
     return steps // batch, steps % batch
+
+
+def graph_plan(steps: int, copies: int, graph_max: int = GRAPH_MAX):
+    """Graphs that make up exactly `steps` launches: [(launches, replays), ...].
+
+    Up to graph_max steps: one graph of exactly `steps` launches, replayed
+    once.  Beyond: a graph of B launches (a multiple of the rotation count, so
+    replays continue the rotation) replayed steps // B times, plus one graph of
+    the remainder."""
+    if steps <= graph_max:
+        return [(steps, 1)]
+    batch = max(copies, graph_max // copies * copies)
+    full, tail = split_steps(steps, batch)
+    plan = [(batch, full)]
+    if tail:
+        plan.append((tail, 1))
+    return plan
 
 
 def kernel_source_hash() -> str:
@@ -177,12 +222,20 @@ def parse_clock_line(line: str):
     return {"sm": sm, "sm_max": smax, "reasons": reasons}
 
 
+def summarise_clocks(samples, t0, t1):
+    inside = [s for s in samples if t0 is not None and t1 is not None and t0 <= s["t"] <= t1]
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+            "sm_max_mhz": max(s["sm_max"] for s in inside),
+            "reasons": sorted({r for s in inside for r in s["reasons"]}), "samples": len(inside)}
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms; keeps the samples inside [mark_start, mark_end]."""
+    """nvidia-smi sampled every 50 ms; windows are host-time intervals."""
 
     def __init__(self, gpu_id: str):
         self.samples = []
-        self.window = [None, None]
         self.proc = None
         self.error = None
         try:
@@ -202,12 +255,6 @@ class ClockSampler:
                 s["t"] = time.monotonic()
                 self.samples.append(s)
 
-    def mark_start(self):
-        self.window[0] = time.monotonic()
-
-    def mark_end(self):
-        self.window[1] = time.monotonic()
-
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -216,19 +263,11 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def window(self, t0, t1):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": f"nvidia-smi unavailable: {self.error}"}
-        t0, t1 = self.window
-        inside = [s for s in self.samples if t0 is not None and t1 is not None and t0 <= s["t"] <= t1]
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "timed region shorter than the sampling interval"}
-        reasons = sorted({r for s in inside for r in s["reasons"]})
-        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
-                "sm_max_mhz": max(s["sm_max"] for s in inside), "reasons": reasons,
-                "samples": len(inside)}
+        return summarise_clocks(self.samples, t0, t1)
 
 
 def gpu_id_for(dev: int) -> str:
@@ -332,11 +371,146 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# GPU helpers
+# ---------------------------------------------------------------------------
+
+class Resident:
+    """One workload in device memory: weight copies for the rotation, x, y."""
+
+    def __init__(self, w, dev, l2, inp=None):
+        import numpy as np
+        import torch
+        self.w = w
+        self.inp = inp if inp is not None else synth.make(w)
+
+        def to_dev(arr, f16bits):
+            a = np.ascontiguousarray(arr)
+            return torch.from_numpy(a.view(np.float16) if f16bits else a).to(dev)
+
+        A0 = to_dev(self.inp["A"], f16_weights(w.dtype))
+        self.x = to_dev(self.inp["x"], not f32_x(w.dtype))
+        S0 = to_dev(self.inp["scales"], True) if w.quantised else None
+        if w.dtype == "q8row":
+            S0 = S0.reshape(-1)  # one scale per row: [M]
+        self.wbytes = a_bytes(w.dtype, w.M, w.N) + scale_bytes(w.dtype, w.M, w.N)
+        self.copies = rotation_copies(self.wbytes, l2)
+        self.As = [A0] + [A0.clone() for _ in range(self.copies - 1)]
+        self.Ss = [S0] + [S0.clone() for _ in range(self.copies - 1)] if w.quantised else [None] * self.copies
+        self.y = torch.empty(w.M, dtype=torch.float32, device=dev)
+        self.step_bytes = algorithmic_bytes(w.dtype, w.M, w.N)
+
+    def launch(self, i, overlap=False):
+        import memory_bound_gemv_gb300 as mbg
+        k = i % self.copies
+        mbg.gemv(self.w.dtype, self.As[k], self.x, self.Ss[k], y=self.y, overlap=overlap)
+
+    def free(self):
+        self.As = self.Ss = self.x = self.y = None
+
+
+class Timer:
+    """Graphs of back-to-back launches timed with CUDA events on one stream."""
+
+    def __init__(self, dev, stream, l2):
+        import torch
+        self.dev = dev
+        self.stream = stream
+        # written before each timed region: evicts whatever the warm-up left in L2
+        self.flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+
+    def capture(self, launch, plan, overlap=False):
+        import torch
+        graphs = []
+        with torch.cuda.stream(self.stream):
+            for n, _ in plan:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(n):
+                        launch(i, overlap)
+                graphs.append(g)
+        self.stream.synchronize()
+        return graphs
+
+    def replay(self, graphs, plan):
+        for g, (_, reps) in zip(graphs, plan):
+            for _ in range(reps):
+                g.replay()
+
+    def warm(self, graphs, plan, launches):
+        """Replays every graph at least once and at least `launches` launches in all."""
+        import torch
+        done = 0
+        with torch.cuda.stream(self.stream):
+            while True:
+                for g, (n, _) in zip(graphs, plan):
+                    g.replay()
+                    done += n
+                if done >= launches:
+                    break
+        self.stream.synchronize()
+
+    def timed(self, graphs, plan):
+        """Seconds for one pass of the plan: L2 flushed, a spin kernel queued
+        first so the host's submissions are not timed."""
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.flush_buf.fill_(1)
+            torch.cuda._sleep(GATE_CYCLES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            self.replay(graphs, plan)
+            e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3
+
+    def hold(self, graphs, plan, seconds):
+        """Replays the plan back to back for about `seconds` (clock sampling)."""
+        import torch
+        t_end = time.monotonic() + seconds
+        with torch.cuda.stream(self.stream):
+            while time.monotonic() < t_end:
+                self.replay(graphs, plan)
+                self.stream.synchronize()
+
+
+def probe_ceiling(mbg, stream, probe_buf, sink, reps):
+    import torch
+    probe_bytes = probe_buf.numel() * probe_buf.element_size()
+    res = {}
+    with torch.cuda.stream(stream):
+        for v, name in enumerate(mbg.probe_variants()):
+            for _ in range(2):
+                mbg.gemv_probe_read(probe_buf, sink, v)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                mbg.gemv_probe_read(probe_buf, sink, v)
+            e1.record(stream)
+            e1.synchronize()
+            res[name] = gbs(reps * probe_bytes, e0.elapsed_time(e1) * 1e-3)
+    # bit 63 of the sink: a bulk-copy probe gave up waiting (its time means nothing)
+    if (int(sink.item()) >> 63) & 1:
+        raise SystemExit("a bulk-copy probe timed out; no MBU denominator")
+    return res
+
+
+def parity_all_rows(w, inp, y_gpu):
+    """Max normalised error of y_gpu against the oracle over every row."""
+    import oracle
+    orc = oracle.load()
+    y_ref, den = orc.gemv(w.dtype, inp["A"], inp["x"], w.M, w.N, scales=inp.get("scales"),
+                          threads=cpu_threads())
+    return oracle.max_normalised_error(y_gpu, y_ref, den)
+
+
+TOL = {"f32": 1e-5, "f16": 2e-3, "q8": 2e-3, "q4": 2e-3, "f16x32": 1e-5, "q8row": 2e-3}
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
 def run_ours(args):
-    import numpy as np
     import torch
 
     import memory_bound_gemv_gb300 as mbg
@@ -353,37 +527,19 @@ def run_ours(args):
     w = synth.WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 << 20))
-    inp = synth.make(w)
-
-    def to_dev(arr, kind):
-        if kind == "f16bits":
-            return torch.from_numpy(np.ascontiguousarray(arr).view(np.float16)).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
-
-    A0 = to_dev(inp["A"], "f16bits" if f16_weights(w.dtype) else "raw")
-    x = to_dev(inp["x"], "raw" if f32_x(w.dtype) else "f16bits")
-    S0 = to_dev(inp["scales"], "f16bits") if w.quantised else None
-    if w.dtype == "q8row":
-        S0 = S0.reshape(-1)  # one scale per row: [M]
-    wbytes = a_bytes(w.dtype, w.M, w.N) + scale_bytes(w.dtype, w.M, w.N)
-    copies = rotation_copies(wbytes, l2)
-    As = [A0] + [A0.clone() for _ in range(copies - 1)]
-    Ss = [S0] + [S0.clone() for _ in range(copies - 1)] if w.quantised else [None] * copies
-    y = torch.empty(w.M, dtype=torch.float32, device=dev)
-    step_bytes = algorithmic_bytes(w.dtype, w.M, w.N)
     stream = torch.cuda.Stream(dev)
+    timer = Timer(dev, stream, l2)
+    R = Resident(w, dev, l2)
+    step_bytes = R.step_bytes
 
-    vid = mbg.select_variant(w.dtype, A0, x)
+    vid = mbg.select_variant(w.dtype, R.As[0], R.x)
     vinfo = mbg.variants(w.dtype)[vid]
 
-    def launch(i, overlap=False):
-        mbg.gemv(w.dtype, As[i % copies], x, Ss[i % copies], y=y, overlap=overlap)
-
-    # first launch: keep the result for the parity sample of the cpu_baseline leg
+    # first launch: kept for the parity check (every row against the oracle)
     with torch.cuda.stream(stream):
-        launch(0)
+        R.launch(0)
     stream.synchronize()
-    y_first = y.cpu().numpy().copy()
+    y_first = R.y.cpu().numpy().copy()
     if mbg.gemv_get_device_error(stream) != mbg.OK:
         raise SystemExit("device status word set on the first launch")
 
@@ -391,208 +547,132 @@ def run_ours(args):
     probe_bytes = int(args.probe_gib * (1 << 30)) // 16 * 16
     probe_buf = torch.randint(-2 ** 31, 2 ** 31 - 1, (probe_bytes // 4,), dtype=torch.int32, device=dev)
     sink = torch.zeros(1, dtype=torch.int64, device=dev)
-    probe_names = mbg.probe_variants()
+    probe_before = probe_ceiling(mbg, stream, probe_buf, sink, args.probe_reps)
 
-    def run_probes(reps=args.probe_reps):
-        res = {}
-        with torch.cuda.stream(stream):
-            for v, name in enumerate(probe_names):
-                for _ in range(2):
-                    mbg.gemv_probe_read(probe_buf, sink, v)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(reps):
-                    mbg.gemv_probe_read(probe_buf, sink, v)
-                e1.record(stream)
-                e1.synchronize()
-                res[name] = gbs(reps * probe_bytes, e0.elapsed_time(e1) * 1e-3)
-        # bit 63 of the sink: a bulk-copy probe gave up waiting (its time means nothing)
-        if (int(sink.item()) >> 63) & 1:
-            raise SystemExit("a bulk-copy probe timed out; no MBU denominator")
-        return res
-
-    probe_before = run_probes()
-
-    # ---- graphs of back-to-back launches ----
-    batch = copies * max(1, math.ceil(args.graph_batch / copies))
-    n_full, n_tail = split_steps(args.steps, batch)
-    stream.wait_stream(torch.cuda.current_stream(dev))
+    # ---- the timed region: exactly K launches from warmed graphs ----
     with torch.cuda.stream(stream):
-        for i in range(3):
-            launch(i)
+        for i in range(min(3, R.copies)):
+            R.launch(i)
     stream.synchronize()
-    g_main = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_main, stream=stream):
-        for i in range(batch):
-            launch(i)
-    g_tail = None
-    if n_tail:
-        g_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_tail, stream=stream):
-            for i in range(n_tail):
-                launch(i)
-
-    # warm-up: W launches
-    w_full, w_tail = split_steps(args.warmup, batch)
-    with torch.cuda.stream(stream):
-        for _ in range(w_full):
-            g_main.replay()
-        for i in range(w_tail):
-            launch(i)
-    stream.synchronize()
+    plan = graph_plan(args.steps, R.copies, args.graph_max)
+    graphs = timer.capture(R.launch, plan)
+    timer.warm(graphs, plan, args.warmup)
 
     sampler = ClockSampler(gpu_id_for(local_rank)) if not args.no_clocks else None
     if sampler is not None:
         time.sleep(0.3)  # let nvidia-smi start
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
-    if sampler is not None:
-        sampler.mark_start()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(n_full):
-            g_main.replay()
-        if g_tail is not None:
-            g_tail.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if sampler is not None:
-        sampler.mark_end()
+    t_host0 = time.monotonic()
+    elapsed = timer.timed(graphs, plan)
+    t_host1 = time.monotonic()
     barrier()
-    elapsed = e0.elapsed_time(e1) * 1e-3
+    # the same graphs replayed for a while right after, so that the clocks
+    # under this load are sampled (a timed region of a few launches is far
+    # shorter than the sampling interval)
+    clock_t0 = time.monotonic()
     if sampler is not None:
-        sampler.stop()
+        timer.hold(graphs, plan, args.clock_seconds)
+    clock_t1 = time.monotonic()
     t_max = max_over_ranks(elapsed, dev)
     per_launch = elapsed / max(1, args.steps)
     value = gbs(world * args.steps * step_bytes, t_max)
+    del graphs
 
     # ---- the same chain launched with programmatic dependent launch ----
     # (gemv_ex with GEMV_FLAG_OVERLAP_PRECEDING: each launch may start while
     # the previous one finishes; weights are never written by the chain)
     overlap = None
-    if not args.no_overlap and n_full > 0:
-        g_ov = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            for i in range(copies):
-                launch(i, overlap=True)
-        stream.synchronize()
-        with torch.cuda.graph(g_ov, stream=stream):
-            for i in range(batch):
-                launch(i, overlap=True)
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, w_full)):
-                g_ov.replay()
-        stream.synchronize()
+    if not args.no_overlap:
+        g_ov = timer.capture(R.launch, plan, overlap=True)
+        timer.warm(g_ov, plan, args.warmup)
         barrier()
-        with torch.cuda.stream(stream):
-            o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            o0.record(stream)
-            for _ in range(n_full):
-                g_ov.replay()
-            o1.record(stream)
-        o1.synchronize()
+        ov_t = max_over_ranks(timer.timed(g_ov, plan), dev)
         barrier()
-        ov_t = max_over_ranks(o0.elapsed_time(o1) * 1e-3, dev)
-        ov_steps = n_full * batch
-        overlap = {"value": gbs(world * ov_steps * step_bytes, ov_t), "unit": "GB/s", "steps": ov_steps,
-                   "ms_per_step": ov_t / ov_steps * 1e3,
-                   "how": "same graph of back-to-back launches, each launched with programmatic "
-                          "dependent launch (weights requested before waiting for the previous launch)"}
+        overlap = {"value": gbs(world * args.steps * step_bytes, ov_t), "unit": "GB/s", "steps": args.steps,
+                   "ms_per_step": ov_t / args.steps * 1e3,
+                   "how": "the same launches in the same graphs, each launched with programmatic dependent "
+                          "launch (weights requested before waiting for the previous launch)"}
         del g_ov
+
+    # ---- a long chain for comparison with the short timed region ----
+    long_chain = None
+    if not args.no_long_chain:
+        lplan = graph_plan(args.long_steps, R.copies, args.graph_max)
+        lg = timer.capture(R.launch, lplan)
+        timer.warm(lg, lplan, 1)
+        lt = timer.timed(lg, lplan)
+        long_chain = {"steps": args.long_steps, "us_per_launch": lt / args.long_steps * 1e6,
+                      "value": gbs(args.long_steps * step_bytes, lt), "unit": "GB/s"}
+        del lg
 
     # ---- the same launches without graphs (host-launched stream), for context ----
     eager_steps = min(args.steps, 2000)
     with torch.cuda.stream(stream):
-        for i in range(copies):
-            launch(i)
+        for i in range(R.copies):
+            R.launch(i)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for i in range(eager_steps):
-            launch(i)
+            R.launch(i)
         f1.record(stream)
     f1.synchronize()
     eager_gbs = gbs(eager_steps * step_bytes, f0.elapsed_time(f1) * 1e-3)
 
-    probe_after = run_probes()
+    probe_after = probe_ceiling(mbg, stream, probe_buf, sink, args.probe_reps)
     probe_all = {k: max(probe_before[k], probe_after[k]) for k in probe_before}
     best_probe = max(probe_all, key=probe_all.get)
     ceiling = probe_all[best_probe]
     if overlap is not None:
         overlap["mbu_probe_pct"] = 100.0 * overlap["value"] / world / ceiling
+    if long_chain is not None:
+        long_chain["mbu_probe_pct"] = 100.0 * long_chain["value"] / ceiling
 
-    # ---- end to end: x from pinned host memory, y back to pinned host memory ----
+    # ---- end to end through the C ABI: x from pinned host memory, y back ----
     e2e = None
     if not args.no_e2e:
-        x_host = x.cpu().pin_memory()
-        y_host = torch.empty(w.M, dtype=torch.float32).pin_memory()
-        x_dev = torch.empty_like(x)
-        e2e_steps = min(args.steps, args.e2e_steps)
+        e2e = measure_e2e(args, mbg, R, stream, world, dev)
 
-        def e2e_run(overlap_flag):
-            # one public call per step: x_host -> device, the GEMV, y written to y_host
-            def e2e_step(i):
-                if w.dtype == "q8row":
-                    x_dev.copy_(x_host, non_blocking=True)
-                    mbg.gemv(w.dtype, As[i % copies], x_dev, Ss[i % copies], y=y_dev_rowscale)
-                    y_host.copy_(y_dev_rowscale, non_blocking=True)
-                else:
-                    mbg.gemv_host(w.dtype, As[i % copies], x_host, x_dev, Ss[i % copies], y_host=y_host,
-                                  overlap=overlap_flag)
-
-            with torch.cuda.stream(stream):
-                for i in range(min(args.warmup, 50)):
-                    e2e_step(i)
-                stream.synchronize()
-                barrier()
-                h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                h0.record(stream)
-                for i in range(e2e_steps):
-                    e2e_step(i)
-                h1.record(stream)
-            h1.synchronize()
-            barrier()
-            return max_over_ranks(h0.elapsed_time(h1) * 1e-3, dev)
-
-        y_dev_rowscale = torch.empty_like(y)
-        e2e_t = e2e_run(False)
-        e2e_ov = e2e_run(True) if w.dtype != "q8row" else None
-        e2e = {"value": gbs(world * e2e_steps * step_bytes, e2e_t), "unit": "GB/s",
-               "h2d_bytes_per_step": int(x.numel() * x.element_size()),
-               "d2h_bytes_per_step": int(y.numel() * y.element_size()),
-               "steps": e2e_steps,
-               "how": "per step one gemv_ex_host call through the C ABI: x read from pinned host memory "
-                      "by a copy kernel into a device buffer, the GEMV launched after it with programmatic "
-                      "dependent launch, y written by the GEMV into pinned host memory; weights resident "
-                      "and rotated" if w.dtype != "q8row" else
-                      "per step: pinned x -> device, gemv through the C ABI, y -> pinned host",
-               "overlap_value": gbs(world * e2e_steps * step_bytes, e2e_ov) if e2e_ov else None,
-               "overlap_how": "the same calls with GEMV_FLAG_OVERLAP_PRECEDING (each copy of x may "
-                              "start before the previous GEMV ends)"}
+    # ---- every workload of the five families ----
+    configs = None
+    if not args.no_configs and world == 1:
+        R.free()
+        del probe_buf
+        torch.cuda.empty_cache()
+        configs = measure_configs(args, mbg, dev, l2, stream, timer, ceiling)
 
     peak, peak_kind = measured_peak()
     achieved = gbs(step_bytes, per_launch)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": recorded_traffic(w.name, vinfo["name"]),
-                "kernel": f"gemv_{vinfo['kind']}_kernel {vinfo['name']}"}
-    clocks = sampler.summary() if sampler is not None else {"sm_mhz": None, "note": "disabled"}
+                "kernel": f"{KERNEL_NAMES[vinfo['kind']]} {vinfo['name']}"}
+    clocks = {"sm_mhz": None, "note": "disabled"}
+    if sampler is not None:
+        held = sampler.window(clock_t0, clock_t1)
+        inside = sampler.window(t_host0, t_host1)
+        sampler.stop()
+        clocks = dict(held)
+        clocks["timed_region_samples"] = inside["samples"]
+        clocks["window"] = (f"nvidia-smi every 50 ms while the timed graphs were replayed back to back for "
+                            f"{clock_t1 - clock_t0:.1f} s right after the timed region "
+                            f"({(t_host1 - t_host0) * 1e3:.2f} ms, {inside['samples']} samples inside it)")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
         threads = cpu_threads()
         cb, calls, nrows, el = time_oracle(w, args.cpu_seconds, threads, args.cpu_rows)
-        rows = list(range(nrows))
-        A_s, x_s, s_s, idx = oracle_rows(w, rows)
-        y_ref, den = oracle.load().gemv(w.dtype, A_s, x_s, nrows, w.N, scales=s_s, rows=idx,
-                                        threads=threads)
+        cb1, calls1, nrows1, el1 = time_oracle(w, args.cpu_seconds, 1, args.cpu_rows)
         cpu = {"value": cb, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{calls} oracle passes over rows 0..{nrows - 1} of the workload "
                          f"({el:.1f} s, double precision, {threads} threads)",
-               "parity_max_normalised_error": oracle.max_normalised_error(y_first[:nrows], y_ref, den)}
+               "single_thread": {"value": cb1, "unit": "GB/s", "cores": 1,
+                                 "sample": f"{calls1} passes over rows 0..{nrows1 - 1} ({el1:.1f} s, 1 thread)"}}
 
+    parity_err = parity_all_rows(w, R.inp, y_first)
     published = PUBLISHED.get(w.name)
+    launch_desc = " + ".join(f"{reps} replay{'s' if reps > 1 else ''} of a CUDA graph of {n} back-to-back launches"
+                             for n, reps in plan)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / max(1, args.steps) * 1e3,
@@ -602,11 +682,12 @@ def run_ours(args):
         "dtype": w.dtype, "data": "synthetic (seeded SplitMix64; weights and x normal(0,0.02) "
                                   "rounded to FP16)" if w.dtype == "f16" else "synthetic (seeded SplitMix64)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "weights": w.dtype,
-                   "variant": vinfo["name"], "rotation_copies": copies,
-                   "rotation_bytes": copies * wbytes, "l2_bytes": l2,
-                   "l2_policy": "inputs larger than L2: weights rotate through the copies, each "
-                                "launch reads A cold from HBM",
-                   "launch": f"CUDA graph of {batch} back-to-back launches",
+                   "variant": vinfo["name"], "rotation_copies": R.copies,
+                   "rotation_bytes": R.copies * R.wbytes, "l2_bytes": l2,
+                   "l2_policy": "inputs larger than L2 (weights rotate through the copies, each launch reads "
+                                "A cold from HBM) and L2 flushed by a 2 x L2 write before the timed region",
+                   "launch": f"timed: {launch_desc}; each graph replayed during warm-up; a spin kernel queued "
+                             f"ahead of the timed region",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "mbu": {"probe_gbs": ceiling, "probe_variant": best_probe,
                 "mbu_probe_pct": 100.0 * achieved / ceiling,
@@ -617,9 +698,12 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "parity_max_normalised_error_all_rows": parity_err,
         "eager_stream_gbs": eager_gbs,
         "overlap": overlap,
+        "long_chain": long_chain,
         "ms_per_launch": per_launch * 1e3,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -630,6 +714,144 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_e2e(args, mbg, R, stream, world, dev):
+    """One gemv_ex_host call per step through the C ABI, x in and y out through
+    page-locked host memory; timed on the host clock (including the final
+    synchronisation) and, for comparison, with CUDA events."""
+    import torch
+    w = R.w
+    if w.dtype == "q8row":
+        return None
+    L = mbg.lib()
+    x_host = R.x.cpu().pin_memory()
+    y_host = torch.empty(w.M, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(R.x)
+    steps = min(args.steps, args.e2e_steps) if args.e2e_steps > 0 else args.steps
+    steps = max(steps, args.e2e_min_steps)
+    dt = mbg.DTYPES[w.dtype]
+    a_ptrs = [a.data_ptr() for a in R.As]
+    s_ptrs = [s.data_ptr() if s is not None else None for s in R.Ss]
+    xh, xd, yh = x_host.data_ptr(), x_dev.data_ptr(), y_host.data_ptr()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    fn = L.gemv_ex_host
+
+    def run(flags, n):
+        for i in range(n):
+            k = i % R.copies
+            st = fn(dt, a_ptrs[k], xh, xd, yh, w.M, w.N, s_ptrs[k], flags, sp)
+            if st != mbg.OK:
+                raise SystemExit(f"gemv_ex_host: {mbg.status_string(st)}")
+
+    out = {}
+    for flags, key in ((0, "plain"), (mbg.FLAG_OVERLAP_PRECEDING, "overlap")):
+        run(flags, min(args.warmup + 10, 100))
+        stream.synchronize()
+        barrier()
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        h0.record(stream)
+        run(flags, steps)
+        h1.record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        out[key] = (max_over_ranks(wall, dev), max_over_ranks(h0.elapsed_time(h1) * 1e-3, dev))
+    wall, ev = out["plain"]
+    return {"value": gbs(world * steps * R.step_bytes, wall), "unit": "GB/s",
+            "h2d_bytes_per_step": int(R.x.numel() * R.x.element_size()),
+            "d2h_bytes_per_step": int(w.M * 4), "steps": steps,
+            "us_per_step": wall / steps * 1e6,
+            "how": "host wall clock (perf_counter) around `steps` gemv_ex_host calls through the C ABI and the "
+                   "final stream synchronisation: per step x is read from pinned host memory by a copy kernel "
+                   "into a device buffer, the GEMV runs after it with programmatic dependent launch and writes "
+                   "y into pinned host memory; weights resident and rotated",
+            "device_events_value": gbs(world * steps * R.step_bytes, ev),
+            "overlap_value": gbs(world * steps * R.step_bytes, out["overlap"][0]),
+            "overlap_how": "the same calls with GEMV_FLAG_OVERLAP_PRECEDING (each copy of x may start before "
+                           "the previous GEMV ends), host wall clock"}
+
+
+def measure_configs(args, mbg, dev, l2, stream, timer, ceiling):
+    """Every workload of the five families: time per launch (plain and overlapped
+    chains), GB/s, MBU, parity over every row; FP16 / INT8 / INT4 interleaved."""
+    import torch
+    out = {"how": f"per workload: automatic kernel; a CUDA graph of ~{args.config_launches} back-to-back "
+                  f"launches over the rotated weights, replayed once to warm and once timed after an L2 flush; "
+                  f"MBU against the run's probe ceiling ({ceiling:.0f} GB/s) and the 8 TB/s spec; parity: the "
+                  f"first launch against the double-precision oracle over every row",
+           "workloads": {}, "interleaved": {}}
+    resident = {}
+    keep = {name for group in INTERLEAVED.values() for name in group}
+    t_start = time.monotonic()
+
+    def chain(R, overlap):
+        n = R.copies * max(1, math.ceil(args.config_launches / R.copies))
+        plan = [(n, 1)]
+        g = timer.capture(R.launch, plan, overlap=overlap)
+        timer.warm(g, plan, 1)
+        t = timer.timed(g, plan)
+        return g, plan, t / n
+
+    for name in CONFIG_WORKLOADS:
+        w = synth.WORKLOADS[name]
+        R = Resident(w, dev, l2)
+        with torch.cuda.stream(stream):
+            R.launch(0)
+        stream.synchronize()
+        y0 = R.y.cpu().numpy().copy()
+        err = parity_all_rows(w, R.inp, y0)
+        vid = mbg.select_variant(w.dtype, R.As[0], R.x)
+        vname = mbg.variants(w.dtype)[vid]["name"]
+        vkind = mbg.variants(w.dtype)[vid]["kind"]
+        g, plan, t = chain(R, False)
+        g_ov, _, t_ov = chain(R, True)
+        rec = {"M": w.M, "N": w.N, "weights": w.dtype, "variant": vname,
+               "kernel": KERNEL_NAMES[vkind], "bytes": R.step_bytes, "rotation_copies": R.copies,
+               "us": t * 1e6, "gbs": gbs(R.step_bytes, t),
+               "mbu_probe_pct": 100.0 * gbs(R.step_bytes, t) / ceiling,
+               "mbu_spec_pct": 100.0 * gbs(R.step_bytes, t) / SPEC_HBM_GBS,
+               "overlap_us": t_ov * 1e6, "overlap_gbs": gbs(R.step_bytes, t_ov),
+               "overlap_mbu_probe_pct": 100.0 * gbs(R.step_bytes, t_ov) / ceiling,
+               "parity_max_normalised_error": err, "parity_rows": w.M, "tolerance": TOL[w.dtype],
+               "parity_ok": bool(err <= TOL[w.dtype])}
+        if mbg.gemv_get_device_error(stream) != mbg.OK:
+            rec["device_status"] = "timeout reported"
+        out["workloads"][name] = rec
+        if name in keep:
+            R.inp = None
+            resident[name] = (R, g, plan)
+        else:
+            R.free()
+            del g
+        del g_ov
+        torch.cuda.empty_cache()
+
+    for shape, names in INTERLEAVED.items():
+        best = {n: float("inf") for n in names}
+        for _ in range(args.interleave_rounds):
+            for n in names:
+                R, g, plan = resident[n]
+                best[n] = min(best[n], timer.timed(g, plan) / plan[0][0])
+        f16_t = best[names[0]]
+        entry = {}
+        for n in names:
+            R = resident[n][0]
+            entry[R.w.dtype] = {"workload": n, "us": best[n] * 1e6, "gbs": gbs(R.step_bytes, best[n]),
+                                "mbu_probe_pct": 100.0 * gbs(R.step_bytes, best[n]) / ceiling,
+                                "x_fp16": f16_t / best[n]}
+        out["interleaved"][shape] = entry
+    out["interleaved_how"] = (f"FP16, INT8 and INT4 graphs of the same shape timed in turn, "
+                              f"{args.interleave_rounds} rounds, best round per kernel; x_fp16 = FP16 time / "
+                              f"kernel time (\"membound\", dequant GEMV: INT4 cap 3.87x)")
+    for R, g, plan in resident.values():
+        R.free()
+    resident.clear()
+    torch.cuda.empty_cache()
+    out["seconds"] = time.monotonic() - t_start
+    return out
 
 
 SOFTMAX_METRIC = "achieved HBM GB/s (one read + one write per element) and MBU% vs measured copy ceiling for FP16 row softmax"
@@ -654,6 +876,7 @@ def run_softmax(args):
     y = torch.empty_like(x0)
     step_bytes = 4 * w.M * w.N
     stream = torch.cuda.Stream(dev)
+    timer = Timer(dev, stream, l2)
     with torch.cuda.stream(stream):
         mbg.gemv_softmax_f16(x0, y=y)
     stream.synchronize()
@@ -678,26 +901,15 @@ def run_softmax(args):
                 res[name] = gbs(2 * half * args.probe_reps, e0.elapsed_time(e1) * 1e-3)
         return res
 
+    def launch(i, overlap=False):
+        mbg.gemv_softmax_f16(xs[i % copies], y=y)
+
     before = copy_probe()
-    batch = copies * max(1, math.ceil(min(args.graph_batch, 50) / copies))
-    n_full, n_tail = split_steps(args.steps, batch)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(batch):
-            mbg.gemv_softmax_f16(xs[i % copies], y=y)
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup // batch)):
-            g.replay()
-    stream.synchronize()
-    with torch.cuda.stream(stream):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(max(1, n_full)):
-            g.replay()
-        e1.record(stream)
-    e1.synchronize()
-    steps = max(1, n_full) * batch
-    t = e0.elapsed_time(e1) * 1e-3
+    plan = graph_plan(args.steps, copies, min(args.graph_max, 50 * copies))
+    graphs = timer.capture(launch, plan)
+    timer.warm(graphs, plan, args.warmup)
+    t = timer.timed(graphs, plan)
+    steps = args.steps
     after = copy_probe()
     best = {k: max(before[k], after[k]) for k in before}
     ceiling = max(best.values())
@@ -713,8 +925,9 @@ def run_softmax(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded SplitMix64 normal(0, 2) logits rounded to FP16)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "rotation_copies": copies,
-                       "l2_policy": "inputs larger than L2: the logits rotate through the copies",
-                       "launch": f"CUDA graph of {batch} back-to-back launches"},
+                       "l2_policy": "inputs larger than L2: the logits rotate through the copies; L2 flushed "
+                                    "before the timed region",
+                       "launch": " + ".join(f"{reps} x graph of {n} launches" for n, reps in plan)},
             "mbu": {"copy_probe_gbs": ceiling, "mbu_copy_pct": 100.0 * value / ceiling, "probes": best},
             "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
                          "frac": value / peak, "peak_kind": peak_kind,
@@ -776,23 +989,30 @@ def run_profile_softmax(args):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30000)
-    p.add_argument("--warmup", type=int, default=300)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--op", choices=("gemv", "softmax"), default="gemv")
     p.add_argument("--workload", default=None,
                    choices=sorted(synth.WORKLOADS) + sorted(synth.SOFTMAX_WORKLOADS))
-    p.add_argument("--graph-batch", type=int, default=100)
+    p.add_argument("--graph-max", type=int, default=GRAPH_MAX, help="launches per captured graph")
     p.add_argument("--probe-gib", type=float, default=1.0)
     p.add_argument("--probe-reps", type=int, default=10)
-    p.add_argument("--e2e-steps", type=int, default=5000)
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--e2e-steps", type=int, default=5000, help="e2e steps (at most --steps)")
+    p.add_argument("--e2e-min-steps", type=int, default=200, help="e2e steps at least")
+    p.add_argument("--long-steps", type=int, default=2000, help="launches of the comparison long chain")
+    p.add_argument("--clock-seconds", type=float, default=1.0)
+    p.add_argument("--config-launches", type=int, default=200)
+    p.add_argument("--interleave-rounds", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=5.0)
     p.add_argument("--cpu-rows", type=int, default=512)
     p.add_argument("--reference-seconds", type=float, default=60.0)
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-overlap", action="store_true")
+    p.add_argument("--no-long-chain", action="store_true")
+    p.add_argument("--no-configs", action="store_true", help="skip the per-workload block")
     p.add_argument("--profile", action="store_true", help="one launch of the GEMV, for ncu")
     p.add_argument("--variant", default=None, help="kernel variant name for --profile")
     p.add_argument("--json-out", default=None)

@@ -52,7 +52,10 @@ typedef enum {
     GEMV_ERR_UNSUPPORTED = 3,   /* e.g. INT4 with odd N, size beyond the index range */
     GEMV_ERR_LAUNCH = 4,        /* the CUDA launch failed */
     GEMV_ERR_TIMEOUT = 5,       /* a device-side wait gave up (see gemv_get_device_error) */
-    GEMV_ERR_CUDA = 6           /* another CUDA runtime call failed */
+    GEMV_ERR_CUDA = 6,          /* another CUDA runtime call failed */
+    GEMV_ERR_TIMEOUT_UNDRAINED = 7 /* as GEMV_ERR_TIMEOUT, and the bounded wait for the block's own
+                                      copies still in flight gave up too (see
+                                      gemv_get_device_error) */
 } gemv_status_t;
 
 /* Storage types, used by the variant-introspection calls. */
@@ -217,7 +220,8 @@ gemv_status_t gemv_ex_host_noalloc(int dtype, const void *A, const void *x_host,
  * word into the low 32 bits of *sink with XOR (so no read is dead code).
  * bytes must be a multiple of 16 and buf 16-byte aligned.  `variant` selects
  * the read pattern (0 .. gemv_probe_variant_count()-1).  A bulk pattern whose
- * bounded wait gives up sets bit 63 of *sink.  Achieved bytes / time is the
+ * bounded wait gives up sets bit 63 of *sink (and bit 62 when its wait for
+ * the copies still in flight gave up too).  Achieved bytes / time is the
  * measured read ceiling that memory-bandwidth utilisation is quoted against.
  * "membound", section "Why GEMV, and why MBU" (pure-read probe as the
  * denominator for a read-dominated kernel).
@@ -305,24 +309,30 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
  * 2 = element-wise kernel for layouts without 16-byte alignment;
  * 3 = bulk-copy pipeline: tiles of consecutive rows streamed into a ring of
  * shared-memory stages by bulk async copies (rows_per_group = rows per stage,
- * threads_per_row = consumer threads of the block, plus one producer warp).
+ * threads_per_row = consumer threads of the block, plus one producer warp);
+ * 4 = row bands: for rows of exactly threads_per_row * unroll 16-byte chunks,
+ * each thread keeps the x of its chunks in registers and a window of
+ * rows_per_group rows in flight; block b of the persistent grid takes rows
+ * b, b + grid, b + 2 grid, ...
  */
 typedef struct {
     int dtype;           /* gemv_dtype_t */
     int kind;            /* kernel family, see above */
     int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1),
-                            the consumer threads of the block (family 3) */
-    int rows_per_group;  /* rows one lane group streams together (family 0, x reuse) */
+                            the consumer threads of the block (family 3), the block (family 4) */
+    int rows_per_group;  /* rows one lane group streams together (family 0, x reuse); rows per
+                            stage (family 3); rows in flight per thread (family 4) */
     int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread;
                             family 3: chunks per consumer thread and row when the variant is
                             specialised for rows of exactly unroll * threads_per_row chunks
-                            (0: any row length) */
+                            (0: any row length); family 4: chunks per thread and row */
     int warps;           /* warps per block */
     int math;            /* 0: operands converted to FP32; 1: binary16 operands into
                             mixed-precision FMAs with FP32 accumulation */
     int xmode;          /* 0: x copied to shared memory by a bulk async copy,
                            1: x copied to shared memory by vector loads,
-                           2: x read through the L1 cache, 3: element-wise kernel */
+                           2: x read through the L1 cache, 3: element-wise kernel,
+                           4: x held in registers (family 4) */
     char name[48];
 } gemv_variant_info_t;
 
@@ -343,14 +353,40 @@ gemv_status_t gemv_q8_rowscale_run_variant(int variant, const int8_t *A, const u
  * Synchronises `stream`, reads and clears this device's status word.
  * Returns GEMV_ERR_TIMEOUT if any kernel gave up a bounded wait since the
  * last call, GEMV_OK otherwise (GEMV_ERR_CUDA if the CUDA calls fail).
+ * GEMV_ERR_TIMEOUT_UNDRAINED: a block that gave up then also gave up waiting
+ * for a bulk copy it had issued, so that copy may have landed in shared
+ * memory after the block exited; treat every result computed on this device
+ * since the previous call as suspect.
  */
 gemv_status_t gemv_get_device_error(void *stream);
 
 /* Test hooks.  Limit of every device-side wait in nanoseconds (default one
- * second), and a switch that makes the next launches skip the bulk copy of x
- * so that their wait runs out (nothing is copied, nothing faults). */
+ * second; values below 100 us are raised to 100 us, 0 restores the default),
+ * and switches that make the next launches arm a barrier for a bulk copy
+ * without issuing the copy, so that the bounded wait on it runs out (nothing
+ * is copied, nothing faults):
+ *   GEMV_DEBUG_SKIP_X        the bulk copy of x (GEMV kernels staging x that way);
+ *   GEMV_DEBUG_SKIP_STAGE    the first weight stage of every bulk-pipeline block;
+ *   GEMV_DEBUG_SKIP_SEGMENT  the first row segment of every softmax block that
+ *                            stages rows by bulk copies;
+ *   GEMV_DEBUG_SKIP_PROBE    the first chunk of every bulk-copy probe block.
+ * gemv_debug_skip_x_copy(on) sets or clears GEMV_DEBUG_SKIP_X alone. */
+#define GEMV_DEBUG_SKIP_X 1u
+#define GEMV_DEBUG_SKIP_STAGE 2u
+#define GEMV_DEBUG_SKIP_SEGMENT 4u
+#define GEMV_DEBUG_SKIP_PROBE 8u
 void gemv_debug_set_wait_limit_ns(uint64_t ns);
 void gemv_debug_skip_x_copy(int on);
+void gemv_debug_skip_copies(unsigned int mask);
+
+/* Test hook: a kernel that lets the next kernel on `stream` start at once
+ * (programmatic dependent launch) and only after delay_ns fills
+ * dst[0..bytes) with the 32-bit pattern `word` -- a preceding kernel that
+ * writes a GEMV's operands late, for checking the ordering of gemv_ex_host.
+ * dst: device memory, 4-byte aligned; bytes a multiple of 4; delay_ns at most
+ * one second (longer is clamped). */
+gemv_status_t gemv_debug_late_fill(void *dst, size_t bytes, uint32_t word, uint64_t delay_ns,
+                                   void *stream);
 
 const char *gemv_status_string(gemv_status_t status);
 int gemv_last_cuda_error(void); /* last cudaError_t seen by this thread, 0 if none */

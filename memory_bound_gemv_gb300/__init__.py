@@ -25,10 +25,14 @@ GROUP = 128
 
 STATUS = {0: "GEMV_OK", 1: "GEMV_ERR_INVALID_VALUE", 2: "GEMV_ERR_MISALIGNED",
           3: "GEMV_ERR_UNSUPPORTED", 4: "GEMV_ERR_LAUNCH", 5: "GEMV_ERR_TIMEOUT",
-          6: "GEMV_ERR_CUDA"}
-OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_CUDA = range(7)
+          6: "GEMV_ERR_CUDA", 7: "GEMV_ERR_TIMEOUT_UNDRAINED"}
+(OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_CUDA,
+ ERR_TIMEOUT_UNDRAINED) = range(8)
 
-XMODES = {0: "bulk", 1: "vec", 2: "l1", 3: "elem"}
+# test hooks (gemv_debug_skip_copies)
+SKIP_X, SKIP_STAGE, SKIP_SEGMENT, SKIP_PROBE = 1, 2, 4, 8
+
+XMODES = {0: "bulk", 1: "vec", 2: "l1", 3: "elem", 4: "reg"}
 
 
 class GemvError(RuntimeError):
@@ -37,7 +41,7 @@ class GemvError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
 
 
-KINDS = {0: "vec", 1: "tile", 2: "elem", 3: "bulk"}
+KINDS = {0: "vec", 1: "tile", 2: "elem", 3: "bulk", 4: "band"}
 
 
 class VariantInfo(ctypes.Structure):
@@ -101,6 +105,10 @@ def _declare(L):
     L.gemv_debug_set_wait_limit_ns.restype = None
     L.gemv_debug_skip_x_copy.argtypes = [i32]
     L.gemv_debug_skip_x_copy.restype = None
+    L.gemv_debug_skip_copies.argtypes = [ctypes.c_uint]
+    L.gemv_debug_skip_copies.restype = None
+    L.gemv_debug_late_fill.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64, vp]
+    L.gemv_debug_late_fill.restype = st
     L.gemv_status_string.argtypes = [st]
     L.gemv_status_string.restype = ctypes.c_char_p
     L.gemv_last_cuda_error.argtypes = []
@@ -515,6 +523,19 @@ def debug_set_wait_limit_ns(ns: int):
 
 def debug_skip_x_copy(on: bool):
     lib().gemv_debug_skip_x_copy(1 if on else 0)
+
+
+def debug_skip_copies(mask: int):
+    """Test hook: SKIP_X | SKIP_STAGE | SKIP_SEGMENT | SKIP_PROBE (0 clears all)."""
+    lib().gemv_debug_skip_copies(mask)
+
+
+def debug_late_fill(dst, word: int, delay_ns: int, stream=None):
+    """Test hook: fill dst (a CUDA tensor) with a 32-bit pattern after delay_ns,
+    letting the next kernel on the stream start at once."""
+    nbytes = dst.numel() * dst.element_size()
+    _raise(lib().gemv_debug_late_fill(dst.data_ptr(), nbytes, word, delay_ns, _stream_ptr(stream)),
+           "gemv_debug_late_fill")
 
 
 def status_string(status: int) -> str:

@@ -47,7 +47,7 @@ struct DeviceState {
 DeviceState g_devices[kMaxDevices];
 
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
-std::atomic<int> g_skip_x_copy{0};
+std::atomic<unsigned int> g_skip_copies{0};
 thread_local int t_last_cuda_error = 0;
 
 gemv_status_t cuda_fail(cudaError_t e, gemv_status_t code)
@@ -157,6 +157,7 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N, int64_t groups)
                                          is_quant(dtype));
         return static_cast<size_t>(L.total);
     }
+    if (v.kind == KIND_BAND) return 0;  // x in registers, static shared memory only
     if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)
         return static_cast<size_t>(v.x_offset) + static_cast<size_t>(N) * x_elem_bytes(dtype);
     if (v.kind == KIND_TILE) return static_cast<size_t>(v.x_offset);
@@ -187,6 +188,10 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
         const int64_t tx = v.rows_per_group * (rb + (quant ? 2 * g : 0));
         if (tx >= (1 << 20)) return false;
         return true;  // persistent grid
+    }
+    if (v.kind == KIND_BAND) {
+        // every thread takes exactly `unroll` chunks of each row
+        return rb / 16 == static_cast<int64_t>(v.lanes_per_row) * v.unroll;  // persistent grid
     }
     if (v.kind == KIND_TILE) {
         // every row must be covered by one request per thread
@@ -357,7 +362,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
     a.nchunks = static_cast<int>(a.row_bytes / 16);
     a.err = d->status;
     a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-    a.skip_x_copy = g_skip_x_copy.load(std::memory_order_relaxed);
+    a.skip_copies = g_skip_copies.load(std::memory_order_relaxed);
     a.pdl = ((flags & GEMV_FLAG_OVERLAP_PRECEDING) && v.supports_pdl()) ? 1 : 0;
 
     int64_t blocks;
@@ -366,7 +371,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
         blocks = (M + v.warps - 1) / v.warps;
     } else {
         blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
-        if (v.kind == KIND_TILE || v.kind == KIND_BULK) {
+        if (v.kind == KIND_TILE || v.kind == KIND_BULK || v.kind == KIND_BAND) {
             const int resident = resident_blocks(*d, dtype, vid, v, smem);
             if (resident <= 0) return GEMV_ERR_CUDA;
             if (blocks > resident) blocks = resident;
@@ -549,7 +554,9 @@ gemv_status_t gemv_probe_read(const void *buf, size_t bytes, unsigned long long 
     if (!d) return GEMV_ERR_CUDA;
     const ProbeVariant &p = pv[variant];
     const unsigned grid = static_cast<unsigned>(d->sm_count * p.blocks_per_sm);
-    p.launch(buf, bytes / 16, sink, grid, static_cast<cudaStream_t>(stream));
+    p.launch(buf, bytes / 16, sink, grid, g_wait_limit_ns.load(std::memory_order_relaxed),
+             (g_skip_copies.load(std::memory_order_relaxed) & SKIP_PROBE) != 0,
+             static_cast<cudaStream_t>(stream));
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
 }
@@ -641,6 +648,7 @@ static gemv_status_t softmax_run(const uint16_t *x, uint16_t *y, int64_t M, int6
     if (!d) return GEMV_ERR_CUDA;
     const cudaError_t e = launch_softmax(x, y, M, N, variant, d->status,
                                          g_wait_limit_ns.load(std::memory_order_relaxed),
+                                         g_skip_copies.load(std::memory_order_relaxed),
                                          static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return GEMV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
@@ -691,6 +699,7 @@ gemv_status_t gemv_get_device_error(void *stream)
         e = cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_CUDA);
     }
+    if (word & DEVERR_UNDRAINED) return GEMV_ERR_TIMEOUT_UNDRAINED;
     return (word & DEVERR_TIMEOUT) ? GEMV_ERR_TIMEOUT : GEMV_OK;
 }
 
@@ -704,7 +713,28 @@ void gemv_debug_set_wait_limit_ns(uint64_t ns)
     g_wait_limit_ns.store(ns, std::memory_order_relaxed);
 }
 
-void gemv_debug_skip_x_copy(int on) { g_skip_x_copy.store(on ? 1 : 0, std::memory_order_relaxed); }
+void gemv_debug_skip_x_copy(int on)
+{
+    if (on) g_skip_copies.fetch_or(SKIP_X, std::memory_order_relaxed);
+    else g_skip_copies.fetch_and(~static_cast<unsigned int>(SKIP_X), std::memory_order_relaxed);
+}
+
+gemv_status_t gemv_debug_late_fill(void *dst, size_t bytes, uint32_t word, uint64_t delay_ns, void *stream)
+{
+    if (bytes == 0) return GEMV_OK;
+    if (!dst) return GEMV_ERR_INVALID_VALUE;
+    if (bytes % 4 || !aligned(dst, 4)) return GEMV_ERR_MISALIGNED;
+    if (delay_ns > 1000000000ull) delay_ns = 1000000000ull;
+    if (!current_device()) return GEMV_ERR_CUDA;
+    launch_late_fill(dst, bytes, word, delay_ns, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e, GEMV_ERR_LAUNCH);
+}
+
+void gemv_debug_skip_copies(unsigned int mask)
+{
+    g_skip_copies.store(mask & (SKIP_X | SKIP_STAGE | SKIP_SEGMENT | SKIP_PROBE), std::memory_order_relaxed);
+}
 
 const char *gemv_status_string(gemv_status_t status)
 {
@@ -716,6 +746,7 @@ const char *gemv_status_string(gemv_status_t status)
     case GEMV_ERR_LAUNCH: return "GEMV_ERR_LAUNCH";
     case GEMV_ERR_TIMEOUT: return "GEMV_ERR_TIMEOUT";
     case GEMV_ERR_CUDA: return "GEMV_ERR_CUDA";
+    case GEMV_ERR_TIMEOUT_UNDRAINED: return "GEMV_ERR_TIMEOUT_UNDRAINED";
     default: return "GEMV_ERR_UNKNOWN";
     }
 }

@@ -9,7 +9,7 @@ namespace mbg {
 
 // One thread per 16-byte chunk (vector layout) -> EPC outputs.
 template <int DT>
-__global__ void dequant_vec_kernel(const unsigned char *A, const uint16_t *scales, float *W,
+__global__ void mbg_dequant_vec_kernel(const unsigned char *A, const uint16_t *scales, float *W,
                                    int64_t M, int64_t N, int64_t row_bytes, int64_t groups)
 {
     constexpr int EPC = Fmt<DT>::EPC;
@@ -48,7 +48,7 @@ __global__ void dequant_vec_kernel(const unsigned char *A, const uint16_t *scale
 
 // One thread per element (any layout).
 template <int DT>
-__global__ void dequant_elem_kernel(GemvArgs p, float *W)
+__global__ void mbg_dequant_elem_kernel(GemvArgs p, float *W)
 {
     const int64_t total = p.M * p.N;
     for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < total;
@@ -73,8 +73,8 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
     const auto *a = static_cast<const unsigned char *>(A);
     if (vec) {
         const unsigned g = grid_for(M * (row_bytes / 16), 256);
-        if (dtype == DT_Q8) dequant_vec_kernel<DT_Q8><<<g, 256, 0, s>>>(a, scales, W, M, N, row_bytes, groups);
-        else dequant_vec_kernel<DT_Q4><<<g, 256, 0, s>>>(a, scales, W, M, N, row_bytes, groups);
+        if (dtype == DT_Q8) mbg_dequant_vec_kernel<DT_Q8><<<g, 256, 0, s>>>(a, scales, W, M, N, row_bytes, groups);
+        else mbg_dequant_vec_kernel<DT_Q4><<<g, 256, 0, s>>>(a, scales, W, M, N, row_bytes, groups);
     } else {
         GemvArgs p{};
         p.A = A;
@@ -85,12 +85,12 @@ void launch_dequant(int dtype, const void *A, const uint16_t *scales, float *W, 
         p.groups = groups;
         p.scale_elem_shift = 7;  // 128 columns per scale
         const unsigned g = grid_for(M * N, 256);
-        if (dtype == DT_Q8) dequant_elem_kernel<DT_Q8><<<g, 256, 0, s>>>(p, W);
-        else dequant_elem_kernel<DT_Q4><<<g, 256, 0, s>>>(p, W);
+        if (dtype == DT_Q8) mbg_dequant_elem_kernel<DT_Q8><<<g, 256, 0, s>>>(p, W);
+        else mbg_dequant_elem_kernel<DT_Q4><<<g, 256, 0, s>>>(p, W);
     }
 }
 
-__global__ void fill_zero_kernel(float *y, int64_t M)
+__global__ void mbg_fill_zero_kernel(float *y, int64_t M)
 {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -99,7 +99,7 @@ __global__ void fill_zero_kernel(float *y, int64_t M)
 
 void launch_fill_zero(float *y, int64_t M, cudaStream_t s)
 {
-    fill_zero_kernel<<<grid_for(M, 256), 256, 0, s>>>(y, M);
+    mbg_fill_zero_kernel<<<grid_for(M, 256), 256, 0, s>>>(y, M);
 }
 
 }  // namespace mbg

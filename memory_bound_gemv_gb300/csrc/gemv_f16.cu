@@ -7,6 +7,12 @@
 namespace mbg {
 
 static const Variant kTableF16[] = {
+    // row bands, x in registers: band_t<threads>_c<chunks per thread>_u<rows in flight>
+    // (rows of exactly threads * chunks 16-byte chunks)
+    MBG_BAND(DT_F16, 256, 2, 8, 2, "band_t256_c2_u8"),
+    MBG_BAND(DT_F16, 128, 4, 4, 4, "band_t128_c4_u4"),
+    MBG_BAND(DT_F16, 448, 4, 4, 1, "band_t448_c4_u4"),
+    MBG_BAND(DT_F16, 896, 2, 3, 1, "band_t896_c2_u3"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_F16, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_F16, 256, 1, 3, "bulk_t256_r1_s3"),

@@ -9,17 +9,28 @@
 // memory; when the caller allows it (early), it reads x before that wait and
 // only writes the device buffer after it.  The GEMV after it starts
 // streaming its weights while x is still in flight.
+//
+// Ordering.  The GEMV after the copy is launched with programmatic
+// dependent launch and loads weights before its own wait, which only orders
+// it after the copy kernel.  So unless the caller has promised that the
+// kernel before the call leaves the weights alone (early), every copy block
+// first waits for that kernel and only then lets the GEMV start: the GEMV's
+// blocks then begin after that kernel has completed, as with a plain launch.
 #include "gemv_kernels.cuh"
 
 namespace mbg {
 
 namespace {
 
-__global__ void __launch_bounds__(256) copy_in_kernel(const unsigned char *src, unsigned char *dst,
+__global__ void __launch_bounds__(256) mbg_copy_in_kernel(const unsigned char *src, unsigned char *dst,
                                                       int64_t bytes, int vec, int early)
 {
-    pdl_trigger();
-    if (!early) pdl_wait();
+    if (early) {
+        pdl_trigger();
+    } else {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n16 = vec ? bytes / 16 : 0;
@@ -36,7 +47,33 @@ __global__ void __launch_bounds__(256) copy_in_kernel(const unsigned char *src, 
     for (int64_t b = n16 * 16 + t0; b < bytes; b += stride) dst[b] = src[b];
 }
 
+// Test helper: lets the next kernel start at once, then after delay_ns
+// fills dst with a 32-bit pattern (a preceding kernel that writes a GEMV's
+// operands late).  The delay is a spin on the global timer that ends by
+// itself.
+__global__ void __launch_bounds__(256) mbg_late_fill_kernel(uint32_t *dst, size_t words, uint32_t word,
+                                                            uint64_t delay_ns)
+{
+    pdl_trigger();
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < delay_ns) {
+    }
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words; i += stride)
+        dst[i] = word;
+}
+
 }  // namespace
+
+void launch_late_fill(void *dst, size_t bytes, uint32_t word, uint64_t delay_ns, cudaStream_t s)
+{
+    const size_t words = bytes / 4;
+    size_t blocks = (words + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 1024) blocks = 1024;
+    mbg_late_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint32_t *>(dst), words,
+                                                                        word, delay_ns);
+}
 
 void launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, cudaStream_t s)
 {
@@ -57,7 +94,7 @@ void launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    (void)cudaLaunchKernelEx(&cfg, copy_in_kernel, sp, dp, bytes, vec ? 1 : 0, early ? 1 : 0);
+    (void)cudaLaunchKernelEx(&cfg, mbg_copy_in_kernel, sp, dp, bytes, vec ? 1 : 0, early ? 1 : 0);
 }
 
 }  // namespace mbg

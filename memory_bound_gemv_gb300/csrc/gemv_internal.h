@@ -10,18 +10,32 @@ namespace mbg {
 // Storage types.  DT_F16X32: binary16 weights with an FP32 x.
 enum { DT_F32 = 0, DT_F16 = 1, DT_Q8 = 2, DT_Q4 = 3, DT_F16X32 = 4, DT_COUNT = 5 };
 
-enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3 };
+// x staging: bulk copy into shared memory, vector loads into shared memory,
+// read through L1, element-wise kernel, held in registers (row-band kernel).
+enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3, XMODE_REG = 4 };
 
 // Kernel families: warp/sub-warp rows streamed with a rolling buffer, row
-// tiles walked by a persistent grid, element-wise fallback.
-enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3 };
+// tiles walked by a persistent grid, element-wise fallback, bulk-copy
+// pipeline, row bands with x in registers.
+enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3, KIND_BAND = 4 };
 
 // Dot-product arithmetic: operands converted to FP32, or binary16 operands
 // fed to mixed-precision FMAs with FP32 accumulation.
 enum { MATH_F32 = 0, MATH_MIXED = 1 };
 
-// Device status bits (the device status word).
-enum : unsigned int { DEVERR_TIMEOUT = 1u };
+// Device status bits (the device status word).  DEVERR_UNDRAINED: after a
+// wait gave up, the bounded wait for the block's own copies still in flight
+// gave up too, so a copy may have landed in shared memory the block no
+// longer owned.
+enum : unsigned int { DEVERR_TIMEOUT = 1u, DEVERR_UNDRAINED = 2u };
+
+// Test hooks: copies that a launch arms its barrier for but does not issue,
+// so that the bounded wait on it runs out (nothing is copied, nothing
+// faults).  SKIP_X: the bulk copy of x; SKIP_STAGE: the first weight stage
+// of every bulk-pipeline block; SKIP_SEGMENT: the first row segment of every
+// softmax block that stages rows by bulk copies; SKIP_PROBE: the first chunk
+// of every bulk-copy probe block.
+enum : unsigned int { SKIP_X = 1u, SKIP_STAGE = 2u, SKIP_SEGMENT = 4u, SKIP_PROBE = 8u };
 
 // Columns per FP16 scale in the quantised formats.
 constexpr int kGroup = 128;
@@ -44,7 +58,7 @@ struct GemvArgs {
     int nchunks;              // row_bytes / 16 (vector kernels)
     unsigned int *err;        // device status word
     uint64_t wait_limit_ns;   // bound of every device-side wait
-    int skip_x_copy;          // test hook: arm the barrier but issue no copy
+    unsigned int skip_copies; // test hook (SKIP_*): arm the barrier but issue no copy
     int scale_shift;          // scale group of 16-byte chunk c: c >> scale_shift
     int scale_elem_shift;     // scale group of column j: j >> scale_elem_shift
     int pdl;                  // stream the weights before waiting for the preceding
@@ -72,11 +86,12 @@ struct Variant {
     int math;            // MATH_F32 or MATH_MIXED
     int stages;          // bulk-pipeline depth (KIND_BULK)
     bool x_regs = false; // bulk pipeline keeps x in registers, not in shared memory
-    bool supports_pdl() const { return kind == KIND_TILE || kind == KIND_BULK; }
+    bool supports_pdl() const { return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND; }
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
         if (kind == KIND_BULK) return rows_per_group;
+        if (kind == KIND_BAND) return 1;  // one block per row at most
         return warps * (32 / lanes_per_row) * rows_per_group;
     }
 };
@@ -121,8 +136,9 @@ struct ProbeVariant {
     int unroll;
     int blocks_per_sm;
     int segment;  // 0: grid-stride tiles, 1: one contiguous segment per warp, 2: prefetching tiles
+    // limit_ns bounds the bulk patterns' waits; skip_first: SKIP_PROBE hook
     void (*launch)(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
-                   cudaStream_t s);
+                   uint64_t limit_ns, bool skip_first, cudaStream_t s);
 };
 const ProbeVariant *probe_variants(int *count);
 
@@ -138,6 +154,10 @@ void launch_fill_zero(float *y, int64_t M, cudaStream_t s);
 // for the preceding kernel.
 void launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, cudaStream_t s);
 
+// Test helper (gemv_host.cu): a kernel that lets its successor start at once
+// and fills dst with `word` only after delay_ns.
+void launch_late_fill(void *dst, size_t bytes, uint32_t word, uint64_t delay_ns, cudaStream_t s);
+
 // Symmetric quantisation (gemv_quantize.cu): bits 8 or 4; one scale per row
 // or per 128 columns; FP32 or binary16 weights.
 void launch_quantize(int bits, bool per_row, bool f16in, const void *W, void *A, uint16_t *scales,
@@ -146,7 +166,8 @@ void launch_quantize(int bits, bool per_row, bool f16in, const void *W, void *A,
 // Row softmax (gemv_softmax.cu).  variant < 0 chooses; cudaErrorNotSupported
 // when the variant cannot serve the shape or alignment.
 cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
-                           unsigned int *err, uint64_t wait_limit_ns, cudaStream_t s);
+                           unsigned int *err, uint64_t wait_limit_ns, unsigned int skip,
+                           cudaStream_t s);
 int softmax_variant_count();
 const char *softmax_variant_name(int v);
 

@@ -1,6 +1,6 @@
 // GEMV kernel templates (sm_103a).
 //
-// gemv_vec_kernel: the vectorised path.  A lane group of LPR lanes owns RPW
+// mbg_warprow_kernel: the vectorised path.  A lane group of LPR lanes owns RPW
 // consecutive rows; lane t of the group streams the 16-byte chunks
 // t, t+LPR, t+2*LPR, ... of each of those rows, so with LPR = 32 a warp reads
 // 512 contiguous bytes of a row per step ("cuda-gemv-optimization", kernel 4;
@@ -14,7 +14,7 @@
 // so the copy of x overlaps the first DRAM round trip.  Lane partials are
 // combined with an XOR butterfly inside the group and one lane stores y.
 //
-// gemv_elem_kernel: element-wise path for layouts the vector path cannot take
+// mbg_elem_kernel: element-wise path for layouts the vector path cannot take
 // (unaligned pointers or a row pitch that is not a multiple of 16 bytes).
 #pragma once
 
@@ -24,7 +24,7 @@
 namespace mbg {
 
 template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
-__global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
+__global__ void __launch_bounds__(WARPS * 32) mbg_warprow_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
     constexpr int EPC = F::EPC;
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
             const uint32_t b = smem_addr(bar);
             mbar_init(b, 1);
             mbar_arrive_expect_tx(b, xbytes);
-            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
+            if (!(p.skip_copies & SKIP_X)) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
         }
     }
 
@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
             if (threadIdx.x == 0) report_error(p.err, DEVERR_TIMEOUT);
             // A copy that was issued may still land: give it one more bounded
             // wait before the block's shared memory is released.
-            if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns);
+            if (!(p.skip_copies & SKIP_X) && !mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns))
+                report_error(p.err, DEVERR_UNDRAINED);
             return;
         }
     }
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_vec_kernel(const GemvArgs p)
 // ("llama.cpp GEMV CUDA": a block-wide row with a warp reduction, warp sums
 // in shared memory and a second warp reduction).
 template <int DT, int G, int CPT, int T, int XMODE, int MATH>
-__global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
+__global__ void __launch_bounds__(T) mbg_rowtile_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
     constexpr int EPC = F::EPC;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
             const uint32_t b = smem_addr(bar);
             mbar_init(b, 1);
             mbar_arrive_expect_tx(b, xbytes);
-            if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
+            if (!(p.skip_copies & SKIP_X)) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, b);
         }
     };
     if constexpr (XBULK) {
@@ -280,7 +281,8 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
     if constexpr (XBULK) {
         if (!mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns)) {
             if (tid == 0) report_error(p.err, DEVERR_TIMEOUT);
-            if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns);
+            if (!(p.skip_copies & SKIP_X) && !mbar_wait_bounded(smem_addr(bar), 0, p.wait_limit_ns))
+                report_error(p.err, DEVERR_UNDRAINED);
             return;
         }
     }
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(T) gemv_tile_kernel(const GemvArgs p)
 // ever reads the x of chunks t, t + T, ...; XR keeps those vectors in its
 // registers (loaded once), so x takes no shared memory and no staging barrier.
 template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
-__global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
+__global__ void __launch_bounds__(T + 32) mbg_bulkpipe_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
     constexpr int XCB = x_chunk_bytes<DT>();
@@ -444,6 +446,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         const uint32_t sbytes = stage_scales ? static_cast<uint32_t>(rows * 2 * p.groups) : 0u;
         const uint32_t b = smem_addr(&full[slot]);
         mbar_arrive_expect_tx(b, bytes + sbytes);
+        if (it == 0 && (p.skip_copies & SKIP_STAGE)) return;  // test hook: the wait must run out
         bulk_copy_g2s(smem_addr(smem + L.stage + slot * L.stage_bytes),
                       static_cast<const unsigned char *>(p.A) + r0 * p.row_bytes, bytes, b);
         if (stage_scales)
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         if constexpr (XV == 1) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(smem_addr(xbar), xbytes);
-                if (!p.skip_x_copy) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
+                if (!(p.skip_copies & SKIP_X)) bulk_copy_g2s(smem_addr(xs), p.x, xbytes, smem_addr(xbar));
             }
         } else {
             // the consumer warps load x: the first stage goes out at once, the
@@ -535,13 +538,17 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
         }
         if (lane == 0) {
             // copies issued for iterations [done, issued) may still be in flight
-            for (int64_t j = done; j < issued; ++j)
-                mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
-                                  p.wait_limit_ns);
+            bool drained = true;
+            for (int64_t j = done; j < issued; ++j) {
+                if (j == 0 && (p.skip_copies & SKIP_STAGE)) continue;  // never issued
+                drained &= mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
+                                             p.wait_limit_ns);
+            }
             if (XV == 1 && *abort_flag) {
                 // the x copy, too, may still be in flight
-                if (!p.skip_x_copy) mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns);
+                if (!(p.skip_copies & SKIP_X)) drained &= mbar_wait_bounded(smem_addr(xbar), 0, p.wait_limit_ns);
             }
+            if (!drained) report_error(p.err, DEVERR_UNDRAINED);
         }
         return;
     }
@@ -697,6 +704,224 @@ __global__ void __launch_bounds__(T + 32) gemv_bulk_kernel(const GemvArgs p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Row-band kernel (x held in registers)
+// ---------------------------------------------------------------------------
+//
+// For rows of exactly T * CPT chunks.  Thread t of a block always multiplies
+// the chunks t, t + T, ..., t + (CPT - 1) T of a row, so it loads the x
+// vectors of those chunks into registers once and never reads x again (for
+// INT4 that is 64 bytes of x per 16-byte chunk of A, which from shared
+// memory would cost four loads per chunk and row).  Block b of the
+// persistent grid takes rows b, b + grid, b + 2 grid, ...: every block owns
+// floor(M / grid) or ceil(M / grid) rows, and at any moment the grid as a
+// whole streams one dense band of consecutive rows.  Each thread keeps its
+// chunks of the next U rows in flight in a rolling window of registers: the
+// loads of row j + U are issued as soon as row j has been taken out of its
+// slot, before row j is multiplied.  Per row, the lane partials meet in a
+// warp butterfly and the warps' partials in shared memory, one block barrier
+// per U rows ("llama.cpp GEMV CUDA": warp reduction, warp sums through shared
+// memory, a second reduction).  Quantised chunks are summed into two FP32
+// partials of exact binary16 products and scaled once per chunk (a chunk
+// never straddles a 128-column group).
+//
+// The products are volatile asm: the compiler keeps them in program order
+// relative to the (volatile) loads, so the loads of row j + U are issued
+// before row j is multiplied and each slot's registers are reused at once
+// (otherwise the scheduler hoists all U loads of the next rows above the
+// products and needs a second window of registers).
+__device__ __forceinline__ void mfma_pair_ordered(uint32_t a, uint32_t b, float &c0, float &c1)
+{
+    asm volatile("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+                 " fma.rn.f32.f16 %0, a0, b0, %0;\n fma.rn.f32.f16 %1, a1, b1, %1;\n}"
+                 : "+f"(c0), "+f"(c1)
+                 : "r"(a), "r"(b));
+}
+
+template <int DT, bool PAIRED>
+__device__ __forceinline__ void band_chunk(const uint4 a, const uint4 (&xv)[x_chunk_vecs<DT>()],
+                                           float &c0, float &c1)
+{
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    if constexpr (DT == DT_F16) {
+        mfma_pair_ordered(w[0], xv[0].x, c0, c1);
+        mfma_pair_ordered(w[1], xv[0].y, c0, c1);
+        mfma_pair_ordered(w[2], xv[0].z, c0, c1);
+        mfma_pair_ordered(w[3], xv[0].w, c0, c1);
+    } else if constexpr (DT == DT_Q8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t h[2];
+            q8_codes_h2(w[k], h);
+            const uint4 &x = xv[k >> 1];
+            mfma_pair_ordered(h[0], (k & 1) ? x.z : x.x, c0, c1);
+            mfma_pair_ordered(h[1], (k & 1) ? x.w : x.y, c0, c1);
+        }
+    } else {
+        static_assert(DT == DT_Q4 && PAIRED, "INT4 takes x in the paired order");
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t h[4];
+            q4_codes_h2(w[k], h);
+            const uint4 &x = xv[k];
+            mfma_pair_ordered(h[0], x.x, c0, c1);
+            mfma_pair_ordered(h[1], x.y, c0, c1);
+            mfma_pair_ordered(h[2], x.z, c0, c1);
+            mfma_pair_ordered(h[3], x.w, c0, c1);
+        }
+    }
+}
+
+// Predicated loads that leave the destination unchanged when the predicate is
+// false (the same registers either way, so a rolling window needs no copies).
+__device__ __forceinline__ void ld_stream16_if(uint4 &v, const void *p, bool pred)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
+                 " @q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];\n}"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "l"(p), "r"(static_cast<int>(pred)));
+}
+
+// 16-bit load into the low half of a 32-bit register (zero-extended); the
+// binary16 value is converted only where it is used, so the load stays in
+// flight.
+__device__ __forceinline__ void ld_u16_if(uint32_t &v, const void *p, bool pred)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.u16 %0, [%1];\n}"
+                 : "+r"(v)
+                 : "l"(p), "r"(static_cast<int>(pred)));
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+template <int DT, int T, int CPT, int U, int MINB>
+__global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
+{
+    using F = Fmt<DT>;
+    constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int NW = T / 32;
+    constexpr int ROWB = T * CPT * 16;  // bytes per row
+    constexpr bool PAIRED = DT == DT_Q4;
+    static_assert(T % 32 == 0 && NW <= 32, "block shape");
+    static_assert(F::XB == 2, "binary16 x (mixed-precision products)");
+
+    __shared__ float part[2][U][NW];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t grid = gridDim.x;
+    const int64_t b = blockIdx.x;
+    // rows of this block: b + j * grid for 0 <= j < J
+    const int64_t J = b < p.M ? (p.M - 1 - b) / grid + 1 : 0;
+    const unsigned char *abase = static_cast<const unsigned char *>(p.A) + tid * 16;
+
+    pdl_trigger();
+    // the first U rows of this block into L2 while the preceding kernel
+    // drains (a hint only: it changes no value a later load returns)
+    if (tid < U && tid < J)
+        prefetch_l2(static_cast<const unsigned char *>(p.A) + (b + tid * grid) * ROWB, ROWB);
+    if (!p.pdl) pdl_wait();
+
+    // scale of chunk c of a row: scales[row * groups + (c >> scale_shift)]
+    int soff[CPT];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) soff[k] = (tid + k * T) >> p.scale_shift;
+
+    uint4 a[U][CPT];
+    uint32_t sc[U][CPT];  // binary16 scale bits
+#pragma unroll
+    for (int r = 0; r < U; ++r)
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            a[r][k] = make_uint4(0u, 0u, 0u, 0u);
+            sc[r][k] = 0u;
+        }
+    // rows are loaded strictly in the order j = 0, 1, 2, ...: one pointer
+    // per operand walks them (grid rows apart)
+    int64_t jn = 0;
+    const unsigned char *an = abase + b * ROWB;
+    const int64_t astep = grid * ROWB;
+    const uint16_t *sn = F::QUANT ? p.scales + b * p.groups : nullptr;
+    const int64_t sstep = grid * p.groups;
+    auto load_next = [&](uint4 (&dst)[CPT], uint32_t (&sd)[CPT]) {
+        const bool ok = jn < J;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) ld_stream16_if(dst[k], an + k * T * 16, ok);
+        if constexpr (F::QUANT) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) ld_u16_if(sd[k], sn + soff[k], ok);
+            asm volatile("add.s64 %0, %0, %1;" : "+l"(sn) : "l"(sstep));
+        }
+        // advanced in place (volatile), so that the compiler does not keep
+        // one precomputed address per slot of the window
+        asm volatile("add.s64 %0, %0, %1;" : "+l"(an) : "l"(astep));
+        ++jn;
+    };
+#pragma unroll
+    for (int r = 0; r < U; ++r) load_next(a[r], sc[r]);
+    if (p.pdl) pdl_wait();
+
+    // this thread's x vectors (read after the wait: the preceding kernel may
+    // have written x); re-paired for INT4 so that every product takes the
+    // same half of both operands
+    uint4 xr[CPT][XV];
+    {
+        const uint4 *xs = static_cast<const uint4 *>(p.x);
+#pragma unroll
+        for (int k = 0; k < CPT; ++k)
+#pragma unroll
+            for (int v = 0; v < XV; ++v) xr[k][v] = ld_l2_16(xs + (tid + k * T) * XV + v);
+        if constexpr (PAIRED) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k)
+#pragma unroll
+                for (int v = 0; v < XV; ++v) xr[k][v] = pair_x_vec(xr[k][v]);
+        }
+    }
+
+    int half = 0;
+    for (int64_t j0 = 0; j0 < J; j0 += U) {
+#pragma unroll
+        for (int r = 0; r < U; ++r) {
+            // row j0 + r is multiplied straight from its slot, then the slot
+            // is refilled in place with row j0 + U + r (no second window of
+            // registers; U - 1 rows stay in flight while a row is multiplied)
+            if (j0 + r < J) {
+                float acc = 0.f;
+                if constexpr (F::QUANT) {
+#pragma unroll
+                    for (int k = 0; k < CPT; ++k) {
+                        const float s = half_bits_to_float(sc[r][k]);
+                        float c0 = 0.f, c1 = 0.f;
+                        band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
+                        acc = fmaf(s, c0, acc);
+                        acc = fmaf(s, c1, acc);
+                    }
+                } else {
+                    float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < CPT; ++k) band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
+                    acc = c0 + c1;
+                }
+                // this warp's share of row j0 + r, left for the block sum
+                acc = group_sum<32>(acc);
+                if (lane == 0) part[half][r][warp] = acc;
+            }
+            load_next(a[r], sc[r]);  // row j0 + U + r
+        }
+        __syncthreads();
+        if (tid < U && j0 + tid < J) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) v += part[half][tid][w];
+            p.y[b + (j0 + tid) * grid] = v;
+        }
+        half ^= 1;
+    }
+}
+
 template <int DT, int G, int CPT, int T>
 constexpr int tile_x_offset()
 {
@@ -735,7 +960,7 @@ __device__ __forceinline__ float elem_x(const GemvArgs &p, int64_t j)
 }
 
 template <int DT, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) gemv_elem_kernel(const GemvArgs p)
+__global__ void __launch_bounds__(WARPS * 32) mbg_elem_kernel(const GemvArgs p)
 {
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -758,20 +983,20 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_elem_kernel(const GemvArgs p)
 template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
 void launch_vec(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool)
 {
-    gemv_vec_kernel<DT, LPR, RPW, U, WARPS, XMODE><<<grid, WARPS * 32, smem, s>>>(a);
+    mbg_warprow_kernel<DT, LPR, RPW, U, WARPS, XMODE><<<grid, WARPS * 32, smem, s>>>(a);
 }
 
 template <int DT, int LPR, int RPW, int U, int WARPS, int XMODE>
 cudaError_t smem_limit_vec(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_vec_kernel<DT, LPR, RPW, U, WARPS, XMODE>,
+    return cudaFuncSetAttribute(mbg_warprow_kernel<DT, LPR, RPW, U, WARPS, XMODE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 template <int DT, int WARPS>
 void launch_elem(const GemvArgs &a, unsigned grid, size_t, cudaStream_t s, bool)
 {
-    gemv_elem_kernel<DT, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
+    mbg_elem_kernel<DT, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
 }
 
 template <int DT, int WARPS>
@@ -806,13 +1031,13 @@ void launch_maybe_pdl(Kernel k, const GemvArgs &a, unsigned grid, unsigned block
 template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 void launch_tile(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>, a, grid, T, smem, s, pdl);
+    launch_maybe_pdl(mbg_rowtile_kernel<DT, G, CPT, T, XMODE, MATH>, a, grid, T, smem, s, pdl);
 }
 
 template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 cudaError_t smem_limit_tile(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>,
+    return cudaFuncSetAttribute(mbg_rowtile_kernel<DT, G, CPT, T, XMODE, MATH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -820,7 +1045,7 @@ template <int DT, int G, int CPT, int T, int XMODE, int MATH>
 cudaError_t occupancy_tile(int *blocks, size_t smem)
 {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        blocks, gemv_tile_kernel<DT, G, CPT, T, XMODE, MATH>, T, smem);
+        blocks, mbg_rowtile_kernel<DT, G, CPT, T, XMODE, MATH>, T, smem);
 }
 
 #define MBG_TILE_M(DT, G, CPT, T, XM, MATH, NAME)                                              \
@@ -834,20 +1059,20 @@ cudaError_t occupancy_tile(int *blocks, size_t smem)
 template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 void launch_bulk(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>, a, grid, T + 32, smem, s, pdl);
+    launch_maybe_pdl(mbg_bulkpipe_kernel<DT, T, RS, S, MATH, CF, XR>, a, grid, T + 32, smem, s, pdl);
 }
 
 template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 cudaError_t smem_limit_bulk(int bytes)
 {
-    return cudaFuncSetAttribute(gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>,
+    return cudaFuncSetAttribute(mbg_bulkpipe_kernel<DT, T, RS, S, MATH, CF, XR>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 template <int DT, int T, int RS, int S, int MATH, int CF, bool XR>
 cudaError_t occupancy_bulk(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_bulk_kernel<DT, T, RS, S, MATH, CF, XR>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_bulkpipe_kernel<DT, T, RS, S, MATH, CF, XR>,
                                                          T + 32, smem);
 }
 
@@ -864,6 +1089,32 @@ cudaError_t occupancy_bulk(int *blocks, size_t smem)
 #define MBG_BULK_F(DT, T, RS, S, CF, NAME) \
     MBG_BULK_MF(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), CF, NAME)
 #define MBG_BULK_FX(DT, T, RS, S, CF, NAME) MBG_BULK_MFX(DT, T, RS, S, MATH_MIXED, CF, true, NAME)
+
+template <int DT, int T, int CPT, int U, int MINB>
+void launch_band(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    launch_maybe_pdl(mbg_rowband_kernel<DT, T, CPT, U, MINB>, a, grid, T, smem, s, pdl);
+}
+
+template <int DT, int T, int CPT, int U, int MINB>
+cudaError_t smem_limit_band(int)
+{
+    return cudaSuccess;  // static shared memory only
+}
+
+template <int DT, int T, int CPT, int U, int MINB>
+cudaError_t occupancy_band(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_rowband_kernel<DT, T, CPT, U, MINB>,
+                                                         T, smem);
+}
+
+// band_t<threads>_c<chunks per thread>_u<rows in flight per thread>: rows of
+// exactly threads * chunks 16-byte chunks; x in registers
+#define MBG_BAND(DT, T, CPT, U, MINB, NAME)                                                      \
+    Variant{DT, T, U, CPT, T / 32, XMODE_REG, NAME, &launch_band<DT, T, CPT, U, MINB>,           \
+            &smem_limit_band<DT, T, CPT, U, MINB>, KIND_BAND, 0,                                  \
+            &occupancy_band<DT, T, CPT, U, MINB>, MATH_MIXED, 0}
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -21,7 +21,7 @@
 namespace mbg {
 
 template <int THREADS, int U, int SEGMENT>
-__global__ void __launch_bounds__(THREADS) probe_read_kernel(const uint4 *buf, size_t n16,
+__global__ void __launch_bounds__(THREADS) mbg_probe_read_kernel(const uint4 *buf, size_t n16,
                                                              unsigned long long *sink)
 {
     uint32_t fold = 0;
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(THREADS) probe_read_kernel(const uint4 *buf, s
 }
 
 template <int THREADS, int U>
-__global__ void __launch_bounds__(THREADS) probe_tile_kernel(const uint4 *buf, size_t n16,
+__global__ void __launch_bounds__(THREADS) mbg_probe_tile_kernel(const uint4 *buf, size_t n16,
                                                              unsigned long long *sink)
 {
     uint32_t fold = 0;
@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(THREADS) probe_tile_kernel(const uint4 *buf, s
 // stride order) through an S-deep ring of shared-memory stages with
 // cp.async.bulk, waits on each stage's mbarrier (bounded), and XOR-folds the
 // chunk before the stage is refilled.  On a timeout it waits (bounded) for the
-// copies still in flight and sets bit 63 of *sink.
+// copies still in flight and sets bit 63 of *sink, and bit 62 as well if that
+// wait gave up too.  skip_first (test hook): the first chunk's barrier is
+// armed but no copy is issued, so its wait runs out.
 template <int B, int S>
-__global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t n16,
-                                                        unsigned long long *sink)
+__global__ void __launch_bounds__(32) mbg_probe_bulk_kernel(const uint4 *buf, size_t n16,
+                                                        unsigned long long *sink, uint64_t limit_ns,
+                                                        int skip_first)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
@@ -120,7 +123,6 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t
     const size_t nchunks = (nbytes + B - 1) / B;
     const size_t grid = gridDim.x;
     const size_t iters = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / grid + 1 : 0;
-    constexpr uint64_t kLimitNs = 1000000000ull;
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(smem_addr(&bar[s]), 1);
     __syncwarp();
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t
             const uint32_t b = smem_addr(&bar[k % S]);
             const uint32_t n = chunk_bytes(k);
             mbar_arrive_expect_tx(b, n);
+            if (k == 0 && skip_first) return;
             bulk_copy_g2s(smem_addr(ring + (k % S) * B),
                           reinterpret_cast<const unsigned char *>(buf) + (blockIdx.x + k * grid) * static_cast<size_t>(B),
                           n, b);
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t
     size_t k = 0;
     for (; k < iters; ++k) {
         ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(smem_addr(&bar[k % S]), static_cast<uint32_t>((k / S) & 1), kLimitNs));
+                        mbar_wait_bounded(smem_addr(&bar[k % S]), static_cast<uint32_t>((k / S) & 1), limit_ns));
         if (!ok) break;
         const uint4 *r = reinterpret_cast<const uint4 *>(ring + (k % S) * B);
         const uint32_t n = chunk_bytes(k) / 16;
@@ -157,10 +160,14 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t
         if (issued < iters) issue(issued++);
     }
     if (!ok) {
-        if (lane == 0)
-            for (size_t j = k; j < issued; ++j)
-                mbar_wait_bounded(smem_addr(&bar[j % S]), static_cast<uint32_t>((j / S) & 1), kLimitNs);
-        if (lane == 0) atomicOr(sink, 1ull << 63);
+        if (lane == 0) {
+            bool drained = true;
+            for (size_t j = k; j < issued; ++j) {
+                if (j == 0 && skip_first) continue;  // never issued
+                drained &= mbar_wait_bounded(smem_addr(&bar[j % S]), static_cast<uint32_t>((j / S) & 1), limit_ns);
+            }
+            atomicOr(sink, drained ? (1ull << 63) : (3ull << 62));
+        }
         return;
     }
 #pragma unroll
@@ -170,25 +177,26 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const uint4 *buf, size_t
 
 template <int B, int S>
 void launch_probe_bulk(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
-                       cudaStream_t s)
+                       uint64_t limit_ns, bool skip_first, cudaStream_t s)
 {
     const int smem = 128 + S * B;
-    cudaFuncSetAttribute(probe_bulk_kernel<B, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    probe_bulk_kernel<B, S><<<grid, 32, smem, s>>>(static_cast<const uint4 *>(buf), n16, sink);
+    cudaFuncSetAttribute(mbg_probe_bulk_kernel<B, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    mbg_probe_bulk_kernel<B, S><<<grid, 32, smem, s>>>(static_cast<const uint4 *>(buf), n16, sink, limit_ns,
+                                                       skip_first ? 1 : 0);
 }
 
 template <int THREADS, int U>
 void launch_probe_tile(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
-                       cudaStream_t s)
+                       uint64_t, bool, cudaStream_t s)
 {
-    probe_tile_kernel<THREADS, U><<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
+    mbg_probe_tile_kernel<THREADS, U><<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
 }
 
 template <int THREADS, int U, int SEGMENT>
 void launch_probe(const void *buf, size_t n16, unsigned long long *sink, unsigned grid,
-                  cudaStream_t s)
+                  uint64_t, bool, cudaStream_t s)
 {
-    probe_read_kernel<THREADS, U, SEGMENT>
+    mbg_probe_read_kernel<THREADS, U, SEGMENT>
         <<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(buf), n16, sink);
 }
 

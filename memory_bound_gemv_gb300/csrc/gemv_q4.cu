@@ -7,6 +7,15 @@
 namespace mbg {
 
 static const Variant kTableQ4[] = {
+    // row bands, x in registers: band_t<threads>_c<chunks per thread>_u<rows in flight>
+    // (rows of exactly threads * chunks 16-byte chunks)
+    MBG_BAND(DT_Q4, 128, 1, 12, 4, "band_t128_c1_u12"),
+    MBG_BAND(DT_Q4, 128, 1, 16, 3, "band_t128_c1_u16"),
+    MBG_BAND(DT_Q4, 128, 1, 24, 2, "band_t128_c1_u24"),
+    MBG_BAND(DT_Q4, 64, 2, 8, 6, "band_t64_c2_u8"),
+    MBG_BAND(DT_Q4, 448, 1, 12, 1, "band_t448_c1_u12"),
+    MBG_BAND(DT_Q4, 448, 1, 8, 1, "band_t448_c1_u8"),
+    MBG_BAND(DT_Q4, 224, 2, 8, 1, "band_t224_c2_u8"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
     // given row length the first that fits is the automatic choice

@@ -36,7 +36,7 @@ __device__ __forceinline__ float load_w(const QuantArgs &p, int64_t k)
 }
 
 template <int QMAX, bool F16IN, bool PACK4>
-__global__ void __launch_bounds__(256) quantize_kernel(const QuantArgs p)
+__global__ void __launch_bounds__(256) mbg_quantize_kernel(const QuantArgs p)
 {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantArgs p)
 template <int QMAX, bool PACK4>
 void launch_q(const QuantArgs &p, bool f16in, unsigned blocks, cudaStream_t s)
 {
-    if (f16in) quantize_kernel<QMAX, true, PACK4><<<blocks, 256, 0, s>>>(p);
-    else quantize_kernel<QMAX, false, PACK4><<<blocks, 256, 0, s>>>(p);
+    if (f16in) mbg_quantize_kernel<QMAX, true, PACK4><<<blocks, 256, 0, s>>>(p);
+    else mbg_quantize_kernel<QMAX, false, PACK4><<<blocks, 256, 0, s>>>(p);
 }
 
 }  // namespace

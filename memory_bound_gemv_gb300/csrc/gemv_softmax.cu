@@ -3,7 +3,7 @@
 // combined with the online update m' = max(m, m2), d' = d e^(m - m') +
 // d2 e^(m2 - m')), and a copy probe for its read + write ceiling.
 //
-// softmax_vec_kernel: a row is read once into registers (16-byte loads; the
+// mbg_softmax_vec_kernel: a row is read once into registers (16-byte loads; the
 // persistent grid loads the next row while it finishes the current one), each
 // thread keeps exp(x_j - m_t) for its own maximum m_t and its partial sum,
 // the (max, sum) pairs are combined across the warp, the block and -- for
@@ -12,7 +12,7 @@
 // read and one write per element (the page's version re-reads the row through
 // L2 for a second pass; with the row in registers there is no second read).
 //
-// softmax_bulk_kernel: the same single read and write, with the row segments
+// mbg_softmax_cluster_kernel: the same single read and write, with the row segments
 // staged by bulk async copies into a ring of shared-memory buffers instead of
 // register prefetch, so a persistent grid of blocks (or clusters) keeps the
 // next rows in flight without spending registers on them.  Each thread keeps
@@ -20,7 +20,7 @@
 // exchange per row (one barrier of the block or cluster), which also frees
 // the row's buffer for the next copy.
 //
-// softmax_elem_kernel: any layout or length.  One block per row, the page's
+// mbg_softmax_elem_kernel: any layout or length.  One block per row, the page's
 // two passes: the online update over the row, then exp(x - m) / d re-reading
 // the row.
 #include <cooperative_groups.h>
@@ -114,7 +114,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 // persistent grid keeps reads in flight while it finishes a row.  All CTAs of
 // a cluster walk the same rows, so they meet the same cluster barriers.
 template <int T, int EPT, int C>
-__global__ void __launch_bounds__(T) softmax_vec_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N)
+__global__ void __launch_bounds__(T) mbg_softmax_vec_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N)
 {
     constexpr int VPT = EPT / 8;  // 16-byte vectors per thread
     __shared__ MaxSum red[33];
@@ -315,8 +315,9 @@ __host__ __device__ constexpr int softmax_bulk_smem(int T, int EPT, int C, int N
 // the status word and the block's abort flag; the block then runs on without
 // writing y, so that the barriers of the cluster still match.
 template <int T, int EPT, int C, int NB, bool PAIR>
-__global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N,
-                                                         unsigned int *err, uint64_t wait_limit_ns)
+__global__ void __launch_bounds__(T) mbg_softmax_cluster_kernel(const uint16_t *x, uint16_t *y, int64_t M, int N,
+                                                         unsigned int *err, uint64_t wait_limit_ns,
+                                                         unsigned int skip)
 {
     constexpr int VPT = EPT / 8;
     constexpr int NW = T / 32;
@@ -347,17 +348,18 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
     uint32_t issued[NB], pending[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) issued[b] = pending[b] = 0;
-    auto issue = [&](int64_t row, int b) {
+    auto issue = [&](int64_t row, int b, bool skip_copy) {
         const uint32_t bar = smem_addr(&full[b]);
         mbar_arrive_expect_tx(bar, seg_bytes);
-        bulk_copy_g2s(smem_addr(bufs + b * SEGE * 2), x + row * N + seg0, seg_bytes, bar);
         ++issued[b];
+        if (skip_copy) return;  // test hook: armed, never filled, so the wait runs out
+        bulk_copy_g2s(smem_addr(bufs + b * SEGE * 2), x + row * N + seg0, seg_bytes, bar);
         pending[b] = 1;
     };
     if (tid == 0 && seg_bytes) {
         for (int b = 0; b < NB; ++b) {
             const int64_t row = cid + b * ncl;
-            if (row < M) issue(row, b);
+            if (row < M) issue(row, b, b == 0 && (skip & SKIP_SEGMENT));
         }
     }
 
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
         if constexpr (!PAIR) {
             // every thread has read buffer b: refill it with a later row
             __syncthreads();
-            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b);
+            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b, false);
         }
         // this thread's maximum (on binary16 pairs, then one conversion)
         __half2 hm = __halves2half2(__ushort_as_half(0xFC00u), __ushort_as_half(0xFC00u));
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
         if constexpr (PAIR) {
             // one exchange per row; after it every thread has read buffer b
             const MaxSum tot = row_exchange<T, C>(MaxSum{mt, d}, slots + static_cast<int>(i & 1) * (C * NW), rank);
-            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b);
+            if (tid == 0 && seg_bytes && !*abort_flag && row + NB * ncl < M) issue(row + NB * ncl, b, false);
             inv = (mt == -INFINITY) ? 0.f : exp_approx(mt - tot.m) / tot.d;
         } else {
             inv = 1.f / row_reduce<T, C, false>(d, sl + C * NW, rank);
@@ -442,15 +444,17 @@ __global__ void __launch_bounds__(T) softmax_bulk_kernel(const uint16_t *x, uint
     }
     if (tid == 0 && *abort_flag) {
         // copies issued for rows this block did not take may still land
+        bool drained = true;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
-            if (pending[b]) mbar_wait_bounded(smem_addr(&full[b]), (issued[b] - 1) & 1u, wait_limit_ns);
+            if (pending[b]) drained &= mbar_wait_bounded(smem_addr(&full[b]), (issued[b] - 1) & 1u, wait_limit_ns);
+        if (!drained) report_error(err, DEVERR_UNDRAINED);
     }
 }
 
 // Any layout, any length: one block per row, two passes over the row.
 template <int T>
-__global__ void __launch_bounds__(T) softmax_elem_kernel(const uint16_t *x, uint16_t *y, int64_t N)
+__global__ void __launch_bounds__(T) mbg_softmax_elem_kernel(const uint16_t *x, uint16_t *y, int64_t N)
 {
     __shared__ MaxSum red[33];
     const int64_t row = blockIdx.x;
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(T) softmax_elem_kernel(const uint16_t *x, uint
 // ---------------------------------------------------------------------------
 
 template <int THREADS, int U>
-__global__ void __launch_bounds__(THREADS) probe_copy_kernel(const uint4 *src, uint4 *dst, size_t n16)
+__global__ void __launch_bounds__(THREADS) mbg_probe_copy_kernel(const uint4 *src, uint4 *dst, size_t n16)
 {
     const size_t tile = static_cast<size_t>(THREADS) * U;
     for (size_t t0 = static_cast<size_t>(blockIdx.x) * tile; t0 < n16; t0 += static_cast<size_t>(gridDim.x) * tile) {
@@ -524,7 +528,7 @@ int count_resident_clusters(int dev)
     int n = 0;
     if constexpr (C == 1) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, softmax_vec_kernel<T, EPT, 1>, T, 0) ==
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mbg_softmax_vec_kernel<T, EPT, 1>, T, 0) ==
             cudaSuccess)
             n = per_sm * sms;
     } else {
@@ -538,7 +542,7 @@ int count_resident_clusters(int dev)
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, softmax_vec_kernel<T, EPT, C>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mbg_softmax_vec_kernel<T, EPT, C>, &cfg) != cudaSuccess) n = 0;
     }
     return n > 0 ? n : sms;
 }
@@ -562,7 +566,7 @@ cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N,
     if constexpr (C == 1) clusters = M < resident_clusters<T, EPT, C>() ? M : resident_clusters<T, EPT, C>();
     const unsigned grid = static_cast<unsigned>(clusters * C);
     if constexpr (C == 1) {
-        softmax_vec_kernel<T, EPT, 1><<<grid, T, 0, s>>>(x, y, M, N);
+        mbg_softmax_vec_kernel<T, EPT, 1><<<grid, T, 0, s>>>(x, y, M, N);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -576,7 +580,7 @@ cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N,
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, softmax_vec_kernel<T, EPT, C>, x, y, M, N);
+        return cudaLaunchKernelEx(&cfg, mbg_softmax_vec_kernel<T, EPT, C>, x, y, M, N);
     }
 }
 
@@ -584,20 +588,20 @@ cudaError_t launch_softmax_vec(const uint16_t *x, uint16_t *y, int64_t M, int N,
 // blocks), at most one per row.
 template <int T, int EPT, int C, int NB, bool PAIR>
 cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N, unsigned int *err,
-                                uint64_t wait_limit_ns, cudaStream_t s)
+                                uint64_t wait_limit_ns, unsigned int skip, cudaStream_t s)
 {
     constexpr int SMEM = softmax_bulk_smem(T, EPT, C, NB);
     static std::once_flag once[kSoftmaxMaxDevices];
     static int val[kSoftmaxMaxDevices];
     const int resident = per_device_once(once, val, [](int dev) {
         // raise the dynamic shared memory limit once per device, then ask for the occupancy
-        if (cudaFuncSetAttribute(softmax_bulk_kernel<T, EPT, C, NB, PAIR>,
+        if (cudaFuncSetAttribute(mbg_softmax_cluster_kernel<T, EPT, C, NB, PAIR>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
             return 0;
         int sms = 0, n = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if constexpr (C == 1) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, softmax_bulk_kernel<T, EPT, 1, NB, PAIR>, T,
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mbg_softmax_cluster_kernel<T, EPT, 1, NB, PAIR>, T,
                                                               SMEM) != cudaSuccess)
                 return 0;
             return n * sms;
@@ -613,7 +617,7 @@ cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, softmax_bulk_kernel<T, EPT, C, NB, PAIR>, &cfg) != cudaSuccess)
+            if (cudaOccupancyMaxActiveClusters(&n, mbg_softmax_cluster_kernel<T, EPT, C, NB, PAIR>, &cfg) != cudaSuccess)
                 return 0;
             return n;
         }
@@ -632,12 +636,13 @@ cudaError_t launch_softmax_bulk(const uint16_t *x, uint16_t *y, int64_t M, int N
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = C > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, softmax_bulk_kernel<T, EPT, C, NB, PAIR>, x, y, M, N, err, wait_limit_ns);
+    return cudaLaunchKernelEx(&cfg, mbg_softmax_cluster_kernel<T, EPT, C, NB, PAIR>, x, y, M, N, err, wait_limit_ns,
+                              skip);
 }
 
 template <int T, int EPT, int C>
 cudaError_t launch_softmax_vec_v(const uint16_t *x, uint16_t *y, int64_t M, int N, unsigned int *,
-                                 uint64_t, cudaStream_t s)
+                                 uint64_t, unsigned int, cudaStream_t s)
 {
     return launch_softmax_vec<T, EPT, C>(x, y, M, N, s);
 }
@@ -646,7 +651,7 @@ struct SoftmaxVariant {
     int threads, ept, cluster;
     const char *name;
     cudaError_t (*launch)(const uint16_t *, uint16_t *, int64_t, int, unsigned int *, uint64_t,
-                          cudaStream_t);
+                          unsigned int, cudaStream_t);
     int capacity() const { return threads * ept * cluster; }
 };
 
@@ -688,7 +693,8 @@ const char *softmax_variant_name(int v)
 // Chooses (variant < 0) or runs a given variant; returns a CUDA error, or
 // cudaErrorNotSupported when the variant cannot serve the shape.
 cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N, int variant,
-                           unsigned int *err, uint64_t wait_limit_ns, cudaStream_t s)
+                           unsigned int *err, uint64_t wait_limit_ns, unsigned int skip,
+                           cudaStream_t s)
 {
     const bool vec_ok = N % 8 == 0 && N <= (1 << 30) &&
                         (reinterpret_cast<uintptr_t>(x) % 16) == 0 &&
@@ -707,10 +713,10 @@ cudaError_t launch_softmax(const uint16_t *x, uint16_t *y, int64_t M, int64_t N,
     if (variant < kSoftmaxVariants) {
         const SoftmaxVariant &v = kSoftmax[variant];
         if (!vec_ok || N > v.capacity()) return cudaErrorNotSupported;
-        return v.launch(x, y, M, static_cast<int>(N), err, wait_limit_ns, s);
+        return v.launch(x, y, M, static_cast<int>(N), err, wait_limit_ns, skip, s);
     }
     if (M > 0x7fffffffLL) return cudaErrorNotSupported;
-    softmax_elem_kernel<256><<<static_cast<unsigned>(M), 256, 0, s>>>(x, y, N);
+    mbg_softmax_elem_kernel<256><<<static_cast<unsigned>(M), 256, 0, s>>>(x, y, N);
     return cudaGetLastError();
 }
 
@@ -723,7 +729,7 @@ struct CopyVariant {
 template <int THREADS, int U>
 void launch_copy(const void *src, void *dst, size_t n16, unsigned grid, cudaStream_t s)
 {
-    probe_copy_kernel<THREADS, U>
+    mbg_probe_copy_kernel<THREADS, U>
         <<<grid, THREADS, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16);
 }
 

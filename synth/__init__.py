@@ -37,8 +37,10 @@ two's-complement code of a value in [-8, 7].
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 from typing import Dict, Optional, Tuple
 
 import numpy as np
@@ -230,7 +232,7 @@ SOFTMAX_WORKLOADS: Dict[str, Workload] = {
 }
 
 
-def _draw(dist: Tuple, seed: int, tag: int, start: int, count: int) -> np.ndarray:
+def _draw_serial(dist: Tuple, seed: int, tag: int, start: int, count: int) -> np.ndarray:
     kind = dist[0]
     if kind == "uniform":
         return uniform(seed, tag, start, count, dist[1], dist[2])
@@ -239,6 +241,42 @@ def _draw(dist: Tuple, seed: int, tag: int, start: int, count: int) -> np.ndarra
     if kind == "int":
         return integers(seed, tag, start, count, dist[1], dist[2])
     raise ValueError(f"unknown distribution {dist!r}")
+
+
+_PARALLEL_MIN = 1 << 23  # elements; smaller draws stay on one thread
+
+
+def _host_threads() -> int:
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(32, n))
+
+
+def _draw(dist: Tuple, seed: int, tag: int, start: int, count: int,
+          parallel: bool = True) -> np.ndarray:
+    """``count`` values of ``dist`` from stream positions ``start..``.
+
+    Every output depends only on (seed, tag, position), so large draws are
+    split into position ranges filled by several threads (numpy releases the
+    interpreter lock inside its array loops); the values are the same as on
+    one thread."""
+    nthreads = _host_threads()
+    if not parallel or count < _PARALLEL_MIN or nthreads == 1:
+        return _draw_serial(dist, seed, tag, start, count)
+    first = _draw_serial(dist, seed, tag, start, min(count, _CHUNK))
+    out = np.empty(count, dtype=first.dtype)
+    out[:first.size] = first
+    pieces = [(off, min(_CHUNK, count - off)) for off in range(first.size, count, _CHUNK)]
+
+    def fill(piece):
+        off, n = piece
+        out[off:off + n] = _draw_serial(dist, seed, tag, start + off, n)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=nthreads) as ex:
+        list(ex.map(fill, pieces))
+    return out
 
 
 def _encode_rows(dtype: str, vals: np.ndarray, nrows: int, N: int) -> np.ndarray:
@@ -253,7 +291,7 @@ def _encode_rows(dtype: str, vals: np.ndarray, nrows: int, N: int) -> np.ndarray
     raise ValueError(dtype)
 
 
-def weight_rows(w: Workload, row0: int, nrows: int) -> np.ndarray:
+def weight_rows(w: Workload, row0: int, nrows: int, parallel: bool = True) -> np.ndarray:
     """Rows ``row0 .. row0+nrows-1`` of A in storage format.
 
     f32 -> float32 [n, N]; f16 -> uint16 bits [n, N]; q8 -> int8 [n, N];
@@ -261,7 +299,21 @@ def weight_rows(w: Workload, row0: int, nrows: int) -> np.ndarray:
     """
     if w.dtype == "q4" and w.N % 2:
         raise ValueError("int4 rows need an even column count")
-    vals = _draw(w.a_dist, w.seed, TAG_A, row0 * w.N, nrows * w.N)
+    if parallel and nrows > 1 and nrows * w.N >= _PARALLEL_MIN and _host_threads() > 1:
+        # row blocks drawn and encoded on several threads (same values)
+        nt = _host_threads()
+        step = max(1, -(-nrows // (4 * nt)))
+        blocks = [(r, min(step, nrows - r)) for r in range(0, nrows, step)]
+        parts = [None] * len(blocks)
+
+        def fill(k):
+            r, n = blocks[k]
+            parts[k] = weight_rows(w, row0 + r, n, parallel=False)
+
+        with concurrent.futures.ThreadPoolExecutor(max_workers=nt) as ex:
+            list(ex.map(fill, range(len(blocks))))
+        return np.concatenate(parts, axis=0)
+    vals = _draw(w.a_dist, w.seed, TAG_A, row0 * w.N, nrows * w.N, parallel=parallel)
     return _encode_rows(w.dtype, vals, nrows, w.N)
 
 

@@ -57,26 +57,21 @@ def test_every_variant_small_shapes(dtype):
     assert checked > 0
 
 
-def _sample_rows(M, n=96, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set([0, 1, M // 2, M - 2, M - 1]) | set(rng.integers(0, M, n).tolist())
-    return sorted(r for r in rows if 0 <= r < M)
-
-
 @pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
 def test_workloads_full_size(name):
-    """The named workloads at full size: every row of the small one, sampled rows else."""
+    """The named workloads at full size, every row against the oracle, for the
+    automatic choice and every row-tile, bulk-pipeline, row-band and
+    warp-per-row variant that fits the workload."""
     w = synth.WORKLOADS[name]
     inp = synth.make(w)
     t = upload(w.dtype, inp)
-    rows = None if w.M * w.N <= 1024 * 1024 else _sample_rows(w.M, seed=w.seed)
-    y_ref, den = reference(w.dtype, inp, w.M, w.N, rows=rows)
+    y_ref, den = reference(w.dtype, inp, w.M, w.N, threads=16)
     y = mbg.gemv(w.dtype, t["A"], t["x"], t.get("scales"))
     torch.cuda.synchronize()
     y_np = y.cpu().numpy()
-    y_sel = y_np if rows is None else y_np[rows]
-    assert_close(w.dtype, y_sel, y_ref, den, f"{name} auto")
-    # every tile variant and the warp-per-row variants that fit this workload
+    assert y_np.shape == (w.M,)
+    assert_close(w.dtype, y_np, y_ref, den, f"{name} auto")
+    checked = 0
     for v in mbg.variants(w.dtype):
         if v["kind"] == "elem" or (v["kind"] == "vec" and v["threads_per_row"] != 32):
             continue
@@ -86,10 +81,55 @@ def test_workloads_full_size(name):
             assert e.status == mbg.ERR_UNSUPPORTED
             continue
         torch.cuda.synchronize()
-        y2 = y2.cpu().numpy()
-        assert_close(w.dtype, y2 if rows is None else y2[rows], y_ref, den, f"{name} {v['name']}")
+        assert_close(w.dtype, y2.cpu().numpy(), y_ref, den, f"{name} {v['name']}")
+        checked += 1
+    assert checked > 0
     # outputs are finite everywhere
     assert np.all(np.isfinite(y_np))
+    assert mbg.gemv_get_device_error() == mbg.OK
+
+
+@pytest.mark.parametrize("N", (4096, 14336))
+def test_int8_code_minus_128(N):
+    """INT8 codes span the whole byte, -128 included (the header admits it;
+    the workload recipe draws only -127..127)."""
+    M = 64
+    A = synth.integers(77, 1, 0, M * N, -128, 127).astype(np.int8).reshape(M, N)
+    A[::7, ::5] = -128
+    scales = synth.to_f16_bits(synth.uniform(77, 3, 0, M * synth.n_groups(N), 0.001, 0.01)).reshape(M, -1)
+    x = synth.to_f16_bits(synth.normal(77, 2, 0, N, 1.0))
+    inp = {"A": A, "x": x, "scales": scales}
+    y_ref, den = reference("q8", inp, M, N)
+    t = upload("q8", inp)
+    checked = 0
+    for v in mbg.variants("q8"):
+        try:
+            y = mbg.gemv_run_variant("q8", v["id"], t["A"], t["x"], t["scales"])
+        except mbg.GemvError as e:
+            assert e.status == mbg.ERR_UNSUPPORTED
+            continue
+        torch.cuda.synchronize()
+        assert_close("q8", y.cpu().numpy(), y_ref, den, f"q8 -128 {v['name']}")
+        checked += 1
+    assert checked > 5
+    # -128 on the diagonal with unit scales: y = -128 x exactly (exact in FP32)
+    n = N
+    eye = np.zeros((n // 8, n), dtype=np.int8)
+    eye[np.arange(n // 8), np.arange(n // 8) * 8] = -128
+    ones = np.full((n // 8, synth.n_groups(n)), 0x3C00, dtype=np.uint16)
+    t2 = upload("q8", {"A": eye, "x": x, "scales": ones})
+    expect = -128.0 * x.view(np.float16).astype(np.float64)[::8][: n // 8]
+    for v in mbg.variants("q8"):
+        try:
+            y = mbg.gemv_run_variant("q8", v["id"], t2["A"], t2["x"], t2["scales"])
+        except mbg.GemvError:
+            continue
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().astype(np.float64), expect), v["name"]
+    # dequantisation keeps -128 exact
+    W = mbg.gemv_dequant_q8(t["A"], t["scales"])
+    torch.cuda.synchronize()
+    assert np.array_equal(W.cpu().numpy().astype(np.float64), oracle.load().dequant("q8", A, scales, M, N))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -234,6 +274,154 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         y = mbg.gemv_run_variant(dtype, vid, t["A"], t["x"])
         assert mbg.gemv_get_device_error() == mbg.OK
         assert_close(dtype, y.cpu().numpy(), y_ref, den, "after timeout")
+
+
+def _timeout_then_recovery(run, check, mask):
+    """run() with the given skip hook and a 2 ms wait limit must report a
+    timeout (and no undrained copy); without the hook it must be correct."""
+    assert mbg.gemv_get_device_error() == mbg.OK
+    try:
+        mbg.debug_set_wait_limit_ns(2_000_000)
+        mbg.debug_skip_copies(mask)
+        run()
+        status = mbg.gemv_get_device_error()
+    finally:
+        mbg.debug_skip_copies(0)
+        mbg.debug_set_wait_limit_ns(0)
+    assert status == mbg.ERR_TIMEOUT, mbg.STATUS.get(status, status)
+    check(run())
+    assert mbg.gemv_get_device_error() == mbg.OK
+
+
+@pytest.mark.parametrize("dtype,M,N", [("q4", 300, 4096), ("q8", 300, 4096), ("q4", 37, 14336),
+                                       ("f16", 300, 4096)])
+def test_bulk_pipeline_stage_wait_runs_out(dtype, M, N):
+    """Every bulk-pipeline variant: the first weight stage of every block is
+    armed but never copied; the consumers give up, the producer gives up on
+    the reduced-stage barrier, drains its other stages and the block exits."""
+    inp = synth.make(synth.random_case(dtype, M, N, 515 + M))
+    t = upload(dtype, inp)
+    y_ref, den = reference(dtype, inp, M, N)
+    ran = 0
+    for v in mbg.variants(dtype):
+        if v["kind"] != "bulk":
+            continue
+        try:
+            mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], t.get("scales"))
+        except mbg.GemvError as e:
+            assert e.status == mbg.ERR_UNSUPPORTED
+            continue
+        torch.cuda.synchronize()
+
+        def run(vid=v["id"]):
+            return mbg.gemv_run_variant(dtype, vid, t["A"], t["x"], t.get("scales"))
+
+        def check(y, name=v["name"]):
+            torch.cuda.synchronize()
+            assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{name} after timeout")
+
+        _timeout_then_recovery(run, check, mbg.SKIP_STAGE)
+        ran += 1
+    assert ran > 0
+
+
+def test_softmax_segment_wait_runs_out():
+    """Softmax kernels that stage rows by bulk copies, single blocks and
+    clusters of 2 to 8: the first segment copy of every block is skipped; the
+    blocks give up, keep meeting the cluster barriers, write nothing and exit."""
+    names = mbg.softmax_variants()
+    orc = oracle.load()
+    ran = set()
+    for vid, name in enumerate(names):
+        if not name.startswith("smb_"):
+            continue
+        T = int(name.split("_t")[1].split("_")[0])
+        E = int(name.split("_e")[1].split("_")[0])
+        C = int(name.split("_c")[1].split("_")[0])
+        N = T * E * C
+        M = 12
+        bits = synth.to_f16_bits(synth.normal(600 + vid, 1, 0, M * N, 2.0)).reshape(M, N)
+        x = torch.from_numpy(bits.view(np.float16)).cuda()
+        ref = orc.softmax(bits, M, N)
+
+        def run(v=vid, x=x):
+            return mbg.gemv_softmax_f16(x, variant=v)
+
+        def check(y, ref=ref, name=name):
+            torch.cuda.synchronize()
+            got = y.cpu().numpy().astype(np.float64)
+            err = float(np.max(np.abs(got - ref) / np.maximum(ref, 1e-4)))
+            assert err <= 1e-3, (name, err)
+
+        _timeout_then_recovery(run, check, mbg.SKIP_SEGMENT)
+        ran.add(C)
+    assert {1, 2, 8} <= ran
+
+
+def test_bulk_probe_wait_runs_out():
+    """Bulk-copy probe patterns: the first chunk of every block is skipped; the
+    probe sets bit 63 of the sink (not bit 62: nothing was left in flight)."""
+    rng = np.random.default_rng(8)
+    words = rng.integers(0, 2 ** 32, size=(4 << 20) // 4, dtype=np.uint64).astype(np.uint32)
+    expect = int(np.bitwise_xor.reduce(words))
+    buf = torch.from_numpy(words.view(np.int32)).cuda()
+    ran = 0
+    for v, name in enumerate(mbg.probe_variants()):
+        if not name.startswith("bulk"):
+            continue
+        sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+        try:
+            mbg.debug_set_wait_limit_ns(2_000_000)
+            mbg.debug_skip_copies(mbg.SKIP_PROBE)
+            mbg.gemv_probe_read(buf, sink, v)
+            torch.cuda.synchronize()
+        finally:
+            mbg.debug_skip_copies(0)
+            mbg.debug_set_wait_limit_ns(0)
+        word = int(sink.item()) & 0xFFFFFFFFFFFFFFFF
+        assert (word >> 63) & 1 == 1 and (word >> 62) & 1 == 0, (name, hex(word))
+        sink.zero_()
+        mbg.gemv_probe_read(buf, sink, v)
+        torch.cuda.synchronize()
+        assert int(sink.item()) == expect, name
+        ran += 1
+    assert ran > 0
+
+
+def test_host_call_waits_for_a_kernel_that_writes_the_weights():
+    """gemv_ex_host without the overlap flag: the kernel before the call
+    lets its successor start at once but writes A only later; the GEMV must
+    see the written A (the copy of x waits for that kernel before it lets the
+    GEMV start)."""
+    L = mbg.lib()
+    for dtype, M, N in (("f16", 2048, 4096), ("q4", 1024, 4096)):
+        w = synth.random_case(dtype, M, N, 707)
+        inp = synth.make(w)
+        if dtype == "f16":
+            A_final = np.full((M, N), 0x3C00, dtype=np.uint16)   # all ones
+            word = 0x3C003C00
+        else:
+            A_final = np.full((M, N // 2), 0x11, dtype=np.uint8)  # every code 1
+            word = 0x11111111
+        inp_final = dict(inp, A=A_final)
+        y_ref, den = reference(dtype, inp_final, M, N)
+        t = upload(dtype, inp)
+        A_dev = torch.zeros_like(t["A"])  # zero until the late kernel writes it
+        x_np = inp["x"]
+        x_host = torch.from_numpy(np.ascontiguousarray(x_np).view(np.float16)).pin_memory()
+        x_dev = torch.empty_like(t["x"])
+        y_host = torch.full((M,), np.nan, dtype=torch.float32).pin_memory()
+        s_ptr = t["scales"].data_ptr() if "scales" in t else None
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            A_dev.zero_()
+            mbg.debug_late_fill(A_dev, word, 200_000, stream=s)
+            st = L.gemv_ex_host(mbg.DTYPES[dtype], A_dev.data_ptr(), x_host.data_ptr(), x_dev.data_ptr(),
+                                y_host.data_ptr(), M, N, s_ptr, 0, s.cuda_stream)
+            assert st == mbg.OK, mbg.status_string(st)
+            s.synchronize()
+            assert_close(dtype, y_host.numpy().copy(), y_ref, den, f"{dtype} after a late write")
+    assert mbg.gemv_get_device_error() == mbg.OK
 
 
 def test_runs_on_a_side_stream():
