@@ -172,13 +172,15 @@ gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t
  * The copy of x is a small kernel that reads the host buffer over the
  * CPU-GPU link; it is launched with programmatic dependent launch (its blocks
  * are scheduled while the preceding kernel drains) and reads x only after
- * that kernel has completed.  The GEMV is launched the same way after it, so
- * it streams its weights while x is still being fetched.
- * GEMV_FLAG_OVERLAP_PRECEDING: additionally, the kernel that precedes the
- * call on `stream` writes neither A, scales nor x_host (a previous call of
- * this function qualifies); the copy then reads x_host before that kernel has
- * finished and writes x_dev only after it.  x_host must not change until the
- * call has run on the stream.
+ * that kernel has completed.  The GEMV is launched the same way after it and
+ * waits for the copy to complete before it reads A, scales or x, so the call
+ * keeps the ordering of plain launches.
+ * GEMV_FLAG_OVERLAP_PRECEDING: the kernel that precedes the call on `stream`
+ * writes neither A, scales nor x_host (a previous call of this function
+ * qualifies); the copy then reads x_host before that kernel has finished and
+ * writes x_dev only after it, and the GEMV streams its weights while x is
+ * still being fetched.  x_host must not change until the call has run on the
+ * stream.
  * Same results as gemv_ex on device copies of x (bit for bit).
  * The pages time device-resident operands only; this call has no
  * counterpart there.
@@ -312,27 +314,31 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
  * threads_per_row = consumer threads of the block, plus one producer warp);
  * 4 = row bands: for rows of exactly threads_per_row * unroll 16-byte chunks,
  * each thread keeps the x of its chunks in registers and a window of
- * rows_per_group rows in flight; block b of the persistent grid takes rows
- * b, b + grid, b + 2 grid, ...
+ * rows_per_group rows in flight in registers; tiles of consecutive rows are
+ * dealt to the blocks of a persistent grid in grid-stride order;
+ * 5 = staged row bands: the same work split, with the tiles streamed into a
+ * ring of shared-memory stages by bulk async copies (rows_per_group = rows
+ * per window of tiles).
  */
 typedef struct {
     int dtype;           /* gemv_dtype_t */
     int kind;            /* kernel family, see above */
     int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1),
-                            the consumer threads of the block (family 3), the block (family 4) */
+                            the consumer threads of the block (family 3), the block (families 4, 5) */
     int rows_per_group;  /* rows one lane group streams together (family 0, x reuse); rows per
-                            stage (family 3); rows in flight per thread (family 4) */
+                            stage (family 3); rows in flight per thread (family 4), rows per
+                            window (family 5) */
     int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread;
                             family 3: chunks per consumer thread and row when the variant is
                             specialised for rows of exactly unroll * threads_per_row chunks
-                            (0: any row length); family 4: chunks per thread and row */
+                            (0: any row length); families 4, 5: chunks per thread and row */
     int warps;           /* warps per block */
     int math;            /* 0: operands converted to FP32; 1: binary16 operands into
                             mixed-precision FMAs with FP32 accumulation */
     int xmode;          /* 0: x copied to shared memory by a bulk async copy,
                            1: x copied to shared memory by vector loads,
                            2: x read through the L1 cache, 3: element-wise kernel,
-                           4: x held in registers (family 4) */
+                           4: x held in registers (families 4, 5) */
     char name[48];
 } gemv_variant_info_t;
 

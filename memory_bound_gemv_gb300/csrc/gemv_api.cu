@@ -158,6 +158,11 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N, int64_t groups)
         return static_cast<size_t>(L.total);
     }
     if (v.kind == KIND_BAND) return 0;  // x in registers, static shared memory only
+    if (v.kind == KIND_SBAND) {
+        const StageBandLayout L = stageband_layout(v.stages, v.rows_per_group, v.warps, v.tile_rows,
+                                                   row_bytes_of(dtype, N), groups, is_quant(dtype));
+        return static_cast<size_t>(L.total);
+    }
     if (v.xmode == XMODE_BULK || v.xmode == XMODE_VEC)
         return static_cast<size_t>(v.x_offset) + static_cast<size_t>(N) * x_elem_bytes(dtype);
     if (v.kind == KIND_TILE) return static_cast<size_t>(v.x_offset);
@@ -192,6 +197,14 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
     if (v.kind == KIND_BAND) {
         // every thread takes exactly `unroll` chunks of each row
         return rb / 16 == static_cast<int64_t>(v.lanes_per_row) * v.unroll;  // persistent grid
+    }
+    if (v.kind == KIND_SBAND) {
+        if (rb / 16 != static_cast<int64_t>(v.lanes_per_row) * v.unroll) return false;
+        // a tile's scales are one bulk copy: 16-byte aligned rows of scales
+        if (is_quant(dtype) && ((2 * groups) % 16 || !aligned(scales, 16))) return false;
+        // one stage is one transaction count of an mbarrier
+        const int64_t tx = v.tile_rows * (rb + (is_quant(dtype) ? 2 * groups : 0));
+        return tx < (1 << 20);  // persistent grid
     }
     if (v.kind == KIND_TILE) {
         // every row must be covered by one request per thread
@@ -236,6 +249,8 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
 
 // The automatic choice (measured on GB300 over the workload families):
 // - layouts the vector kernels cannot take: element-wise kernel;
+// - FP32 and FP16 rows that a row-band variant covers exactly (x in
+//   registers): the first such variant in table order (measured best first);
 // - INT8, and INT4 rows of at least 4 KB: the bulk-copy pipeline, with
 //   8-16 KB of rows per stage;
 // - otherwise row tiles with the narrowest group that requests a whole row at
@@ -254,6 +269,11 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if (!vec_ok) return find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     const int64_t chunks = rb / 16;
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
+    if (dtype == DT_F32 || dtype == DT_F16) {
+        for (int k = 0; k < n; ++k) {
+            if (v[k].kind == KIND_BAND && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
+        }
+    }
     // the quantised types are bound by instruction issue: the bulk-copy
     // pipeline (no load instructions for A) wins.  A variant specialised for
     // exactly this row length (a fixed chunk count per consumer thread) comes
@@ -371,7 +391,7 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
         blocks = (M + v.warps - 1) / v.warps;
     } else {
         blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
-        if (v.kind == KIND_TILE || v.kind == KIND_BULK || v.kind == KIND_BAND) {
+        if (v.kind == KIND_TILE || v.kind == KIND_BULK || v.kind == KIND_BAND || v.kind == KIND_SBAND) {
             const int resident = resident_blocks(*d, dtype, vid, v, smem);
             if (resident <= 0) return GEMV_ERR_CUDA;
             if (blocks > resident) blocks = resident;
@@ -469,9 +489,11 @@ gemv_status_t gemv_ex_host(int dtype, const void *A, const void *x_host, void *x
                    static_cast<cudaStream_t>(stream));
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, GEMV_ERR_LAUNCH);
-    // the GEMV never writes what the copy reads, and reads x only after the
-    // copy has completed (griddepcontrol.wait): it may always overlap it
-    return run(dtype, -1, A, x_dev, y, M, N, scales, stream, GEMV_FLAG_OVERLAP_PRECEDING);
+    // the GEMV waits for the copy (griddepcontrol.wait) before it reads x;
+    // it streams weights before that wait only under the caller's promise
+    // that the kernel before this call leaves them alone (the copy itself
+    // never writes them)
+    return run(dtype, -1, A, x_dev, y, M, N, scales, stream, flags);
 }
 
 gemv_status_t gemv_ex(int dtype, const void *A, const void *x, float *y, int64_t M, int64_t N,

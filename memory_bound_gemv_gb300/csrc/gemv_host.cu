@@ -10,12 +10,14 @@
 // only writes the device buffer after it.  The GEMV after it starts
 // streaming its weights while x is still in flight.
 //
-// Ordering.  The GEMV after the copy is launched with programmatic
-// dependent launch and loads weights before its own wait, which only orders
-// it after the copy kernel.  So unless the caller has promised that the
-// kernel before the call leaves the weights alone (early), every copy block
-// first waits for that kernel and only then lets the GEMV start: the GEMV's
-// blocks then begin after that kernel has completed, as with a plain launch.
+// Ordering.  The copy lets the GEMV after it start at once, and the GEMV
+// orders itself after the copy with its own wait (griddepcontrol.wait), which
+// returns only once the copy grid has completed -- and the copy completes
+// only after its own wait for the kernel before the call.  Unless the caller
+// has promised that the kernel before the call leaves the weights, scales and
+// x alone (early), the GEMV therefore touches no memory before that wait
+// (only L2 prefetch hints); with the promise it streams its weights at once
+// and reads x after the wait.
 #include "gemv_kernels.cuh"
 
 namespace mbg {
@@ -25,12 +27,8 @@ namespace {
 __global__ void __launch_bounds__(256) mbg_copy_in_kernel(const unsigned char *src, unsigned char *dst,
                                                       int64_t bytes, int vec, int early)
 {
-    if (early) {
-        pdl_trigger();
-    } else {
-        pdl_wait();
-        pdl_trigger();
-    }
+    pdl_trigger();
+    if (!early) pdl_wait();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n16 = vec ? bytes / 16 : 0;

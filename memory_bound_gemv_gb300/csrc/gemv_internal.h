@@ -16,8 +16,9 @@ enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3, XMODE_REG = 
 
 // Kernel families: warp/sub-warp rows streamed with a rolling buffer, row
 // tiles walked by a persistent grid, element-wise fallback, bulk-copy
-// pipeline, row bands with x in registers.
-enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3, KIND_BAND = 4 };
+// pipeline, row bands with x in registers (rows in flight in registers, or
+// staged in shared memory by bulk copies).
+enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3, KIND_BAND = 4, KIND_SBAND = 5 };
 
 // Dot-product arithmetic: operands converted to FP32, or binary16 operands
 // fed to mixed-precision FMAs with FP32 accumulation.
@@ -86,12 +87,16 @@ struct Variant {
     int math;            // MATH_F32 or MATH_MIXED
     int stages;          // bulk-pipeline depth (KIND_BULK)
     bool x_regs = false; // bulk pipeline keeps x in registers, not in shared memory
-    bool supports_pdl() const { return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND; }
+    int tile_rows = 1;   // row bands: consecutive rows per tile
+    bool supports_pdl() const
+    {
+        return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND || kind == KIND_SBAND;
+    }
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
         if (kind == KIND_BULK) return rows_per_group;
-        if (kind == KIND_BAND) return 1;  // one block per row at most
+        if (kind == KIND_BAND || kind == KIND_SBAND) return tile_rows;  // one block per tile at most
         return warps * (32 / lanes_per_row) * rows_per_group;
     }
 };
@@ -106,6 +111,25 @@ struct BulkLayout {
 };
 
 __host__ __device__ inline int round16(int64_t v) { return static_cast<int>((v + 15) / 16 * 16); }
+
+// Shared-memory layout of the staged row-band kernel (host and device agree
+// on it): S mbarriers, the warp partials [2][U][NW], then S stages of G rows
+// of A followed by their G rows of scales.
+struct StageBandLayout {
+    int part, stage, stage_bytes, scale_off, total;
+};
+
+__host__ __device__ inline StageBandLayout stageband_layout(int S, int U, int NW, int G, int64_t row_bytes,
+                                                           int64_t groups, bool quant)
+{
+    StageBandLayout L;
+    L.part = round16(8 * S);
+    L.stage = (L.part + 2 * U * NW * 4 + 127) / 128 * 128;
+    L.scale_off = static_cast<int>(G * row_bytes);
+    L.stage_bytes = L.scale_off + (quant ? round16(G * 2 * groups) : 0);
+    L.total = L.stage + S * L.stage_bytes;
+    return L;
+}
 
 __host__ __device__ inline BulkLayout bulk_layout(int S, int RS, int T, int64_t row_bytes,
                                                   int64_t x_bytes, int64_t groups, bool quant)

@@ -743,7 +743,12 @@ __device__ __forceinline__ void band_chunk(const uint4 a, const uint4 (&xv)[x_ch
                                            float &c0, float &c1)
 {
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-    if constexpr (DT == DT_F16) {
+    if constexpr (DT == DT_F32) {
+        c0 = fmaf(__uint_as_float(w[0]), __uint_as_float(xv[0].x), c0);
+        c1 = fmaf(__uint_as_float(w[1]), __uint_as_float(xv[0].y), c1);
+        c0 = fmaf(__uint_as_float(w[2]), __uint_as_float(xv[0].z), c0);
+        c1 = fmaf(__uint_as_float(w[3]), __uint_as_float(xv[0].w), c1);
+    } else if constexpr (DT == DT_F16) {
         mfma_pair_ordered(w[0], xv[0].x, c0, c1);
         mfma_pair_ordered(w[1], xv[0].y, c0, c1);
         mfma_pair_ordered(w[2], xv[0].z, c0, c1);
@@ -797,37 +802,92 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits)
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
 
-template <int DT, int T, int CPT, int U, int MINB>
+// 16-byte streaming load into registers that already hold the slot's
+// previous data (the same registers, so a rolling window needs no copies).
+__device__ __forceinline__ void ld_stream16_into(uint4 &v, const void *p)
+{
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void ld_u16_into(uint32_t &v, const void *p)
+{
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "+r"(v) : "l"(p));
+}
+
+// Sums U values (U a power of two, at most 32) over the 32 lanes of a warp:
+// afterwards lane l holds the warp sum of value l >> (5 - log2 U).  At each
+// of the first log2 U steps a lane keeps half of its values (the upper half
+// when its lane bit at that distance is set) and adds its partner's copy of
+// them (one shuffle per kept value); the remaining steps are a plain XOR
+// butterfly.  U - 1 + 5 - log2 U shuffles instead of 5 U.
+template <int U>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[U], int lane)
+{
+    static_assert(U >= 1 && U <= 32 && (U & (U - 1)) == 0, "U: a power of two up to 32");
+    float w[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) w[i] = v[i];
+    int d = 16;
+#pragma unroll
+    for (int k = U; k > 1; k >>= 1, d >>= 1) {
+        const bool up = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < k / 2; ++i) {
+            const float keep = up ? w[i + k / 2] : w[i];
+            const float send = up ? w[i] : w[i + k / 2];
+            w[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
+    float s = w[0];
+#pragma unroll
+    for (; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+    return s;
+}
+
+// G consecutive rows form a tile; tiles are dealt to blocks in grid-stride
+// order (tile b, b + grid, ...), TW tiles (U = G * TW rows) in flight per
+// thread.  Rows of a tile are ROWB bytes apart, so their addresses are
+// immediate offsets of one pointer per tile.
+template <int DT, int T, int CPT, int G, int TW, int MINB>
 __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
     constexpr int XV = x_chunk_vecs<DT>();
     constexpr int NW = T / 32;
+    constexpr int U = G * TW;           // rows in flight per thread
     constexpr int ROWB = T * CPT * 16;  // bytes per row
     constexpr bool PAIRED = DT == DT_Q4;
     static_assert(T % 32 == 0 && NW <= 32, "block shape");
-    static_assert(F::XB == 2, "binary16 x (mixed-precision products)");
+    static_assert(F::XB == 2 || DT == DT_F32, "binary16 x (mixed-precision products) or FP32");
+    static_assert((U & (U - 1)) == 0 && U <= 32, "rows in flight: a power of two up to 32");
 
     __shared__ float part[2][U][NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t grid = gridDim.x;
     const int64_t b = blockIdx.x;
-    // rows of this block: b + j * grid for 0 <= j < J
-    const int64_t J = b < p.M ? (p.M - 1 - b) / grid + 1 : 0;
+    const int64_t ntiles = (p.M + G - 1) / G;
+    // tiles of this block: b + i * grid for 0 <= i < I
+    const int64_t I = b < ntiles ? (ntiles - 1 - b) / grid + 1 : 0;
     const unsigned char *abase = static_cast<const unsigned char *>(p.A) + tid * 16;
 
     pdl_trigger();
-    // the first U rows of this block into L2 while the preceding kernel
+    // the first tiles of this block into L2 while the preceding kernel
     // drains (a hint only: it changes no value a later load returns)
-    if (tid < U && tid < J)
-        prefetch_l2(static_cast<const unsigned char *>(p.A) + (b + tid * grid) * ROWB, ROWB);
+    if (tid < TW && tid < I) {
+        const int64_t row0 = (b + tid * grid) * G;
+        const int64_t rows = p.M - row0 < G ? p.M - row0 : G;
+        prefetch_l2(static_cast<const unsigned char *>(p.A) + row0 * ROWB, static_cast<uint32_t>(rows * ROWB));
+    }
     if (!p.pdl) pdl_wait();
 
     // scale of chunk c of a row: scales[row * groups + (c >> scale_shift)]
     int soff[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) soff[k] = (tid + k * T) >> p.scale_shift;
+    const int64_t sgrp = p.groups;  // scales per row
 
     uint4 a[U][CPT];
     uint32_t sc[U][CPT];  // binary16 scale bits
@@ -838,29 +898,41 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
             a[r][k] = make_uint4(0u, 0u, 0u, 0u);
             sc[r][k] = 0u;
         }
-    // rows are loaded strictly in the order j = 0, 1, 2, ...: one pointer
-    // per operand walks them (grid rows apart)
-    int64_t jn = 0;
-    const unsigned char *an = abase + b * ROWB;
-    const int64_t astep = grid * ROWB;
-    const uint16_t *sn = F::QUANT ? p.scales + b * p.groups : nullptr;
-    const int64_t sstep = grid * p.groups;
-    auto load_next = [&](uint4 (&dst)[CPT], uint32_t (&sd)[CPT]) {
-        const bool ok = jn < J;
+    // tiles are loaded strictly in the order i = 0, 1, 2, ...: one pointer per
+    // operand walks them (grid tiles apart; both steps in bytes, advanced by
+    // a volatile add so that the compiler keeps no address per slot)
+    int64_t in = 0;
+    const unsigned char *an = abase + b * G * ROWB;
+    const int64_t astep = grid * G * ROWB;
+    const unsigned char *sn = F::QUANT ? reinterpret_cast<const unsigned char *>(p.scales + b * G * sgrp) : nullptr;
+    const int64_t sstep = grid * G * sgrp * 2;
+    // FULL: the tile and all its rows exist (no predicates)
+    auto load_tile = [&](int w, auto full) {
+        constexpr bool FULL = decltype(full)::value;
+        const int64_t row0 = (b + in * grid) * G;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) ld_stream16_if(dst[k], an + k * T * 16, ok);
-        if constexpr (F::QUANT) {
+        for (int g = 0; g < G; ++g) {
+            const bool ok = FULL || (in < I && row0 + g < p.M);
 #pragma unroll
-            for (int k = 0; k < CPT; ++k) ld_u16_if(sd[k], sn + soff[k], ok);
-            asm volatile("add.s64 %0, %0, %1;" : "+l"(sn) : "l"(sstep));
+            for (int k = 0; k < CPT; ++k) {
+                if constexpr (FULL) ld_stream16_into(a[w * G + g][k], an + g * ROWB + k * T * 16);
+                else ld_stream16_if(a[w * G + g][k], an + g * ROWB + k * T * 16, ok);
+            }
+            if constexpr (F::QUANT) {
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) {
+                    const void *sp = sn + (g * sgrp + soff[k]) * 2;
+                    if constexpr (FULL) ld_u16_into(sc[w * G + g][k], sp);
+                    else ld_u16_if(sc[w * G + g][k], sp, ok);
+                }
+            }
         }
-        // advanced in place (volatile), so that the compiler does not keep
-        // one precomputed address per slot of the window
+        if constexpr (F::QUANT) asm volatile("add.s64 %0, %0, %1;" : "+l"(sn) : "l"(sstep));
         asm volatile("add.s64 %0, %0, %1;" : "+l"(an) : "l"(astep));
-        ++jn;
+        ++in;
     };
 #pragma unroll
-    for (int r = 0; r < U; ++r) load_next(a[r], sc[r]);
+    for (int w = 0; w < TW; ++w) load_tile(w, std::false_type{});
     if (p.pdl) pdl_wait();
 
     // this thread's x vectors (read after the wait: the preceding kernel may
@@ -881,42 +953,230 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
         }
     }
 
-    int half = 0;
-    for (int64_t j0 = 0; j0 < J; j0 += U) {
+    // the products of row slot r (rows of tiles that do not exist give
+    // values that are never stored)
+    auto row_dot = [&](int r) {
+        float acc = 0.f;
+        if constexpr (F::QUANT) {
 #pragma unroll
-        for (int r = 0; r < U; ++r) {
-            // row j0 + r is multiplied straight from its slot, then the slot
-            // is refilled in place with row j0 + U + r (no second window of
-            // registers; U - 1 rows stay in flight while a row is multiplied)
-            if (j0 + r < J) {
-                float acc = 0.f;
-                if constexpr (F::QUANT) {
-#pragma unroll
-                    for (int k = 0; k < CPT; ++k) {
-                        const float s = half_bits_to_float(sc[r][k]);
-                        float c0 = 0.f, c1 = 0.f;
-                        band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
-                        acc = fmaf(s, c0, acc);
-                        acc = fmaf(s, c1, acc);
-                    }
-                } else {
-                    float c0 = 0.f, c1 = 0.f;
-#pragma unroll
-                    for (int k = 0; k < CPT; ++k) band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
-                    acc = c0 + c1;
-                }
-                // this warp's share of row j0 + r, left for the block sum
-                acc = group_sum<32>(acc);
-                if (lane == 0) part[half][r][warp] = acc;
+            for (int k = 0; k < CPT; ++k) {
+                const float s = half_bits_to_float(sc[r][k]);
+                float c0 = 0.f, c1 = 0.f;
+                band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
+                acc = fmaf(s, c0, acc);
+                acc = fmaf(s, c1, acc);
             }
-            load_next(a[r], sc[r]);  // row j0 + U + r
-        }
-        __syncthreads();
-        if (tid < U && j0 + tid < J) {
-            float v = 0.f;
+        } else {
+            float c0 = 0.f, c1 = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) v += part[half][tid][w];
-            p.y[b + (j0 + tid) * grid] = v;
+            for (int k = 0; k < CPT; ++k) band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
+            acc = c0 + c1;
+        }
+        return acc;
+    };
+
+    int half = 0;
+    for (int64_t i0 = 0; i0 < I; i0 += TW) {
+        // every tile of this window and of the next one exists in full
+        const int64_t last = i0 + 2 * TW - 1;
+        const bool full = last < I && (b + last * grid) * G + G <= p.M;
+        float acc[U];
+        auto window = [&](auto fl) {
+#pragma unroll
+            for (int w = 0; w < TW; ++w) {
+                // rows of tile i0 + w are multiplied straight from their
+                // slots, which are then refilled in place with tile i0 + TW + w
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[w * G + g] = row_dot(w * G + g);
+                load_tile(w, fl);
+            }
+        };
+        if (full) window(std::true_type{});
+        else window(std::false_type{});
+        // lane l ends with the warp's share of row slot l >> (5 - log2 U)
+        const float s = warp_sum_rows<U>(acc, lane);
+        constexpr int LPR = 32 / U;  // lanes holding each row's sum
+        if ((lane & (LPR - 1)) == 0) part[half][lane / LPR][warp] = s;
+        __syncthreads();
+        if (tid < U) {
+            const int64_t i = i0 + tid / G;
+            const int64_t row = (b + i * grid) * G + tid % G;
+            if (i < I && row < p.M) {
+                float v = 0.f;
+#pragma unroll
+                for (int q = 0; q < NW; ++q) v += part[half][tid][q];
+                p.y[row] = v;
+            }
+        }
+        half ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Staged row-band kernel (x in registers, tiles of A staged by bulk copies)
+// ---------------------------------------------------------------------------
+//
+// The row-band kernel's work split (thread t multiplies chunks t, t + T, ...
+// of every row with x held in registers; tiles of G consecutive rows dealt
+// to blocks in grid-stride order), but the tiles reach the block through a
+// ring of 2 TW shared-memory stages filled by bulk async copies, so the bytes
+// in flight cost no registers.  Thread 0 issues the copies; everybody reads
+// the stage (one 16-byte shared load per chunk and row).  The block barrier
+// that closes each window of TW tiles (after the warp partials are written)
+// also tells thread 0 that the window's stages have been read, and it
+// refills them with the tiles 2 TW ahead.  Every wait is bounded: a thread
+// whose wait gives up carries that into the window's barrier
+// (__syncthreads_or), so the whole block leaves together; thread 0 first
+// waits (bounded) for the copies it still has in flight.
+template <int DT, int T, int CPT, int G, int TW, int MINB>
+__global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p)
+{
+    using F = Fmt<DT>;
+    constexpr int XV = x_chunk_vecs<DT>();
+    constexpr int NW = T / 32;
+    constexpr int U = G * TW;           // rows per window
+    constexpr int S = 2 * TW;           // stages
+    constexpr int ROWB = T * CPT * 16;  // bytes per row
+    constexpr bool PAIRED = DT == DT_Q4;
+    static_assert(T % 32 == 0 && NW <= 32, "block shape");
+    static_assert(F::XB == 2 || DT == DT_F32, "binary16 x (mixed-precision products) or FP32");
+    static_assert((U & (U - 1)) == 0 && U <= 32, "rows per window: a power of two up to 32");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const StageBandLayout L = stageband_layout(S, U, NW, G, ROWB, p.groups, F::QUANT);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    float *part = reinterpret_cast<float *>(smem + L.part);  // [2][U][NW]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t grid = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t ntiles = (p.M + G - 1) / G;
+    const int64_t I = b < ntiles ? (ntiles - 1 - b) / grid + 1 : 0;  // tiles b + i * grid
+    const int64_t sgrp = p.groups;
+
+    int64_t issued = 0;  // thread 0: tiles whose copies have been issued
+    auto issue = [&](int64_t i) {
+        const int s = static_cast<int>(i % S);
+        const int64_t row0 = (b + i * grid) * G;
+        const int64_t rows = p.M - row0 < G ? p.M - row0 : G;
+        const uint32_t abytes = static_cast<uint32_t>(rows * ROWB);
+        const uint32_t sbytes = F::QUANT ? static_cast<uint32_t>(rows * sgrp * 2) : 0u;
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, abytes + sbytes);
+        if (i == 0 && (p.skip_copies & SKIP_STAGE)) return;  // test hook: the wait must run out
+        bulk_copy_g2s(smem_addr(smem + L.stage + s * L.stage_bytes),
+                      static_cast<const unsigned char *>(p.A) + row0 * ROWB, abytes, bar);
+        if constexpr (F::QUANT)
+            bulk_copy_g2s(smem_addr(smem + L.stage + s * L.stage_bytes + L.scale_off), p.scales + row0 * sgrp,
+                          sbytes, bar);
+    };
+
+    pdl_trigger();
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(&full[s]), 1);
+        if (I > 0) {
+            // the first tile into L2 while the preceding kernel drains (a hint)
+            const int64_t row0 = b * G;
+            const int64_t rows = p.M - row0 < G ? p.M - row0 : G;
+            prefetch_l2(static_cast<const unsigned char *>(p.A) + row0 * ROWB, static_cast<uint32_t>(rows * ROWB));
+        }
+    }
+    if (!p.pdl) pdl_wait();
+    if (tid == 0)
+        for (; issued < S && issued < I; ++issued) issue(issued);
+    __syncthreads();  // barriers initialised before anyone waits on them
+    if (p.pdl) pdl_wait();
+
+    // this thread's x vectors (after the wait: the preceding kernel may have
+    // written x), re-paired for INT4
+    uint4 xr[CPT][XV];
+    {
+        const uint4 *xs = static_cast<const uint4 *>(p.x);
+#pragma unroll
+        for (int k = 0; k < CPT; ++k)
+#pragma unroll
+            for (int v = 0; v < XV; ++v) xr[k][v] = ld_l2_16(xs + (tid + k * T) * XV + v);
+        if constexpr (PAIRED) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k)
+#pragma unroll
+                for (int v = 0; v < XV; ++v) xr[k][v] = pair_x_vec(xr[k][v]);
+        }
+    }
+    // shared-space offsets of this thread's chunks and scales within a row
+    const uint32_t stage0 = smem_addr(smem + L.stage);
+    uint32_t soff[CPT];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) soff[k] = 2u * static_cast<uint32_t>((tid + k * T) >> p.scale_shift);
+
+    int half = 0;
+    for (int64_t i0 = 0; i0 < I; i0 += TW) {
+        bool ok = true;
+        float acc[U];
+#pragma unroll
+        for (int w = 0; w < TW; ++w) {
+            const int64_t i = i0 + w;
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[w * G + g] = 0.f;
+            if (i < I) {
+                const int s = static_cast<int>(i % S);
+                ok &= mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((i / S) & 1), p.wait_limit_ns);
+                const uint32_t st = stage0 + static_cast<uint32_t>(s) * L.stage_bytes;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    // rows past the end of A hold stale bytes: their sums are never stored
+                    float a = 0.f;
+                    if constexpr (F::QUANT) {
+#pragma unroll
+                        for (int k = 0; k < CPT; ++k) {
+                            const uint4 v = lds128(st + g * ROWB + (tid + k * T) * 16);
+                            const float sc = lds_half_as_float(st + L.scale_off + g * sgrp * 2 + soff[k]);
+                            float c0 = 0.f, c1 = 0.f;
+                            band_chunk<DT, PAIRED>(v, xr[k], c0, c1);
+                            a = fmaf(sc, c0, a);
+                            a = fmaf(sc, c1, a);
+                        }
+                    } else {
+                        float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+                        for (int k = 0; k < CPT; ++k)
+                            band_chunk<DT, PAIRED>(lds128(st + g * ROWB + (tid + k * T) * 16), xr[k], c0, c1);
+                        a = c0 + c1;
+                    }
+                    acc[w * G + g] = a;
+                }
+            }
+        }
+        // lane l ends with the warp's share of row slot l >> (5 - log2 U)
+        const float sum = warp_sum_rows<U>(acc, lane);
+        constexpr int LPR = 32 / U;
+        if ((lane & (LPR - 1)) == 0) part[(half * U + lane / LPR) * NW + warp] = sum;
+        // every thread has read the window's stages and written its partials;
+        // a wait that gave up anywhere makes the whole block leave here
+        if (__syncthreads_or(ok ? 0 : 1)) {
+            if (tid == 0) {
+                report_error(p.err, DEVERR_TIMEOUT);
+                bool drained = true;
+                for (int64_t j = i0; j < issued; ++j) {
+                    if (j == 0 && (p.skip_copies & SKIP_STAGE)) continue;  // never issued
+                    drained &= mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
+                                                 p.wait_limit_ns);
+                }
+                if (!drained) report_error(p.err, DEVERR_UNDRAINED);
+            }
+            return;
+        }
+        if (tid == 0)
+            for (; issued < i0 + S + TW && issued < I; ++issued) issue(issued);
+        if (tid < U) {
+            const int64_t i = i0 + tid / G;
+            const int64_t row = (b + i * grid) * G + tid % G;
+            if (i < I && row < p.M) {
+                float v = 0.f;
+#pragma unroll
+                for (int q = 0; q < NW; ++q) v += part[(half * U + tid) * NW + q];
+                p.y[row] = v;
+            }
         }
         half ^= 1;
     }
@@ -1090,31 +1350,60 @@ cudaError_t occupancy_bulk(int *blocks, size_t smem)
     MBG_BULK_MF(DT, T, RS, S, ((DT) == DT_F32 || (DT) == DT_F16X32 ? MATH_F32 : MATH_MIXED), CF, NAME)
 #define MBG_BULK_FX(DT, T, RS, S, CF, NAME) MBG_BULK_MFX(DT, T, RS, S, MATH_MIXED, CF, true, NAME)
 
-template <int DT, int T, int CPT, int U, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int MINB>
 void launch_band(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(mbg_rowband_kernel<DT, T, CPT, U, MINB>, a, grid, T, smem, s, pdl);
+    launch_maybe_pdl(mbg_rowband_kernel<DT, T, CPT, G, TW, MINB>, a, grid, T, smem, s, pdl);
 }
 
-template <int DT, int T, int CPT, int U, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int MINB>
 cudaError_t smem_limit_band(int)
 {
     return cudaSuccess;  // static shared memory only
 }
 
-template <int DT, int T, int CPT, int U, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int MINB>
 cudaError_t occupancy_band(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_rowband_kernel<DT, T, CPT, U, MINB>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_rowband_kernel<DT, T, CPT, G, TW, MINB>,
                                                          T, smem);
 }
 
-// band_t<threads>_c<chunks per thread>_u<rows in flight per thread>: rows of
-// exactly threads * chunks 16-byte chunks; x in registers
-#define MBG_BAND(DT, T, CPT, U, MINB, NAME)                                                      \
-    Variant{DT, T, U, CPT, T / 32, XMODE_REG, NAME, &launch_band<DT, T, CPT, U, MINB>,           \
-            &smem_limit_band<DT, T, CPT, U, MINB>, KIND_BAND, 0,                                  \
-            &occupancy_band<DT, T, CPT, U, MINB>, MATH_MIXED, 0}
+// band_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles in flight>:
+// rows of exactly threads * chunks 16-byte chunks; x in registers
+#define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME)                                                   \
+    Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME, &launch_band<DT, T, CPT, G, TW, MINB>, \
+            &smem_limit_band<DT, T, CPT, G, TW, MINB>, KIND_BAND, 0,                               \
+            &occupancy_band<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 0,   \
+            false, G}
+
+template <int DT, int T, int CPT, int G, int TW, int MINB>
+void launch_stageband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    launch_maybe_pdl(mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>, a, grid, T, smem, s, pdl);
+}
+
+template <int DT, int T, int CPT, int G, int TW, int MINB>
+cudaError_t smem_limit_stageband(int bytes)
+{
+    return cudaFuncSetAttribute(mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DT, int T, int CPT, int G, int TW, int MINB>
+cudaError_t occupancy_stageband(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>,
+                                                         T, smem);
+}
+
+// sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>:
+// rows of exactly threads * chunks 16-byte chunks; x in registers; 2 w stages
+#define MBG_SBAND(DT, T, CPT, G, TW, MINB, NAME)                                                         \
+    Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME, &launch_stageband<DT, T, CPT, G, TW, MINB>,   \
+            &smem_limit_stageband<DT, T, CPT, G, TW, MINB>, KIND_SBAND, 0,                                \
+            &occupancy_stageband<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 2 * (TW), \
+            false, G}
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -7,15 +7,22 @@
 namespace mbg {
 
 static const Variant kTableQ4[] = {
-    // row bands, x in registers: band_t<threads>_c<chunks per thread>_u<rows in flight>
-    // (rows of exactly threads * chunks 16-byte chunks)
-    MBG_BAND(DT_Q4, 128, 1, 12, 4, "band_t128_c1_u12"),
-    MBG_BAND(DT_Q4, 128, 1, 16, 3, "band_t128_c1_u16"),
-    MBG_BAND(DT_Q4, 128, 1, 24, 2, "band_t128_c1_u24"),
-    MBG_BAND(DT_Q4, 64, 2, 8, 6, "band_t64_c2_u8"),
-    MBG_BAND(DT_Q4, 448, 1, 12, 1, "band_t448_c1_u12"),
-    MBG_BAND(DT_Q4, 448, 1, 8, 1, "band_t448_c1_u8"),
-    MBG_BAND(DT_Q4, 224, 2, 8, 1, "band_t224_c2_u8"),
+    // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
+    // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks)
+    MBG_BAND(DT_Q4, 128, 1, 4, 4, 3, "band_t128_c1_g4_w4"),
+    MBG_BAND(DT_Q4, 128, 1, 2, 4, 4, "band_t128_c1_g2_w4"),
+    MBG_BAND(DT_Q4, 64, 2, 4, 2, 5, "band_t64_c2_g4_w2"),
+    MBG_BAND(DT_Q4, 448, 1, 2, 4, 1, "band_t448_c1_g2_w4"),
+    MBG_BAND(DT_Q4, 448, 1, 4, 2, 1, "band_t448_c1_g4_w2"),
+    MBG_BAND(DT_Q4, 224, 2, 2, 4, 1, "band_t224_c2_g2_w4"),
+    // staged row bands (tiles of A in shared memory by bulk copies):
+    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>
+    MBG_SBAND(DT_Q4, 128, 1, 4, 2, 6, "sband_t128_c1_g4_w2"),
+    MBG_SBAND(DT_Q4, 128, 1, 4, 4, 3, "sband_t128_c1_g4_w4"),
+    MBG_SBAND(DT_Q4, 128, 1, 8, 2, 3, "sband_t128_c1_g8_w2"),
+    MBG_SBAND(DT_Q4, 448, 1, 2, 2, 2, "sband_t448_c1_g2_w2"),
+    MBG_SBAND(DT_Q4, 224, 2, 2, 2, 3, "sband_t224_c2_g2_w2"),
+    MBG_SBAND(DT_Q4, 224, 2, 2, 4, 2, "sband_t224_c2_g2_w4"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
     // given row length the first that fits is the automatic choice

@@ -7,15 +7,22 @@
 namespace mbg {
 
 static const Variant kTableQ8[] = {
-    // row bands, x in registers: band_t<threads>_c<chunks per thread>_u<rows in flight>
-    // (rows of exactly threads * chunks 16-byte chunks)
-    MBG_BAND(DT_Q8, 256, 1, 12, 2, "band_t256_c1_u12"),
-    MBG_BAND(DT_Q8, 256, 1, 16, 2, "band_t256_c1_u16"),
-    MBG_BAND(DT_Q8, 128, 2, 8, 4, "band_t128_c2_u8"),
-    MBG_BAND(DT_Q8, 896, 1, 4, 1, "band_t896_c1_u4"),
-    MBG_BAND(DT_Q8, 896, 1, 6, 1, "band_t896_c1_u6"),
-    MBG_BAND(DT_Q8, 448, 2, 6, 1, "band_t448_c2_u6"),
-    MBG_BAND(DT_Q8, 448, 2, 4, 1, "band_t448_c2_u4"),
+    // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
+    // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks)
+    MBG_BAND(DT_Q8, 256, 1, 2, 4, 2, "band_t256_c1_g2_w4"),
+    MBG_BAND(DT_Q8, 256, 1, 4, 4, 1, "band_t256_c1_g4_w4"),
+    MBG_BAND(DT_Q8, 128, 2, 2, 4, 3, "band_t128_c2_g2_w4"),
+    MBG_BAND(DT_Q8, 448, 2, 2, 2, 1, "band_t448_c2_g2_w2"),
+    MBG_BAND(DT_Q8, 896, 1, 2, 2, 1, "band_t896_c1_g2_w2"),
+    MBG_BAND(DT_Q8, 224, 4, 2, 2, 1, "band_t224_c4_g2_w2"),
+    // staged row bands (tiles of A in shared memory by bulk copies):
+    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>
+    MBG_SBAND(DT_Q8, 256, 1, 2, 2, 4, "sband_t256_c1_g2_w2"),
+    MBG_SBAND(DT_Q8, 256, 1, 4, 2, 2, "sband_t256_c1_g4_w2"),
+    MBG_SBAND(DT_Q8, 128, 2, 2, 4, 4, "sband_t128_c2_g2_w4"),
+    MBG_SBAND(DT_Q8, 448, 2, 2, 2, 1, "sband_t448_c2_g2_w2"),
+    MBG_SBAND(DT_Q8, 448, 2, 1, 4, 1, "sband_t448_c2_g1_w4"),
+    MBG_SBAND(DT_Q8, 896, 1, 2, 2, 1, "sband_t896_c1_g2_w2"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
