@@ -11,10 +11,11 @@ x, stream A, accumulate, reduce, write y.  Weights rotate through enough
 copies (at least max(256 MiB, 4 x L2)) that every launch reads A cold from
 HBM ("membound", gotcha 1); x stays resident.  The K timed steps are one CUDA
 graph of exactly K back-to-back launches (or replays of a graph of B launches
-plus one graph of the remainder), each graph replayed during warm-up; before
-the timed region L2 is flushed and a short spin kernel is queued so that the
-host's submission of the graph is not inside the timed region.  Time comes
-from CUDA events on the launching stream.  Algorithmic bytes per step = A +
+plus one graph of the remainder), each graph replayed during warm-up; right
+before the timed region a short spin kernel (so that the host's submission of
+the graph is not timed) and an untimed replay of one rotation of the weights
+(so that the first timed launch follows a launch of the same kernel, as in a
+decode loop).  Time comes from CUDA events on the launching stream.  Algorithmic bytes per step = A +
 scales + x read once, y written once ("Making GEMV Fast", section "Memory
 Access").
 
@@ -414,30 +415,28 @@ class Resident:
 
 
 class Timer:
-    """Graphs of back-to-back launches timed with CUDA events on one stream."""
+    """Graphs of back-to-back launches timed with CUDA events on one stream.
+
+    Every timed pass is preceded by an untimed replay of one full rotation
+    (launches on copies 0 .. copies-1): the first timed launch then follows a
+    launch of the same kernel, as every later one does, and reads copy 0,
+    which was last touched `copies` launches (at least 4 x L2 of weights)
+    earlier.  Measured on the headline: one launch alone takes ~22 us, the
+    first of a short chain ~7-10 us more than the steady 15.9 us, because
+    consecutive launches hide each other's ramp; without the pre-roll a
+    20-launch region carries that once."""
 
     def __init__(self, dev, stream, l2):
-        import torch
         self.dev = dev
         self.stream = stream
-        # read before each timed region: evicts whatever the warm-up left in L2
-        # (a read leaves no dirty lines whose write-back would land in the
-        # timed region)
-        self.flush_buf = torch.ones(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
-        self.flush_out = torch.empty(1, dtype=torch.int64, device=dev)
-        with torch.cuda.stream(stream):
-            self._flush()  # loads the reduction kernel now, not in a timed region
-        stream.synchronize()
 
-    def _flush(self):
-        import torch
-        torch.sum(self.flush_buf, dim=0, dtype=torch.int64, out=self.flush_out.view(()))
-
-    def capture(self, launch, plan, overlap=False):
+    def capture(self, launch, plan, overlap=False, copies=None):
+        """Graphs for the plan, plus (first) the pre-roll graph of one rotation."""
         import torch
         graphs = []
         with torch.cuda.stream(self.stream):
-            for n, _ in plan:
+            sizes = ([copies] if copies else []) + [n for n, _ in plan]
+            for n in sizes:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=self.stream):
                     for i in range(n):
@@ -447,7 +446,7 @@ class Timer:
         return graphs
 
     def replay(self, graphs, plan):
-        for g, (_, reps) in zip(graphs, plan):
+        for g, (_, reps) in zip(graphs[1:], plan):
             for _ in range(reps):
                 g.replay()
 
@@ -456,8 +455,9 @@ class Timer:
         import torch
         done = 0
         with torch.cuda.stream(self.stream):
+            graphs[0].replay()
             while True:
-                for g, (n, _) in zip(graphs, plan):
+                for g, (n, _) in zip(graphs[1:], plan):
                     g.replay()
                     done += n
                 if done >= launches:
@@ -465,13 +465,13 @@ class Timer:
         self.stream.synchronize()
 
     def timed(self, graphs, plan):
-        """Seconds for one pass of the plan: a spin kernel queued first so that
-        the host's submissions are not timed, then L2 flushed by a read right
-        before the first timed launch (memory stays busy up to it)."""
+        """Seconds for one pass of the plan: a spin kernel first (the host's
+        submissions are not timed), then the untimed pre-roll, then the plan
+        between two events."""
         import torch
         with torch.cuda.stream(self.stream):
             torch.cuda._sleep(GATE_CYCLES)
-            self._flush()
+            graphs[0].replay()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(self.stream)
             self.replay(graphs, plan)
@@ -571,7 +571,7 @@ def run_ours(args):
             R.launch(i)
     stream.synchronize()
     plan = graph_plan(args.steps, R.copies, args.graph_max)
-    graphs = timer.capture(R.launch, plan)
+    graphs = timer.capture(R.launch, plan, copies=R.copies)
     timer.warm(graphs, plan, args.warmup)
 
     sampler = ClockSampler(gpu_id_for(local_rank)) if not args.no_clocks else None
@@ -600,7 +600,7 @@ def run_ours(args):
     # the previous one finishes; weights are never written by the chain)
     overlap = None
     if not args.no_overlap:
-        g_ov = timer.capture(R.launch, plan, overlap=True)
+        g_ov = timer.capture(R.launch, plan, overlap=True, copies=R.copies)
         timer.warm(g_ov, plan, args.warmup)
         barrier()
         ov_t = max_over_ranks(timer.timed(g_ov, plan), dev)
@@ -615,7 +615,7 @@ def run_ours(args):
     long_chain = None
     if not args.no_long_chain:
         lplan = graph_plan(args.long_steps, R.copies, args.graph_max)
-        lg = timer.capture(R.launch, lplan)
+        lg = timer.capture(R.launch, lplan, copies=R.copies)
         timer.warm(lg, lplan, 1)
         lt = timer.timed(lg, lplan)
         long_chain = {"steps": args.long_steps, "us_per_launch": lt / args.long_steps * 1e6,
@@ -700,10 +700,12 @@ def run_ours(args):
         "config": {"workload": w.name, "M": w.M, "N": w.N, "weights": w.dtype,
                    "variant": vinfo["name"], "rotation_copies": R.copies,
                    "rotation_bytes": R.copies * R.wbytes, "l2_bytes": l2,
-                   "l2_policy": "inputs larger than L2 (weights rotate through the copies, each launch reads "
-                                "A cold from HBM) and L2 flushed by reading a 2 x L2 buffer before the timed region",
-                   "launch": f"timed: {launch_desc}; each graph replayed during warm-up; a spin kernel queued "
-                             f"ahead of the timed region",
+                   "l2_policy": "inputs larger than L2: the weights rotate through the copies, so each launch "
+                                "reads a copy last touched `rotation_copies` launches earlier (cold from HBM)",
+                   "launch": f"timed: {launch_desc}; each graph replayed during warm-up; right before the timed "
+                             f"region a spin kernel (so no host submission is timed) and an untimed replay of one "
+                             f"rotation ({R.copies} launches), so that the first timed launch follows a launch of "
+                             f"the same kernel as every later one does",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "mbu": {"probe_gbs": ceiling, "probe_variant": best_probe,
                 "mbu_probe_pct": 100.0 * achieved / ceiling,
@@ -795,7 +797,8 @@ def measure_configs(args, mbg, dev, l2, stream, timer, ceiling):
     chains), GB/s, MBU, parity over every row; FP16 / INT8 / INT4 interleaved."""
     import torch
     out = {"how": f"per workload: automatic kernel; a CUDA graph of ~{args.config_launches} back-to-back "
-                  f"launches over the rotated weights, replayed once to warm and once timed after an L2 flush; "
+                  f"launches over the rotated weights, replayed once to warm and once timed after an untimed "
+                  f"replay of one rotation; "
                   f"MBU against the run's probe ceiling ({ceiling:.0f} GB/s) and the 8 TB/s spec; parity: the "
                   f"first launch against the double-precision oracle over every row",
            "workloads": {}, "interleaved": {}}
@@ -806,7 +809,7 @@ def measure_configs(args, mbg, dev, l2, stream, timer, ceiling):
     def chain(R, overlap):
         n = R.copies * max(1, math.ceil(args.config_launches / R.copies))
         plan = [(n, 1)]
-        g = timer.capture(R.launch, plan, overlap=overlap)
+        g = timer.capture(R.launch, plan, overlap=overlap, copies=R.copies)
         timer.warm(g, plan, 1)
         t = timer.timed(g, plan)
         return g, plan, t / n
@@ -922,7 +925,7 @@ def run_softmax(args):
 
     before = copy_probe()
     plan = graph_plan(args.steps, copies, min(args.graph_max, 50 * copies))
-    graphs = timer.capture(launch, plan)
+    graphs = timer.capture(launch, plan, copies=copies)
     timer.warm(graphs, plan, args.warmup)
     t = timer.timed(graphs, plan)
     steps = args.steps
@@ -941,8 +944,7 @@ def run_softmax(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded SplitMix64 normal(0, 2) logits rounded to FP16)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "rotation_copies": copies,
-                       "l2_policy": "inputs larger than L2: the logits rotate through the copies; L2 flushed "
-                                    "before the timed region",
+                       "l2_policy": "inputs larger than L2: the logits rotate through the copies",
                        "launch": " + ".join(f"{reps} x graph of {n} launches" for n, reps in plan)},
             "mbu": {"copy_probe_gbs": ceiling, "mbu_copy_pct": 100.0 * value / ceiling, "probes": best},
             "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",

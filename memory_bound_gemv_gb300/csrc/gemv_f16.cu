@@ -20,9 +20,9 @@ static const Variant kTableF16[] = {
     MBG_BAND(DT_F16, 448, 4, 2, 2, 1, "band_t448_c4_g2_w2"),
     MBG_BAND(DT_F16, 512, 4, 2, 2, 1, "band_t512_c4_g2_w2"),
     // staged row bands (tiles of A in shared memory by bulk copies):
-    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>
-    MBG_SBAND(DT_F16, 256, 2, 2, 2, 3, "sband_t256_c2_g2_w2"),
-    MBG_SBAND(DT_F16, 448, 4, 1, 2, 1, "sband_t448_c4_g1_w2"),
+    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>_p<windows in flight>
+    MBG_SBAND(DT_F16, 256, 2, 2, 2, 1, 3, "sband_t256_c2_g2_w2_p1"),
+    MBG_SBAND(DT_F16, 448, 4, 1, 2, 1, 1, "sband_t448_c4_g1_w2_p1"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_F16, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_F16, 256, 1, 3, "bulk_t256_r1_s3"),

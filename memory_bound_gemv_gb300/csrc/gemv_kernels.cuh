@@ -777,6 +777,68 @@ __device__ __forceinline__ void band_chunk(const uint4 a, const uint4 (&xv)[x_ch
     }
 }
 
+// The G rows of a tile times one x chunk, word by word with the rows
+// innermost, into two FP32 partials per row: 2 G independent accumulation
+// chains, so the half-rate mixed-precision FMAs of different rows overlap.
+template <int DT, bool PAIRED, int G>
+__device__ __forceinline__ void tile_chunk(const uint4 (&a)[G], const uint4 (&xv)[x_chunk_vecs<DT>()],
+                                           float (&c0)[G], float (&c1)[G])
+{
+    if constexpr (DT == DT_F32) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            c0[g] = fmaf(__uint_as_float(a[g].x), __uint_as_float(xv[0].x), c0[g]);
+            c1[g] = fmaf(__uint_as_float(a[g].y), __uint_as_float(xv[0].y), c1[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            c0[g] = fmaf(__uint_as_float(a[g].z), __uint_as_float(xv[0].z), c0[g]);
+            c1[g] = fmaf(__uint_as_float(a[g].w), __uint_as_float(xv[0].w), c1[g]);
+        }
+    } else if constexpr (DT == DT_F16) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t xw = q == 0 ? xv[0].x : q == 1 ? xv[0].y : q == 2 ? xv[0].z : xv[0].w;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t w = q == 0 ? a[g].x : q == 1 ? a[g].y : q == 2 ? a[g].z : a[g].w;
+                mfma_pair(w, xw, c0[g], c1[g]);
+            }
+        }
+    } else if constexpr (DT == DT_Q8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 &x = xv[q >> 1];
+            const uint32_t x01 = (q & 1) ? x.z : x.x;
+            const uint32_t x23 = (q & 1) ? x.w : x.y;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t w = q == 0 ? a[g].x : q == 1 ? a[g].y : q == 2 ? a[g].z : a[g].w;
+                uint32_t h[2];
+                q8_codes_h2(w, h);
+                mfma_pair(h[0], x01, c0[g], c1[g]);
+                mfma_pair(h[1], x23, c0[g], c1[g]);
+            }
+        }
+    } else {
+        static_assert(DT == DT_Q4 && PAIRED, "INT4 takes x in the paired order");
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 &x = xv[q];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t w = q == 0 ? a[g].x : q == 1 ? a[g].y : q == 2 ? a[g].z : a[g].w;
+                uint32_t h[4];
+                q4_codes_h2(w, h);
+                mfma_pair(h[0], x.x, c0[g], c1[g]);
+                mfma_pair(h[1], x.y, c0[g], c1[g]);
+                mfma_pair(h[2], x.z, c0[g], c1[g]);
+                mfma_pair(h[3], x.w, c0[g], c1[g]);
+            }
+        }
+    }
+}
+
 // Predicated loads that leave the destination unchanged when the predicate is
 // false (the same registers either way, so a rolling window needs no copies).
 __device__ __forceinline__ void ld_stream16_if(uint4 &v, const void *p, bool pred)
@@ -915,7 +977,7 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
             const bool ok = FULL || (in < I && row0 + g < p.M);
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
-                if constexpr (FULL) ld_stream16_into(a[w * G + g][k], an + g * ROWB + k * T * 16);
+                        if constexpr (FULL) ld_stream16_into(a[w * G + g][k], an + g * ROWB + k * T * 16);
                 else ld_stream16_if(a[w * G + g][k], an + g * ROWB + k * T * 16, ok);
             }
             if constexpr (F::QUANT) {
@@ -953,26 +1015,34 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
         }
     }
 
-    // the products of row slot r (rows of tiles that do not exist give
-    // values that are never stored)
-    auto row_dot = [&](int r) {
-        float acc = 0.f;
-        if constexpr (F::QUANT) {
+    // the products of the G row slots of tile slot w into acc (rows of tiles
+    // that do not exist give values that are never stored)
+    auto tile_dot = [&](int w, float (&acc)[U]) {
+        float c0[G], c1[G];
 #pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const float s = half_bits_to_float(sc[r][k]);
-                float c0 = 0.f, c1 = 0.f;
-                band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
-                acc = fmaf(s, c0, acc);
-                acc = fmaf(s, c1, acc);
+        for (int g = 0; g < G; ++g) c0[g] = c1[g] = 0.f;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            uint4 ak[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) ak[g] = a[w * G + g][k];
+            if constexpr (F::QUANT) {
+                float d0[G], d1[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) d0[g] = d1[g] = 0.f;
+                tile_chunk<DT, PAIRED, G>(ak, xr[k], d0, d1);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float s = half_bits_to_float(sc[w * G + g][k]);
+                    c0[g] = fmaf(s, d0[g], c0[g]);
+                    c1[g] = fmaf(s, d1[g], c1[g]);
+                }
+            } else {
+                tile_chunk<DT, PAIRED, G>(ak, xr[k], c0, c1);
             }
-        } else {
-            float c0 = 0.f, c1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) band_chunk<DT, PAIRED>(a[r][k], xr[k], c0, c1);
-            acc = c0 + c1;
         }
-        return acc;
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[w * G + g] = c0[g] + c1[g];
     };
 
     int half = 0;
@@ -986,8 +1056,7 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
             for (int w = 0; w < TW; ++w) {
                 // rows of tile i0 + w are multiplied straight from their
                 // slots, which are then refilled in place with tile i0 + TW + w
-#pragma unroll
-                for (int g = 0; g < G; ++g) acc[w * G + g] = row_dot(w * G + g);
+                tile_dot(w, acc);
                 load_tile(w, fl);
             }
         };
@@ -1019,23 +1088,24 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
 // The row-band kernel's work split (thread t multiplies chunks t, t + T, ...
 // of every row with x held in registers; tiles of G consecutive rows dealt
 // to blocks in grid-stride order), but the tiles reach the block through a
-// ring of 2 TW shared-memory stages filled by bulk async copies, so the bytes
-// in flight cost no registers.  Thread 0 issues the copies; everybody reads
-// the stage (one 16-byte shared load per chunk and row).  The block barrier
-// that closes each window of TW tiles (after the warp partials are written)
-// also tells thread 0 that the window's stages have been read, and it
-// refills them with the tiles 2 TW ahead.  Every wait is bounded: a thread
+// ring of (PF + 1) TW shared-memory stages filled by bulk async copies, so
+// the bytes in flight cost no registers: PF windows of TW tiles are in flight
+// while one is multiplied.  Thread 0 issues the copies; everybody reads the
+// stage (one 16-byte shared load per chunk and row).  The block barrier that
+// closes each window of TW tiles (after the warp partials are written) also
+// tells thread 0 that the window's stages have been read, and it refills them
+// with the tiles (PF + 1) TW ahead.  Every wait is bounded: a thread
 // whose wait gives up carries that into the window's barrier
 // (__syncthreads_or), so the whole block leaves together; thread 0 first
 // waits (bounded) for the copies it still has in flight.
-template <int DT, int T, int CPT, int G, int TW, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 __global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p)
 {
     using F = Fmt<DT>;
     constexpr int XV = x_chunk_vecs<DT>();
     constexpr int NW = T / 32;
     constexpr int U = G * TW;           // rows per window
-    constexpr int S = 2 * TW;           // stages
+    constexpr int S = (PF + 1) * TW;    // stages
     constexpr int ROWB = T * CPT * 16;  // bytes per row
     constexpr bool PAIRED = DT == DT_Q4;
     static_assert(T % 32 == 0 && NW <= 32, "block shape");
@@ -1122,29 +1192,32 @@ __global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p
                 const int s = static_cast<int>(i % S);
                 ok &= mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((i / S) & 1), p.wait_limit_ns);
                 const uint32_t st = stage0 + static_cast<uint32_t>(s) * L.stage_bytes;
+                // rows past the end of A hold stale bytes: their sums are never stored
+                float c0[G], c1[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    // rows past the end of A hold stale bytes: their sums are never stored
-                    float a = 0.f;
+                for (int g = 0; g < G; ++g) c0[g] = c1[g] = 0.f;
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) {
+                    uint4 ak[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) ak[g] = lds128(st + g * ROWB + (tid + k * T) * 16);
                     if constexpr (F::QUANT) {
+                        float d0[G], d1[G];
 #pragma unroll
-                        for (int k = 0; k < CPT; ++k) {
-                            const uint4 v = lds128(st + g * ROWB + (tid + k * T) * 16);
+                        for (int g = 0; g < G; ++g) d0[g] = d1[g] = 0.f;
+                        tile_chunk<DT, PAIRED, G>(ak, xr[k], d0, d1);
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
                             const float sc = lds_half_as_float(st + L.scale_off + g * sgrp * 2 + soff[k]);
-                            float c0 = 0.f, c1 = 0.f;
-                            band_chunk<DT, PAIRED>(v, xr[k], c0, c1);
-                            a = fmaf(sc, c0, a);
-                            a = fmaf(sc, c1, a);
+                            c0[g] = fmaf(sc, d0[g], c0[g]);
+                            c1[g] = fmaf(sc, d1[g], c1[g]);
                         }
                     } else {
-                        float c0 = 0.f, c1 = 0.f;
-#pragma unroll
-                        for (int k = 0; k < CPT; ++k)
-                            band_chunk<DT, PAIRED>(lds128(st + g * ROWB + (tid + k * T) * 16), xr[k], c0, c1);
-                        a = c0 + c1;
+                        tile_chunk<DT, PAIRED, G>(ak, xr[k], c0, c1);
                     }
-                    acc[w * G + g] = a;
                 }
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[w * G + g] = c0[g] + c1[g];
             }
         }
         // lane l ends with the warp's share of row slot l >> (5 - log2 U)
@@ -1167,7 +1240,7 @@ __global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p
             return;
         }
         if (tid == 0)
-            for (; issued < i0 + S + TW && issued < I; ++issued) issue(issued);
+            for (; issued < i0 + S + TW && issued < I; ++issued) issue(issued);  // into the window's stages
         if (tid < U) {
             const int64_t i = i0 + tid / G;
             const int64_t row = (b + i * grid) * G + tid % G;
@@ -1377,33 +1450,34 @@ cudaError_t occupancy_band(int *blocks, size_t smem)
             &occupancy_band<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 0,   \
             false, G}
 
-template <int DT, int T, int CPT, int G, int TW, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 void launch_stageband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>, a, grid, T, smem, s, pdl);
+    launch_maybe_pdl(mbg_stageband_kernel<DT, T, CPT, G, TW, PF, MINB>, a, grid, T, smem, s, pdl);
 }
 
-template <int DT, int T, int CPT, int G, int TW, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 cudaError_t smem_limit_stageband(int bytes)
 {
-    return cudaFuncSetAttribute(mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>,
+    return cudaFuncSetAttribute(mbg_stageband_kernel<DT, T, CPT, G, TW, PF, MINB>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DT, int T, int CPT, int G, int TW, int MINB>
+template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 cudaError_t occupancy_stageband(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_stageband_kernel<DT, T, CPT, G, TW, MINB>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_stageband_kernel<DT, T, CPT, G, TW, PF, MINB>,
                                                          T, smem);
 }
 
-// sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>:
-// rows of exactly threads * chunks 16-byte chunks; x in registers; 2 w stages
-#define MBG_SBAND(DT, T, CPT, G, TW, MINB, NAME)                                                         \
-    Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME, &launch_stageband<DT, T, CPT, G, TW, MINB>,   \
-            &smem_limit_stageband<DT, T, CPT, G, TW, MINB>, KIND_SBAND, 0,                                \
-            &occupancy_stageband<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 2 * (TW), \
-            false, G}
+// sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>_p<windows
+// in flight>: rows of exactly threads * chunks 16-byte chunks; x in registers;
+// (p + 1) w stages
+#define MBG_SBAND(DT, T, CPT, G, TW, PF, MINB, NAME)                                                   \
+    Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME,                                          \
+            &launch_stageband<DT, T, CPT, G, TW, PF, MINB>, &smem_limit_stageband<DT, T, CPT, G, TW, PF, MINB>, \
+            KIND_SBAND, 0, &occupancy_stageband<DT, T, CPT, G, TW, PF, MINB>,                           \
+            (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, ((PF) + 1) * (TW), false, G}
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

@@ -15,14 +15,20 @@ static const Variant kTableQ4[] = {
     MBG_BAND(DT_Q4, 448, 1, 2, 4, 1, "band_t448_c1_g2_w4"),
     MBG_BAND(DT_Q4, 448, 1, 4, 2, 1, "band_t448_c1_g4_w2"),
     MBG_BAND(DT_Q4, 224, 2, 2, 4, 1, "band_t224_c2_g2_w4"),
+    MBG_BAND(DT_Q4, 128, 1, 2, 2, 6, "band_t128_c1_g2_w2"),
+    MBG_BAND(DT_Q4, 128, 1, 4, 2, 5, "band_t128_c1_g4_w2"),
+    MBG_BAND(DT_Q4, 448, 1, 2, 2, 2, "band_t448_c1_g2_w2"),
     // staged row bands (tiles of A in shared memory by bulk copies):
-    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>
-    MBG_SBAND(DT_Q4, 128, 1, 4, 2, 6, "sband_t128_c1_g4_w2"),
-    MBG_SBAND(DT_Q4, 128, 1, 4, 4, 3, "sband_t128_c1_g4_w4"),
-    MBG_SBAND(DT_Q4, 128, 1, 8, 2, 3, "sband_t128_c1_g8_w2"),
-    MBG_SBAND(DT_Q4, 448, 1, 2, 2, 2, "sband_t448_c1_g2_w2"),
-    MBG_SBAND(DT_Q4, 224, 2, 2, 2, 3, "sband_t224_c2_g2_w2"),
-    MBG_SBAND(DT_Q4, 224, 2, 2, 4, 2, "sband_t224_c2_g2_w4"),
+    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>_p<windows in flight>
+    MBG_SBAND(DT_Q4, 128, 1, 4, 2, 1, 6, "sband_t128_c1_g4_w2_p1"),
+    MBG_SBAND(DT_Q4, 128, 1, 4, 2, 2, 4, "sband_t128_c1_g4_w2_p2"),
+    MBG_SBAND(DT_Q4, 128, 1, 2, 4, 2, 4, "sband_t128_c1_g2_w4_p2"),
+    MBG_SBAND(DT_Q4, 128, 1, 8, 2, 1, 3, "sband_t128_c1_g8_w2_p1"),
+    MBG_SBAND(DT_Q4, 128, 1, 4, 2, 3, 3, "sband_t128_c1_g4_w2_p3"),
+    MBG_SBAND(DT_Q4, 448, 1, 2, 2, 1, 2, "sband_t448_c1_g2_w2_p1"),
+    MBG_SBAND(DT_Q4, 448, 1, 2, 2, 2, 1, "sband_t448_c1_g2_w2_p2"),
+    MBG_SBAND(DT_Q4, 224, 2, 2, 2, 2, 3, "sband_t224_c2_g2_w2_p2"),
+    MBG_SBAND(DT_Q4, 224, 2, 1, 4, 2, 3, "sband_t224_c2_g1_w4_p2"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
     // given row length the first that fits is the automatic choice

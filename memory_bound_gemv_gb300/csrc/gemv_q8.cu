@@ -16,13 +16,13 @@ static const Variant kTableQ8[] = {
     MBG_BAND(DT_Q8, 896, 1, 2, 2, 1, "band_t896_c1_g2_w2"),
     MBG_BAND(DT_Q8, 224, 4, 2, 2, 1, "band_t224_c4_g2_w2"),
     // staged row bands (tiles of A in shared memory by bulk copies):
-    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>
-    MBG_SBAND(DT_Q8, 256, 1, 2, 2, 4, "sband_t256_c1_g2_w2"),
-    MBG_SBAND(DT_Q8, 256, 1, 4, 2, 2, "sband_t256_c1_g4_w2"),
-    MBG_SBAND(DT_Q8, 128, 2, 2, 4, 4, "sband_t128_c2_g2_w4"),
-    MBG_SBAND(DT_Q8, 448, 2, 2, 2, 1, "sband_t448_c2_g2_w2"),
-    MBG_SBAND(DT_Q8, 448, 2, 1, 4, 1, "sband_t448_c2_g1_w4"),
-    MBG_SBAND(DT_Q8, 896, 1, 2, 2, 1, "sband_t896_c1_g2_w2"),
+    // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>_p<windows in flight>
+    MBG_SBAND(DT_Q8, 256, 1, 2, 2, 1, 4, "sband_t256_c1_g2_w2_p1"),
+    MBG_SBAND(DT_Q8, 256, 1, 2, 2, 2, 3, "sband_t256_c1_g2_w2_p2"),
+    MBG_SBAND(DT_Q8, 128, 2, 2, 4, 2, 3, "sband_t128_c2_g2_w4_p2"),
+    MBG_SBAND(DT_Q8, 448, 2, 2, 2, 1, 1, "sband_t448_c2_g2_w2_p1"),
+    MBG_SBAND(DT_Q8, 448, 2, 1, 2, 2, 1, "sband_t448_c2_g1_w2_p2"),
+    MBG_SBAND(DT_Q8, 896, 1, 1, 2, 2, 1, "sband_t896_c1_g1_w2_p2"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),
     // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
