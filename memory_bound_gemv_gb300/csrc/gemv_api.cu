@@ -274,15 +274,14 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
             if (v[k].kind == KIND_BAND && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         }
     }
-    // the quantised types are bound by instruction issue: the bulk-copy
-    // pipeline (no load instructions for A) wins.  A variant specialised for
-    // exactly this row length (a fixed chunk count per consumer thread) comes
-    // first, in table order (measured best first); otherwise the general
-    // pipelines for INT8 and for INT4 rows of 4 KB or more, and row tiles for
-    // shorter INT4 rows
+    // the quantised types are bound by instruction issue: a row band or a
+    // bulk-copy pipeline specialised for exactly this row length comes first,
+    // in table order (measured best first); otherwise the general pipelines
+    // for INT8 and for INT4 rows of 4 KB or more, and row tiles for shorter
+    // INT4 rows
     if ((dtype == DT_Q8 || dtype == DT_Q4) && small_x) {
         for (int k = 0; k < n; ++k) {
-            if (v[k].kind == KIND_BULK && v[k].unroll > 0 &&
+            if ((v[k].kind == KIND_BAND || (v[k].kind == KIND_BULK && v[k].unroll > 0)) &&
                 variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
                 return k;
         }

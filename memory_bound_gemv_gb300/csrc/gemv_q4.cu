@@ -7,8 +7,13 @@
 namespace mbg {
 
 static const Variant kTableQ4[] = {
-    // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
-    // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks)
+    // the automatic choice takes, in table order, the first row band or
+    // fixed-count bulk pipeline that covers the row exactly (measured best first)
+    // bulk-copy pipelines specialised for rows of exactly f * t chunks:
+    // bulk_t<consumer threads>_r<rows per stage>_s<stages>_f<chunks per thread>
+    MBG_BULK_F(DT_Q4, 224, 2, 3, 2, "bulk_t224_r2_s3_f2"),
+    MBG_BULK_F(DT_Q4, 128, 4, 3, 1, "bulk_t128_r4_s3_f1"),
+    // other row bands (x in registers), band_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles in flight>
     MBG_BAND(DT_Q4, 128, 1, 4, 4, 3, "band_t128_c1_g4_w4"),
     MBG_BAND(DT_Q4, 128, 1, 2, 4, 4, "band_t128_c1_g2_w4"),
     MBG_BAND(DT_Q4, 64, 2, 4, 2, 5, "band_t64_c2_g4_w2"),
@@ -29,11 +34,7 @@ static const Variant kTableQ4[] = {
     MBG_SBAND(DT_Q4, 448, 1, 2, 2, 2, 1, "sband_t448_c1_g2_w2_p2"),
     MBG_SBAND(DT_Q4, 224, 2, 2, 2, 2, 3, "sband_t224_c2_g2_w2_p2"),
     MBG_SBAND(DT_Q4, 224, 2, 1, 4, 2, 3, "sband_t224_c2_g1_w4_p2"),
-    // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
-    // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
-    // given row length the first that fits is the automatic choice
-    MBG_BULK_F(DT_Q4, 224, 2, 3, 2, "bulk_t224_r2_s3_f2"),
-    MBG_BULK_F(DT_Q4, 128, 4, 3, 1, "bulk_t128_r4_s3_f1"),
+    // general variants (explicit choice, and the fallbacks of the automatic one)
     MBG_BULK(DT_Q4, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q4, 256, 1, 3, "bulk_t256_r1_s3"),
     MBG_BULK(DT_Q4, 512, 1, 4, "bulk_t512_r1_s4"),

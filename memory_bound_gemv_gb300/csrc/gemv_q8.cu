@@ -7,9 +7,16 @@
 namespace mbg {
 
 static const Variant kTableQ8[] = {
-    // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
-    // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks)
+    // the automatic choice takes, in table order, the first row band or
+    // fixed-count bulk pipeline that covers the row exactly (measured best first)
     MBG_BAND(DT_Q8, 256, 1, 2, 4, 2, "band_t256_c1_g2_w4"),
+    // bulk-copy pipelines specialised for rows of exactly f * t chunks:
+    // bulk_t<consumer threads>_r<rows per stage>_s<stages>_f<chunks per thread>
+    MBG_BULK_F(DT_Q8, 128, 4, 3, 2, "bulk_t128_r4_s3_f2"),
+    MBG_BULK_FX(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4_xr"),
+    MBG_BULK_F(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4"),
+    MBG_BULK_F(DT_Q8, 128, 4, 2, 2, "bulk_t128_r4_s2_f2"),
+    // other row bands (x in registers), band_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles in flight>
     MBG_BAND(DT_Q8, 256, 1, 4, 4, 1, "band_t256_c1_g4_w4"),
     MBG_BAND(DT_Q8, 128, 2, 2, 4, 3, "band_t128_c2_g2_w4"),
     MBG_BAND(DT_Q8, 448, 2, 2, 2, 1, "band_t448_c2_g2_w2"),
@@ -23,15 +30,9 @@ static const Variant kTableQ8[] = {
     MBG_SBAND(DT_Q8, 448, 2, 2, 2, 1, 1, "sband_t448_c2_g2_w2_p1"),
     MBG_SBAND(DT_Q8, 448, 2, 1, 2, 2, 1, "sband_t448_c2_g1_w2_p2"),
     MBG_SBAND(DT_Q8, 896, 1, 1, 2, 2, 1, "sband_t896_c1_g1_w2_p2"),
+    // general variants (explicit choice, and the fallbacks of the automatic one)
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),
-    // fixed chunks per consumer thread (rows of exactly f * t chunks); for a
-    // given row length the first that fits is the automatic choice
-    MBG_BULK_F(DT_Q8, 128, 4, 3, 2, "bulk_t128_r4_s3_f2"),
-    // x in registers (_xr): measured +5 % at 14336 columns, slower for 4096
-    MBG_BULK_FX(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4_xr"),
-    MBG_BULK_F(DT_Q8, 224, 1, 3, 4, "bulk_t224_r1_s3_f4"),
-    MBG_BULK_F(DT_Q8, 128, 4, 2, 2, "bulk_t128_r4_s2_f2"),
     MBG_BULK(DT_Q8, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q8, 512, 1, 4, "bulk_t512_r1_s4"),
     MBG_BULK(DT_Q8, 256, 2, 4, "bulk_t256_r2_s4"),
