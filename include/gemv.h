@@ -348,6 +348,10 @@ gemv_status_t gemv_variant_info(int dtype, int variant, gemv_variant_info_t *inf
 int gemv_select_variant(int dtype, const void *A, const void *x, int64_t M, int64_t N);
 gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void *x, float *y,
                                int64_t M, int64_t N, const uint16_t *scales, void *stream);
+/* gemv_run_variant with the launch flags of gemv_ex. */
+gemv_status_t gemv_run_variant_ex(int dtype, int variant, const void *A, const void *x, float *y,
+                                  int64_t M, int64_t N, const uint16_t *scales, unsigned flags,
+                                  void *stream);
 /* The same two calls for gemv_q8_rowscale (variant ids index the INT8 table;
  * the bulk-copy variants return GEMV_ERR_UNSUPPORTED there). */
 int gemv_q8_rowscale_select_variant(const int8_t *A, const uint16_t *x, int64_t M, int64_t N);

@@ -73,6 +73,7 @@ def _declare(L):
         "gemv_dequant_q4": [vp, vp, vp, i64, i64, vp],
         "gemv_variant_info": [i32, i32, ctypes.POINTER(VariantInfo)],
         "gemv_run_variant": [i32, i32, vp, vp, vp, i64, i64, vp, vp],
+        "gemv_run_variant_ex": [i32, i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_get_device_error": [vp],
         "gemv_ex": [i32, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
         "gemv_ex_host": [i32, vp, vp, vp, vp, i64, i64, vp, ctypes.c_uint, vp],
@@ -361,17 +362,24 @@ def gemv(dtype: str, A, x, scales=None, y=None, stream=None, overlap: bool = Fal
     raise ValueError(dtype)
 
 
-def gemv_run_variant(dtype: str, variant: int, A, x, scales=None, y=None, stream=None):
+def gemv_run_variant(dtype: str, variant: int, A, x, scales=None, y=None, stream=None,
+                     overlap: bool = False):
     """Run one compiled kernel variant (see ``variants``) on tensors.
 
-    'q8row' (one scale per row) runs a variant of the INT8 table."""
+    'q8row' (one scale per row) runs a variant of the INT8 table.  ``overlap``:
+    launch flag GEMV_FLAG_OVERLAP_PRECEDING (as for ``gemv_ex``)."""
     dt = _table_dtype(dtype)
     M, N = _mn(A, dt)
     y = _out(y, M, A.device)
     s_ptr = scales.data_ptr() if scales is not None else None
     if dtype == "q8row":
+        if overlap:
+            raise ValueError("the row-scale variant runner takes no launch flags")
         st = lib().gemv_q8_rowscale_run_variant(variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
                                                 s_ptr, _stream_ptr(stream))
+    elif overlap:
+        st = lib().gemv_run_variant_ex(dt, variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
+                                       s_ptr, FLAG_OVERLAP_PRECEDING, _stream_ptr(stream))
     else:
         st = lib().gemv_run_variant(dt, variant, A.data_ptr(), x.data_ptr(), y.data_ptr(), M, N,
                                     s_ptr, _stream_ptr(stream))

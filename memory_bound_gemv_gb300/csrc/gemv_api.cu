@@ -30,6 +30,8 @@ constexpr int kMaxDevices = 64;
 // Largest x kept in shared memory by the automatic choice; longer x is read
 // through L1 so that several blocks still fit on an SM.
 constexpr int64_t kAutoSmemX = 64 * 1024;
+// Matrices up to this size may take a row band with a capped grid.
+constexpr int64_t kSmallMatrixBytes = 16ll << 20;
 // Widest row group and chunks per thread of the compiled tile kernels.
 constexpr int kTileMaxThreads = 512;
 constexpr int kTileChunks = 8;
@@ -230,6 +232,7 @@ int resident_blocks(DeviceState &d, int dtype, int vid, const Variant &v, size_t
         t_last_cuda_error = static_cast<int>(e);
         return 0;
     }
+    if (v.max_blocks_per_sm > 0 && per_sm > v.max_blocks_per_sm) per_sm = v.max_blocks_per_sm;
     const int total = per_sm * d.sm_count;
     std::lock_guard<std::mutex> g(d.occ_mutex);
     d.occ[key] = total;
@@ -250,7 +253,8 @@ int find_variant(int dtype, int lpr, int xmode, int kind = KIND_VEC, int warps =
 // The automatic choice (measured on GB300 over the workload families):
 // - layouts the vector kernels cannot take: element-wise kernel;
 // - FP32 and FP16 rows that a row-band variant covers exactly (x in
-//   registers): the first such variant in table order (measured best first);
+//   registers): the first such variant in table order (measured best first;
+//   variants with a capped grid only for matrices up to 16 MB);
 // - INT8, and INT4 rows of at least 4 KB: the bulk-copy pipeline, with
 //   8-16 KB of rows per stage;
 // - otherwise row tiles with the narrowest group that requests a whole row at
@@ -271,6 +275,9 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
     if (dtype == DT_F32 || dtype == DT_F16) {
         for (int k = 0; k < n; ++k) {
+            // a capped grid only for small matrices, where the next launch's
+            // blocks starting beside it matter more than bytes in flight
+            if (v[k].max_blocks_per_sm > 0 && M * rb > kSmallMatrixBytes) continue;
             if (v[k].kind == KIND_BAND && variant_fits(v[k], d, dtype, A, x, M, N, scales, smode)) return k;
         }
     }
@@ -560,6 +567,15 @@ gemv_status_t gemv_run_variant(int dtype, int variant, const void *A, const void
 {
     if (variant < 0) return GEMV_ERR_INVALID_VALUE;
     return run(dtype, variant, A, x, y, M, N, scales, stream);
+}
+
+gemv_status_t gemv_run_variant_ex(int dtype, int variant, const void *A, const void *x, float *y,
+                                  int64_t M, int64_t N, const uint16_t *scales, unsigned flags,
+                                  void *stream)
+{
+    if (variant < 0) return GEMV_ERR_INVALID_VALUE;
+    if (flags & ~static_cast<unsigned>(GEMV_FLAG_OVERLAP_PRECEDING)) return GEMV_ERR_INVALID_VALUE;
+    return run(dtype, variant, A, x, y, M, N, scales, stream, flags);
 }
 
 gemv_status_t gemv_probe_read(const void *buf, size_t bytes, unsigned long long *sink, int variant,

@@ -10,6 +10,7 @@ static const Variant kTableF16[] = {
     // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
     // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks); for a given row
     // length the first that fits is the automatic choice (measured best first)
+    MBG_BAND_CAP(DT_F16, 128, 2, 2, 4, 4, 2, "band_t128_c2_g2_w4_b2"),
     MBG_BAND(DT_F16, 256, 1, 2, 4, 2, "band_t256_c1_g2_w4"),
     MBG_BAND(DT_F16, 128, 2, 2, 4, 4, "band_t128_c2_g2_w4"),
     MBG_BAND(DT_F16, 256, 2, 2, 4, 2, "band_t256_c2_g2_w4"),
@@ -19,6 +20,11 @@ static const Variant kTableF16[] = {
     MBG_BAND(DT_F16, 896, 2, 2, 2, 1, "band_t896_c2_g2_w2"),
     MBG_BAND(DT_F16, 448, 4, 2, 2, 1, "band_t448_c4_g2_w2"),
     MBG_BAND(DT_F16, 512, 4, 2, 2, 1, "band_t512_c4_g2_w2"),
+    // band_..._b<n>: at most n blocks per SM, so that the next launch's blocks fit beside them
+    // (small matrices only)
+    MBG_BAND_CAP(DT_F16, 256, 1, 2, 4, 2, 1, "band_t256_c1_g2_w4_b1"),
+    MBG_BAND_CAP(DT_F16, 128, 2, 2, 2, 4, 2, "band_t128_c2_g2_w2_b2"),
+    MBG_BAND_CAP(DT_F16, 256, 2, 2, 4, 2, 1, "band_t256_c2_g2_w4_b1"),
     // staged row bands (tiles of A in shared memory by bulk copies):
     // sband_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles per window>_p<windows in flight>
     MBG_SBAND(DT_F16, 256, 2, 2, 2, 1, 3, "sband_t256_c2_g2_w2_p1"),

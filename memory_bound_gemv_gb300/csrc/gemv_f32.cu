@@ -10,6 +10,7 @@ static const Variant kTableF32[] = {
     // row bands, x in registers: band_t<threads>_c<chunks per thread>_g<rows per
     // tile>_w<tiles in flight> (rows of exactly threads * chunks 16-byte chunks); for a given row
     // length the first that fits is the automatic choice (measured best first)
+    MBG_BAND_CAP(DT_F32, 128, 2, 2, 2, 4, 2, "band_t128_c2_g2_w2_b2"),
     MBG_BAND(DT_F32, 128, 2, 2, 4, 4, "band_t128_c2_g2_w4"),
     MBG_BAND(DT_F32, 256, 1, 2, 4, 2, "band_t256_c1_g2_w4"),
     MBG_BAND(DT_F32, 128, 4, 2, 2, 4, "band_t128_c4_g2_w2"),
@@ -17,6 +18,12 @@ static const Variant kTableF32[] = {
     MBG_BAND(DT_F32, 256, 4, 2, 2, 2, "band_t256_c4_g2_w2"),
     MBG_BAND(DT_F32, 512, 2, 2, 2, 1, "band_t512_c2_g2_w2"),
     MBG_BAND(DT_F32, 512, 4, 2, 2, 1, "band_t512_c4_g2_w2"),
+    // band_..._b<n>: at most n blocks per SM, so that the next launch's blocks fit beside them
+    // (small matrices only)
+    MBG_BAND_CAP(DT_F32, 128, 2, 2, 4, 4, 1, "band_t128_c2_g2_w4_b1"),
+    MBG_BAND_CAP(DT_F32, 128, 2, 2, 4, 4, 2, "band_t128_c2_g2_w4_b2"),
+    MBG_BAND_CAP(DT_F32, 128, 4, 2, 2, 4, 1, "band_t128_c4_g2_w2_b1"),
+    MBG_BAND_CAP(DT_F32, 128, 4, 2, 2, 4, 2, "band_t128_c4_g2_w2_b2"),
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_F32, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_F32, 256, 1, 3, "bulk_t256_r1_s3"),

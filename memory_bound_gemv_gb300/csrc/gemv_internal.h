@@ -88,6 +88,8 @@ struct Variant {
     int stages;          // bulk-pipeline depth (KIND_BULK)
     bool x_regs = false; // bulk pipeline keeps x in registers, not in shared memory
     int tile_rows = 1;   // row bands: consecutive rows per tile
+    int max_blocks_per_sm = 0;  // cap on the persistent grid (0: as many as fit), leaving room
+                                // for the next launch's blocks to start alongside
     bool supports_pdl() const
     {
         return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND || kind == KIND_SBAND;

@@ -1444,11 +1444,12 @@ cudaError_t occupancy_band(int *blocks, size_t smem)
 
 // band_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles in flight>:
 // rows of exactly threads * chunks 16-byte chunks; x in registers
-#define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME)                                                   \
+#define MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, CAP, NAME)                                          \
     Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME, &launch_band<DT, T, CPT, G, TW, MINB>, \
             &smem_limit_band<DT, T, CPT, G, TW, MINB>, KIND_BAND, 0,                               \
             &occupancy_band<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 0,   \
-            false, G}
+            false, G, CAP}
+#define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME) MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, 0, NAME)
 
 template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 void launch_stageband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)

@@ -113,6 +113,27 @@ def test_variant_id_out_of_range():
     assert L.gemv_run_variant(mbg.F16, -1, FAKE, FAKE, FAKE, 4, 8, None, None) == mbg.ERR_INVALID_VALUE
     info = mbg.VariantInfo()
     assert L.gemv_variant_info(mbg.F16, 10_000, ctypes.byref(info)) == mbg.ERR_INVALID_VALUE
+    # the flagged runner checks the variant id and the flags before anything else
+    assert L.gemv_run_variant_ex(mbg.F16, -1, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_run_variant_ex(mbg.F16, 0, FAKE, FAKE, FAKE, 4, 8, None, 2, None) == mbg.ERR_INVALID_VALUE
+
+
+def test_debug_hook_arguments():
+    """The late-writing test kernel rejects bad arguments before any launch;
+    the skip switches take only the documented bits."""
+    L = mbg.lib()
+    assert L.gemv_debug_late_fill(None, 16, 0, 0, None) == mbg.ERR_INVALID_VALUE
+    assert L.gemv_debug_late_fill(FAKE, 6, 0, 0, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_debug_late_fill(FAKE + 2, 16, 0, 0, None) == mbg.ERR_MISALIGNED
+    assert L.gemv_debug_late_fill(FAKE, 0, 0, 0, None) == mbg.OK
+    L.gemv_debug_skip_copies(0)
+    L.gemv_debug_skip_x_copy(0)
+
+
+def test_status_codes_match_the_header():
+    header = open(os.path.join(ROOT, "include", "gemv.h")).read()
+    for code, name in mbg.STATUS.items():
+        assert f"{name} = {code}" in header, name
 
 
 def test_binding_rejects_cpu_tensors():
