@@ -63,7 +63,8 @@ GATE_CYCLES = 100_000           # spin kernel ahead of a timed region (~50 us)
 GRAPH_MAX = 1000                # launches per captured graph
 
 KERNEL_NAMES = {"vec": "mbg_warprow_kernel", "tile": "mbg_rowtile_kernel", "bulk": "mbg_bulkpipe_kernel",
-                "band": "mbg_rowband_kernel", "sband": "mbg_stageband_kernel", "elem": "mbg_elem_kernel"}
+                "band": "mbg_rowband_kernel", "sband": "mbg_stageband_kernel", "elem": "mbg_elem_kernel",
+                "mma": "mbg_mmaband_kernel", "smma": "mbg_mmastage_kernel"}
 
 # the five workload families, in the order they are reported
 CONFIG_WORKLOADS = ["f32_1024", "f16_4096", "f16_up_14336x4096", "f16_down_4096x14336",

@@ -318,20 +318,29 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
  * dealt to the blocks of a persistent grid in grid-stride order;
  * 5 = staged row bands: the same work split, with the tiles streamed into a
  * ring of shared-memory stages by bulk async copies (rows_per_group = rows
- * per window of tiles).
+ * per window of tiles);
+ * 6 = MMA row bands (INT8 / INT4): tiles of two consecutive rows, each warp
+ * takes `unroll` steps of 512 bytes of each row (rows of exactly warps *
+ * unroll * 512 bytes); the exact binary16 codes are multiplied by x and
+ * summed in FP32 by the warp-level MMA instruction (mma.sync m16n8k16), x
+ * held in registers; rows_per_group = rows in flight per thread;
+ * 7 = staged MMA row bands: the same arithmetic, with tiles of one or more
+ * row pairs streamed into a ring of shared-memory stages by bulk async
+ * copies (rows_per_group = rows per window of tiles).
  */
 typedef struct {
     int dtype;           /* gemv_dtype_t */
     int kind;            /* kernel family, see above */
     int threads_per_row; /* threads that share one row: 1..32 (family 0), 1..512 (family 1),
-                            the consumer threads of the block (family 3), the block (families 4, 5) */
+                            the consumer threads of the block (family 3), the block (families 4-7) */
     int rows_per_group;  /* rows one lane group streams together (family 0, x reuse); rows per
-                            stage (family 3); rows in flight per thread (family 4), rows per
-                            window (family 5) */
+                            stage (family 3); rows in flight per thread (families 4, 6), rows
+                            per window (families 5, 7) */
     int unroll;          /* family 0: loads in flight per lane; family 1: chunks per thread;
                             family 3: chunks per consumer thread and row when the variant is
                             specialised for rows of exactly unroll * threads_per_row chunks
-                            (0: any row length); families 4, 5: chunks per thread and row */
+                            (0: any row length); families 4, 5: chunks per thread and row;
+                            families 6, 7: 512-byte steps per warp and row */
     int warps;           /* warps per block */
     int math;            /* 0: operands converted to FP32; 1: binary16 operands into
                             mixed-precision FMAs with FP32 accumulation */

@@ -41,7 +41,7 @@ class GemvError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
 
 
-KINDS = {0: "vec", 1: "tile", 2: "elem", 3: "bulk", 4: "band", 5: "sband"}
+KINDS = {0: "vec", 1: "tile", 2: "elem", 3: "bulk", 4: "band", 5: "sband", 6: "mma", 7: "smma"}
 
 
 class VariantInfo(ctypes.Structure):

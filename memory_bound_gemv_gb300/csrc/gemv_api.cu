@@ -160,7 +160,8 @@ size_t smem_bytes(const Variant &v, int dtype, int64_t N, int64_t groups)
         return static_cast<size_t>(L.total);
     }
     if (v.kind == KIND_BAND) return 0;  // x in registers, static shared memory only
-    if (v.kind == KIND_SBAND) {
+    if (v.kind == KIND_MMA) return 0;  // x in registers, static shared memory only
+    if (v.kind == KIND_SBAND || v.kind == KIND_SMMA) {
         const StageBandLayout L = stageband_layout(v.stages, v.rows_per_group, v.warps, v.tile_rows,
                                                    row_bytes_of(dtype, N), groups, is_quant(dtype));
         return static_cast<size_t>(L.total);
@@ -199,6 +200,19 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
     if (v.kind == KIND_BAND) {
         // every thread takes exactly `unroll` chunks of each row
         return rb / 16 == static_cast<int64_t>(v.lanes_per_row) * v.unroll;  // persistent grid
+    }
+    if (v.kind == KIND_MMA) {
+        // every warp takes exactly `unroll` steps of 512 bytes of each row; INT4
+        // reads the scales of two neighbouring groups as one 4-byte word
+        if (dtype == DT_Q4 && !aligned(scales, 4)) return false;
+        return is_quant(dtype) && rb == static_cast<int64_t>(v.warps) * v.unroll * 512;  // persistent grid
+    }
+    if (v.kind == KIND_SMMA) {
+        if (!is_quant(dtype) || rb != static_cast<int64_t>(v.warps) * v.unroll * 512) return false;
+        // a tile's scales are one bulk copy: rows of scales a multiple of 16 bytes
+        if ((2 * groups) % 16 || !aligned(scales, 16)) return false;
+        const int64_t tx = v.tile_rows * (rb + 2 * groups);
+        return tx < (1 << 20);  // persistent grid
     }
     if (v.kind == KIND_SBAND) {
         if (rb / 16 != static_cast<int64_t>(v.lanes_per_row) * v.unroll) return false;
@@ -288,7 +302,8 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     // INT4 rows
     if ((dtype == DT_Q8 || dtype == DT_Q4) && small_x) {
         for (int k = 0; k < n; ++k) {
-            if ((v[k].kind == KIND_BAND || (v[k].kind == KIND_BULK && v[k].unroll > 0)) &&
+            if ((v[k].kind == KIND_MMA || v[k].kind == KIND_SMMA || v[k].kind == KIND_BAND ||
+                 (v[k].kind == KIND_BULK && v[k].unroll > 0)) &&
                 variant_fits(v[k], d, dtype, A, x, M, N, scales, smode))
                 return k;
         }
@@ -397,7 +412,8 @@ gemv_status_t run(int dtype, int vid, const void *A, const void *x, float *y, in
         blocks = (M + v.warps - 1) / v.warps;
     } else {
         blocks = (M + v.rows_per_block() - 1) / v.rows_per_block();
-        if (v.kind == KIND_TILE || v.kind == KIND_BULK || v.kind == KIND_BAND || v.kind == KIND_SBAND) {
+        if (v.kind == KIND_TILE || v.kind == KIND_BULK || v.kind == KIND_BAND || v.kind == KIND_SBAND ||
+            v.kind == KIND_MMA || v.kind == KIND_SMMA) {
             const int resident = resident_blocks(*d, dtype, vid, v, smem);
             if (resident <= 0) return GEMV_ERR_CUDA;
             if (blocks > resident) blocks = resident;

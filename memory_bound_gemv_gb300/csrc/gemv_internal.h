@@ -17,8 +17,10 @@ enum { XMODE_BULK = 0, XMODE_VEC = 1, XMODE_L1 = 2, XMODE_ELEM = 3, XMODE_REG = 
 // Kernel families: warp/sub-warp rows streamed with a rolling buffer, row
 // tiles walked by a persistent grid, element-wise fallback, bulk-copy
 // pipeline, row bands with x in registers (rows in flight in registers, or
-// staged in shared memory by bulk copies).
-enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3, KIND_BAND = 4, KIND_SBAND = 5 };
+// staged in shared memory by bulk copies), row bands whose quantised
+// products run on the MMA unit (rows in flight in registers, or staged).
+enum { KIND_VEC = 0, KIND_TILE = 1, KIND_ELEM = 2, KIND_BULK = 3, KIND_BAND = 4, KIND_SBAND = 5,
+       KIND_MMA = 6, KIND_SMMA = 7 };
 
 // Dot-product arithmetic: operands converted to FP32, or binary16 operands
 // fed to mixed-precision FMAs with FP32 accumulation.
@@ -92,13 +94,15 @@ struct Variant {
                                 // for the next launch's blocks to start alongside
     bool supports_pdl() const
     {
-        return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND || kind == KIND_SBAND;
+        return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND || kind == KIND_SBAND ||
+               kind == KIND_MMA || kind == KIND_SMMA;
     }
     int rows_per_block() const
     {
         if (kind == KIND_TILE) return warps * 32 / lanes_per_row;
         if (kind == KIND_BULK) return rows_per_group;
-        if (kind == KIND_BAND || kind == KIND_SBAND) return tile_rows;  // one block per tile at most
+        if (kind == KIND_BAND || kind == KIND_SBAND || kind == KIND_MMA || kind == KIND_SMMA)
+            return tile_rows;  // one block per tile at most
         return warps * (32 / lanes_per_row) * rows_per_group;
     }
 };

@@ -1082,6 +1082,345 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
 }
 
 // ---------------------------------------------------------------------------
+// MMA row-band kernel (INT8 / INT4: products on the warp-level MMA unit)
+// ---------------------------------------------------------------------------
+//
+// The quantised row bands spend most of their issue slots on products: one
+// mixed-precision FMA per weight on top of the unpacking (one LOP3 and one
+// binary16 pair operation per two codes).  Here the exact binary16 codes that
+// the unpacking leaves in registers go straight into
+// mma.sync.m16n8k16.f32.f16.f16.f32 as the A fragment: one instruction takes
+// eight codes per lane (256 per warp), multiplies them exactly (binary16 x
+// binary16 products are exact) and accumulates in FP32.  The MMA unit is used
+// as a dot-product engine; the weights still stream from HBM into registers
+// with 16-byte read-only loads, like every other row band.
+//
+// Layout of one step (512 bytes of each of the 2 rows of a tile): a "slot" is
+// 64 contiguous bytes of a row (one 128-column scale group for INT4, half of
+// one for INT8).  The 16 rows of the MMA's A operand are 16 (row, slot)
+// pairs: A-row i < 8 is row i & 1 of the tile, slot 2 (i >> 1); A-row i + 8
+// is the same row, slot 2 (i >> 1) + 1.  Lane (g, t) (g = lane / 4,
+// t = lane % 4) loads the 16-byte chunk t of A-rows g and g + 8 — chunk t of
+// two adjacent slots of row g & 1.  The eight columns of the B operand carry
+// eight slices of x: column n holds the x of slot n (lane (n, t) supplies
+// its chunk t), so A-row g meets its own x in column 2 (g >> 1) and A-row
+// g + 8 in column 2 (g >> 1) + 1: both land in lane (g, g >> 1) of the
+// result, in registers d[0] and d[3].  The other 48 values of the 16 x 8
+// result are products with foreign slices and are never read.  A lane's two
+// slots are adjacent, so their scales are one 4-byte load (INT4: two
+// neighbouring groups) or one scale (INT8: the two halves of one group).
+// The useful values are scaled, summed over the warp per row and over the
+// warps of the block per row.
+//
+// Thread t of the block always multiplies the same slots of every row, so its
+// x fragments are loaded into registers once.  Tiles of 2 consecutive rows are
+// dealt to the blocks of a persistent grid in grid-stride order; each lane
+// keeps its chunks of the next TW tiles in flight in a rolling window of
+// registers (refilled in place, as in the row-band kernel).  Warp w takes the
+// steps w, w + NW, ..., so for every step index the block reads NW * 512
+// contiguous bytes of each row.  The four MMA pairs of a step go into two
+// accumulators whose first MMA starts from zero.  Rows must be exactly
+// NW * SPW * 512 bytes.
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B (the accumulator input is zero)
+__device__ __forceinline__ void mma_m16n8k16_f16_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                       uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    const float z = 0.f;
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%10, %10, %10, %10};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+// The code unpacking of q8_codes_h2 / q4_codes_h2 as volatile asm: kept in
+// program order between the (volatile) MMAs, so that a word's codes are
+// unpacked right before its MMAs and only one word's codes are live at a time.
+__device__ __forceinline__ uint32_t vlop3_sel_xor(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm volatile("lop3.b32 %0, %1, %2, %3, 0x6C;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t vhsub2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm volatile("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t vhfma2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm volatile("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t vprmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm volatile("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ void q4_codes_h2_ordered(uint32_t w, uint32_t (&h)[4])
+{
+    uint32_t v;
+    asm volatile("shr.b32 %0, %1, 8;" : "=r"(v) : "r"(w));
+    h[0] = vhsub2(vlop3_sel_xor(w, 0x64086408u, 0x000F000Fu), 0x64086408u);
+    h[1] = vhfma2(vlop3_sel_xor(w, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
+    h[2] = vhsub2(vlop3_sel_xor(v, 0x64086408u, 0x000F000Fu), 0x64086408u);
+    h[3] = vhfma2(vlop3_sel_xor(v, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
+}
+__device__ __forceinline__ void q8_codes_h2_ordered(uint32_t w, uint32_t (&h)[2])
+{
+    uint32_t u;
+    asm volatile("xor.b32 %0, %1, 0x80808080;" : "=r"(u) : "r"(w));
+    h[0] = vhsub2(vprmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+    h[1] = vhsub2(vprmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+// Sums each of the TW values over the 16 lanes that share lane bit 2 (lanes
+// of one tile row).  The first log2 TW lane bits of (4, 3, 1) split the
+// values (a lane keeps half of them at each of those steps and adds its
+// partner's copy), the remaining bits of (4, 3, 1, 0) are a plain XOR
+// butterfly.  Afterwards the lanes whose remaining bits are 0 hold the sums;
+// the value a lane holds belongs to tile (bit 4, bit 3, bit 1) of its lane
+// index, taken in that order.
+template <int TW>
+__device__ __forceinline__ float mma_rows_sum(float (&v)[TW], int lane)
+{
+    static_assert(TW == 1 || TW == 2 || TW == 4 || TW == 8, "tiles per window: 1, 2, 4 or 8");
+    constexpr int kDist[4] = {16, 8, 2, 1};
+    float w[TW];
+#pragma unroll
+    for (int i = 0; i < TW; ++i) w[i] = v[i];
+    int step = 0;
+#pragma unroll
+    for (int k = TW; k > 1; k >>= 1, ++step) {
+        const int d = kDist[step];
+        const bool up = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < k / 2; ++i) {
+            const float keep = up ? w[i + k / 2] : w[i];
+            const float send = up ? w[i] : w[i + k / 2];
+            w[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
+    float s = w[0];
+#pragma unroll
+    for (; step < 4; ++step) s += __shfl_xor_sync(0xffffffffu, s, kDist[step]);
+    return s;
+}
+
+// Tile index within a window of TW tiles held by a lane after mma_rows_sum,
+// and the lane bits that must be 0 for the lane to hold a sum.
+template <int TW>
+__device__ __forceinline__ int mma_rows_tile(int lane)
+{
+    if constexpr (TW == 8) return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 1) & 1);
+    if constexpr (TW == 4) return ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+    if constexpr (TW == 2) return (lane >> 4) & 1;
+    return 0;
+}
+template <int TW>
+constexpr int mma_rows_rest()
+{
+    return TW == 8 ? 0x1 : TW == 4 ? 0x3 : TW == 2 ? 0xB : 0x1B;
+}
+
+// 32-bit load into a register that already holds the slot's previous value.
+__device__ __forceinline__ void ld_u32_into(uint32_t &v, const void *p)
+{
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "+r"(v) : "l"(p));
+}
+__device__ __forceinline__ void ld_u32_if(uint32_t &v, const void *p, bool pred)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.u32 %0, [%1];\n}"
+                 : "+r"(v)
+                 : "l"(p), "r"(static_cast<int>(pred)));
+}
+
+template <int DT, int NW, int SPW, int TW, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvArgs p)
+{
+    static_assert(DT == DT_Q8 || DT == DT_Q4, "quantised weights only");
+    static_assert(NW >= 1 && NW <= 32, "block shape");
+    constexpr int XV = DT == DT_Q4 ? 4 : 2;  // 16-byte x vectors per 16-byte chunk of codes
+    constexpr int ROWB = NW * SPW * 512;     // bytes per row
+    constexpr int U = 2 * TW;                // rows per window
+    // INT4: a lane's two slots are two neighbouring scale groups (one 4-byte
+    // load, groups a multiple of 8); INT8: both halves of one group, or the
+    // row's one scale
+    constexpr bool PAIR = DT == DT_Q4;
+
+    __shared__ float part[2][U][NW];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int rsel = g & 1;          // tile row whose chunks this lane loads
+    const bool use = t == (g >> 1);  // this lane holds its A-rows' results
+
+    const int64_t grid = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t ntiles = (p.M + 1) / 2;
+    const int I = static_cast<int>(b < ntiles ? (ntiles - 1 - b) / grid + 1 : 0);
+
+    pdl_trigger();
+    if (tid < TW && tid < I) {
+        const int64_t row0 = (b + tid * grid) * 2;
+        const int64_t rows = p.M - row0 < 2 ? p.M - row0 : 2;
+        prefetch_l2(static_cast<const unsigned char *>(p.A) + row0 * ROWB, static_cast<uint32_t>(rows * ROWB));
+    }
+    if (!p.pdl) pdl_wait();
+
+    // byte offset of this lane's scale(s) of step s within the scales of its row
+    int sidx[SPW];
+#pragma unroll
+    for (int s = 0; s < SPW; ++s) sidx[s] = (((((warp + s * NW) * 8 + 2 * (g >> 1)) * 4) >> p.scale_shift) * 2);
+    const int64_t sgrp = p.groups;
+
+    uint4 a[TW][SPW][2];
+    uint32_t sc[TW][SPW];  // binary16 scale bits (a pair, or one in the low half)
+#pragma unroll
+    for (int w = 0; w < TW; ++w)
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            a[w][s][0] = a[w][s][1] = make_uint4(0u, 0u, 0u, 0u);
+            sc[w][s] = 0u;
+        }
+    int in = 0;
+    const unsigned char *an = static_cast<const unsigned char *>(p.A) + (b * 2 + rsel) * ROWB + warp * 512 +
+                              (g >> 1) * 128 + t * 16;
+    const int64_t astep = grid * 2 * ROWB;
+    const unsigned char *sn = reinterpret_cast<const unsigned char *>(p.scales + (b * 2 + rsel) * sgrp);
+    const int64_t sstep = grid * 2 * sgrp * 2;
+    // FULL: the tile and both its rows exist (no predicates)
+    auto load_tile = [&](int w, auto full) {
+        constexpr bool FULL = decltype(full)::value;
+        const bool ok = FULL || (in < I && (b + static_cast<int64_t>(in) * grid) * 2 + rsel < p.M);
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            const unsigned char *q = an + s * NW * 512;
+            if constexpr (FULL) {
+                ld_stream16_into(a[w][s][0], q);
+                ld_stream16_into(a[w][s][1], q + 64);
+                if constexpr (PAIR) ld_u32_into(sc[w][s], sn + sidx[s]);
+                else ld_u16_into(sc[w][s], sn + sidx[s]);
+            } else {
+                ld_stream16_if(a[w][s][0], q, ok);
+                ld_stream16_if(a[w][s][1], q + 64, ok);
+                if constexpr (PAIR) ld_u32_if(sc[w][s], sn + sidx[s], ok);
+                else ld_u16_if(sc[w][s], sn + sidx[s], ok);
+            }
+        }
+        asm volatile("add.s64 %0, %0, %1;" : "+l"(sn) : "l"(sstep));
+        asm volatile("add.s64 %0, %0, %1;" : "+l"(an) : "l"(astep));
+        ++in;
+    };
+#pragma unroll
+    for (int w = 0; w < TW; ++w) load_tile(w, std::false_type{});
+    if (p.pdl) pdl_wait();
+
+    // B fragments: chunk t of x slot g of each of this lane's steps (read
+    // after the wait: the preceding kernel may have written x); INT4
+    // re-paired four columns apart, the order in which the codes unpack
+    uint4 xr[SPW][XV];
+    {
+        const unsigned char *xs = static_cast<const unsigned char *>(p.x);
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            // first code of the chunk: byte (step * 512 + slot * 64 + t * 16) of the row
+            const int64_t cbyte = static_cast<int64_t>(warp + s * NW) * 512 + g * 64 + t * 16;
+            const int64_t col = DT == DT_Q4 ? cbyte * 2 : cbyte;
+#pragma unroll
+            for (int v = 0; v < XV; ++v) {
+                xr[s][v] = ld_l2_16(xs + col * 2 + v * 16);
+                if constexpr (DT == DT_Q4) xr[s][v] = pair_x_vec(xr[s][v]);
+            }
+        }
+    }
+
+    // tile slot w times x: this lane's share of its row.  Every lane applies
+    // its scales (no divergent branch); the lanes that hold no result (their
+    // sums mix foreign slices) give 0 through one select per tile.
+    auto tile_dot = [&](int w) -> float {
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            float d[2][4];
+            const uint32_t w0[4] = {a[w][s][0].x, a[w][s][0].y, a[w][s][0].z, a[w][s][0].w};
+            const uint32_t w1[4] = {a[w][s][1].x, a[w][s][1].y, a[w][s][1].z, a[w][s][1].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float(&dk)[4] = d[k & 1];
+                if constexpr (DT == DT_Q4) {
+                    uint32_t h[4], h8[4];
+                    q4_codes_h2_ordered(w0[k], h);
+                    q4_codes_h2_ordered(w1[k], h8);
+                    if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], xr[s][k].x, xr[s][k].y);
+                    else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], xr[s][k].x, xr[s][k].y);
+                    mma_m16n8k16_f16(dk, h[2], h8[2], h[3], h8[3], xr[s][k].z, xr[s][k].w);
+                } else {
+                    uint32_t h[2], h8[2];
+                    q8_codes_h2_ordered(w0[k], h);
+                    q8_codes_h2_ordered(w1[k], h8);
+                    const uint4 &x = xr[s][k >> 1];
+                    const uint32_t b0 = (k & 1) ? x.z : x.x, b1 = (k & 1) ? x.w : x.y;
+                    if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], b0, b1);
+                    else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], b0, b1);
+                }
+            }
+            if constexpr (PAIR) {
+                const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc[w][s]));
+                acc = fmaf(sf.x, d[0][0] + d[1][0], acc);
+                acc = fmaf(sf.y, d[0][3] + d[1][3], acc);
+            } else {
+                acc = fmaf(half_bits_to_float(sc[w][s]), (d[0][0] + d[1][0]) + (d[0][3] + d[1][3]), acc);
+            }
+        }
+        return use ? acc : 0.f;
+    };
+
+    int half = 0;
+    for (int i0 = 0; i0 < I; i0 += TW) {
+        // every tile of this window and of the next one exists in full
+        const int last = i0 + 2 * TW - 1;
+        const bool full = last < I && (b + static_cast<int64_t>(last) * grid) * 2 + 2 <= p.M;
+        float acc[TW];
+        auto window = [&](auto fl) {
+#pragma unroll
+            for (int w = 0; w < TW; ++w) {
+                acc[w] = tile_dot(w);
+                load_tile(w, fl);
+            }
+        };
+        if (full) window(std::true_type{});
+        else window(std::false_type{});
+        const float s = mma_rows_sum<TW>(acc, lane);
+        // lanes whose butterfly bits are all 0 hold (tile, row) sums
+        if ((lane & mma_rows_rest<TW>()) == 0) part[half][mma_rows_tile<TW>(lane) * 2 + rsel][warp] = s;
+        __syncthreads();
+        if (tid < U) {
+            const int i = i0 + tid / 2;
+            const int64_t row = (b + static_cast<int64_t>(i) * grid) * 2 + (tid & 1);
+            if (i < I && row < p.M) {
+                float v = 0.f;
+#pragma unroll
+                for (int q = 0; q < NW; ++q) v += part[half][tid][q];
+                p.y[row] = v;
+            }
+        }
+        half ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Staged row-band kernel (x in registers, tiles of A staged by bulk copies)
 // ---------------------------------------------------------------------------
 //
@@ -1244,6 +1583,213 @@ __global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p
         if (tid < U) {
             const int64_t i = i0 + tid / G;
             const int64_t row = (b + i * grid) * G + tid % G;
+            if (i < I && row < p.M) {
+                float v = 0.f;
+#pragma unroll
+                for (int q = 0; q < NW; ++q) v += part[(half * U + tid) * NW + q];
+                p.y[row] = v;
+            }
+        }
+        half ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Staged MMA row-band kernel (INT8 / INT4)
+// ---------------------------------------------------------------------------
+//
+// The MMA row band's arithmetic (exact binary16 codes into
+// mma.sync.m16n8k16, eight slices of x in the eight B columns), with tiles of
+// RP row pairs streamed into a ring of (PF + 1) TW shared-memory stages by
+// bulk async copies (the staged row band's pipeline: thread 0 issues, every
+// wait bounded, the block barrier that closes a window of TW tiles frees its
+// stages).  The bytes in flight cost no registers, so the lookahead (PF
+// windows) can cover the memory latency while enough warps stay resident to
+// keep the MMA and unpacking pipes busy; the row pairs of a tile share the B
+// fragments and the per-tile bookkeeping.
+//
+// Slots in a stage: lane (g, t) reads chunk t of slots k and 4 + k of row
+// g & 1 of each row pair, with k = (g >> 1) ^ (g & 1): the two rows of a
+// pair sit a multiple of 128 bytes apart, and flipping the slot order of the
+// odd row puts the eight lanes of every quarter-warp on 128 distinct bytes of
+// bank space (no bank conflicts).  B column 2k carries the x of slot k and
+// column 2k + 1 that of slot 4 + k, so the results of A-rows g and g + 8 land
+// in lane (g, k), registers d[0] and d[3].
+template <int DT, int NW, int SPW, int RP, int TW, int PF, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) mbg_mmastage_kernel(const GemvArgs p)
+{
+    static_assert(DT == DT_Q8 || DT == DT_Q4, "quantised weights only");
+    static_assert(NW >= 1 && NW <= 32, "block shape");
+    constexpr int G = 2 * RP;                // rows per tile
+    constexpr int XV = DT == DT_Q4 ? 4 : 2;  // 16-byte x vectors per 16-byte chunk of codes
+    constexpr int ROWB = NW * SPW * 512;     // bytes per row
+    constexpr int U = G * TW;                // rows per window
+    constexpr int V = RP * TW;               // row-pair partials per lane and window
+    constexpr int S = (PF + 1) * TW;         // stages
+    static_assert(V == 1 || V == 2 || V == 4 || V == 8, "row pairs per window: 1, 2, 4 or 8");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const StageBandLayout L = stageband_layout(S, U, NW, G, ROWB, p.groups, true);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    float *part = reinterpret_cast<float *>(smem + L.part);  // [2][U][NW]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int rsel = g & 1;                    // row of each pair this lane reads
+    const int kslot = (g >> 1) ^ rsel;         // its slots: kslot and 4 + kslot
+    const bool use = t == kslot;               // this lane holds its A-rows' results
+    const int xslot = (g >> 1) + 4 * (g & 1);  // slot of x in B column g
+    const int64_t grid = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t ntiles = (p.M + G - 1) / G;
+    const int I = static_cast<int>(b < ntiles ? (ntiles - 1 - b) / grid + 1 : 0);  // tiles b + i * grid
+    const int64_t sgrp = p.groups;
+
+    int issued = 0;  // thread 0: tiles whose copies have been issued
+    auto issue = [&](int i) {
+        const int s = i % S;
+        const int64_t row0 = (b + i * grid) * G;
+        const int64_t rows = p.M - row0 < G ? p.M - row0 : G;
+        const uint32_t abytes = static_cast<uint32_t>(rows * ROWB);
+        const uint32_t sbytes = static_cast<uint32_t>(rows * sgrp * 2);
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, abytes + sbytes);
+        if (i == 0 && (p.skip_copies & SKIP_STAGE)) return;  // test hook: the wait must run out
+        bulk_copy_g2s(smem_addr(smem + L.stage + s * L.stage_bytes),
+                      static_cast<const unsigned char *>(p.A) + row0 * ROWB, abytes, bar);
+        bulk_copy_g2s(smem_addr(smem + L.stage + s * L.stage_bytes + L.scale_off), p.scales + row0 * sgrp,
+                      sbytes, bar);
+    };
+
+    pdl_trigger();
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(&full[s]), 1);
+        if (I > 0) {
+            // the first tile into L2 while the preceding kernel drains (a hint)
+            const int64_t row0 = b * G;
+            const int64_t rows = p.M - row0 < G ? p.M - row0 : G;
+            prefetch_l2(static_cast<const unsigned char *>(p.A) + row0 * ROWB, static_cast<uint32_t>(rows * ROWB));
+        }
+    }
+    if (!p.pdl) pdl_wait();
+    if (tid == 0)
+        for (; issued < S && issued < I; ++issued) issue(issued);
+    __syncthreads();  // barriers initialised before anyone waits on them
+    if (p.pdl) pdl_wait();
+
+    // B fragments: chunk t of x slot `xslot` of each of this lane's steps
+    // (after the wait: the preceding kernel may have written x); INT4
+    // re-paired four columns apart, the order in which the codes unpack
+    uint4 xr[SPW][XV];
+    {
+        const unsigned char *xs = static_cast<const unsigned char *>(p.x);
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            const int64_t cbyte = static_cast<int64_t>(warp + s * NW) * 512 + xslot * 64 + t * 16;
+            const int64_t col = DT == DT_Q4 ? cbyte * 2 : cbyte;
+#pragma unroll
+            for (int v = 0; v < XV; ++v) {
+                xr[s][v] = ld_l2_16(xs + col * 2 + v * 16);
+                if constexpr (DT == DT_Q4) xr[s][v] = pair_x_vec(xr[s][v]);
+            }
+        }
+    }
+    // shared-space offsets within a stage (row pair 0): this lane's chunk of
+    // slot kslot of step s (slot 4 + kslot is 256 bytes further), its two scales
+    const uint32_t stage0 = smem_addr(smem + L.stage);
+    uint32_t aoff[SPW], soff[SPW][2];
+#pragma unroll
+    for (int s = 0; s < SPW; ++s) {
+        const int slot0 = (warp + s * NW) * 8 + kslot;
+        aoff[s] = static_cast<uint32_t>(rsel * ROWB + (warp + s * NW) * 512 + kslot * 64 + t * 16);
+        soff[s][0] = static_cast<uint32_t>(L.scale_off + rsel * sgrp * 2 + ((slot0 * 4) >> p.scale_shift) * 2);
+        soff[s][1] = static_cast<uint32_t>(L.scale_off + rsel * sgrp * 2 + (((slot0 + 4) * 4) >> p.scale_shift) * 2);
+    }
+    const uint32_t pair_a = 2u * ROWB;                          // next row pair's weights
+    const uint32_t pair_s = static_cast<uint32_t>(4 * sgrp);    // and scales
+
+    int half = 0;
+    for (int i0 = 0; i0 < I; i0 += TW) {
+        bool ok = true;
+        float acc[V];
+#pragma unroll
+        for (int w = 0; w < TW; ++w) {
+            const int i = i0 + w;
+#pragma unroll
+            for (int r = 0; r < RP; ++r) acc[w * RP + r] = 0.f;
+            if (i < I) {
+                const int s = i % S;
+                ok &= mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((i / S) & 1), p.wait_limit_ns);
+                const uint32_t st = stage0 + static_cast<uint32_t>(s) * L.stage_bytes;
+                // a row past the end of A holds stale bytes: its sum is never stored
+#pragma unroll
+                for (int q = 0; q < SPW; ++q) {
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) {
+                        const uint4 a0 = lds128(st + aoff[q] + r * pair_a);
+                        const uint4 a1 = lds128(st + aoff[q] + r * pair_a + 256);
+                        const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w};
+                        const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w};
+                        float d[2][4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            float(&dk)[4] = d[k & 1];
+                            if constexpr (DT == DT_Q4) {
+                                uint32_t h[4], h8[4];
+                                q4_codes_h2_ordered(w0[k], h);
+                                q4_codes_h2_ordered(w1[k], h8);
+                                if (k < 2)
+                                    mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], xr[q][k].x, xr[q][k].y);
+                                else
+                                    mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], xr[q][k].x, xr[q][k].y);
+                                mma_m16n8k16_f16(dk, h[2], h8[2], h[3], h8[3], xr[q][k].z, xr[q][k].w);
+                            } else {
+                                uint32_t h[2], h8[2];
+                                q8_codes_h2_ordered(w0[k], h);
+                                q8_codes_h2_ordered(w1[k], h8);
+                                const uint4 &x = xr[q][k >> 1];
+                                const uint32_t b0 = (k & 1) ? x.z : x.x, b1 = (k & 1) ? x.w : x.y;
+                                if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], b0, b1);
+                                else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], b0, b1);
+                            }
+                        }
+                        const uint32_t sp = st + r * pair_s;
+                        float &av = acc[w * RP + r];
+                        av = fmaf(lds_half_as_float(sp + soff[q][0]), d[0][0] + d[1][0], av);
+                        av = fmaf(lds_half_as_float(sp + soff[q][1]), d[0][3] + d[1][3], av);
+                    }
+                }
+            }
+        }
+        // lanes that hold no result (their sums mix foreign slices) give 0
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = use ? acc[v] : 0.f;
+        // value v of a lane: row 2 (v % RP) + rsel of tile v / RP of the window
+        const float sum = mma_rows_sum<V>(acc, lane);
+        if ((lane & mma_rows_rest<V>()) == 0) {
+            const int v = mma_rows_tile<V>(lane);
+            part[(half * U + (v / RP) * G + 2 * (v % RP) + rsel) * NW + warp] = sum;
+        }
+        // every thread has read the window's stages and written its partials;
+        // a wait that gave up anywhere makes the whole block leave here
+        if (__syncthreads_or(ok ? 0 : 1)) {
+            if (tid == 0) {
+                report_error(p.err, DEVERR_TIMEOUT);
+                bool drained = true;
+                for (int j = i0; j < issued; ++j) {
+                    if (j == 0 && (p.skip_copies & SKIP_STAGE)) continue;  // never issued
+                    drained &= mbar_wait_bounded(smem_addr(&full[j % S]), static_cast<uint32_t>((j / S) & 1),
+                                                 p.wait_limit_ns);
+                }
+                if (!drained) report_error(p.err, DEVERR_UNDRAINED);
+            }
+            return;
+        }
+        if (tid == 0)
+            for (; issued < i0 + S + TW && issued < I; ++issued) issue(issued);  // into the window's stages
+        if (tid < U) {
+            const int i = i0 + tid / G;
+            const int64_t row = (b + static_cast<int64_t>(i) * grid) * G + tid % G;
             if (i < I && row < p.M) {
                 float v = 0.f;
 #pragma unroll
@@ -1451,6 +1997,32 @@ cudaError_t occupancy_band(int *blocks, size_t smem)
             false, G, CAP}
 #define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME) MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, 0, NAME)
 
+template <int DT, int NW, int SPW, int TW, int MINB>
+void launch_mmaband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    launch_maybe_pdl(mbg_mmaband_kernel<DT, NW, SPW, TW, MINB>, a, grid, NW * 32, smem, s, pdl);
+}
+
+template <int DT, int NW, int SPW, int TW, int MINB>
+cudaError_t smem_limit_mmaband(int)
+{
+    return cudaSuccess;  // static shared memory only
+}
+
+template <int DT, int NW, int SPW, int TW, int MINB>
+cudaError_t occupancy_mmaband(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_mmaband_kernel<DT, NW, SPW, TW, MINB>,
+                                                         NW * 32, smem);
+}
+
+// mma_w<warps>_s<steps per warp>_t<tiles in flight>_m<min blocks per SM>: rows
+// of exactly warps * steps * 512 bytes; x in registers; products on the MMA unit
+#define MBG_MMA(DT, NW, SPW, TW, MINB, NAME)                                                          \
+    Variant{DT, (NW) * 32, 2 * (TW), SPW, NW, XMODE_REG, NAME, &launch_mmaband<DT, NW, SPW, TW, MINB>, \
+            &smem_limit_mmaband<DT, NW, SPW, TW, MINB>, KIND_MMA, 0,                                   \
+            &occupancy_mmaband<DT, NW, SPW, TW, MINB>, MATH_MIXED, 0, false, 2, 0}
+
 template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 void launch_stageband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
@@ -1479,6 +2051,35 @@ cudaError_t occupancy_stageband(int *blocks, size_t smem)
             &launch_stageband<DT, T, CPT, G, TW, PF, MINB>, &smem_limit_stageband<DT, T, CPT, G, TW, PF, MINB>, \
             KIND_SBAND, 0, &occupancy_stageband<DT, T, CPT, G, TW, PF, MINB>,                           \
             (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, ((PF) + 1) * (TW), false, G}
+
+template <int DT, int NW, int SPW, int RP, int TW, int PF, int MINB>
+void launch_mmastage(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    launch_maybe_pdl(mbg_mmastage_kernel<DT, NW, SPW, RP, TW, PF, MINB>, a, grid, NW * 32, smem, s, pdl);
+}
+
+template <int DT, int NW, int SPW, int RP, int TW, int PF, int MINB>
+cudaError_t smem_limit_mmastage(int bytes)
+{
+    return cudaFuncSetAttribute(mbg_mmastage_kernel<DT, NW, SPW, RP, TW, PF, MINB>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DT, int NW, int SPW, int RP, int TW, int PF, int MINB>
+cudaError_t occupancy_mmastage(int *blocks, size_t smem)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        blocks, mbg_mmastage_kernel<DT, NW, SPW, RP, TW, PF, MINB>, NW * 32, smem);
+}
+
+// smma_w<warps>_s<steps per warp>_r<row pairs per tile>_t<tiles per
+// window>_p<windows in flight>_m<min blocks per SM>: rows of exactly warps *
+// steps * 512 bytes; (p + 1) t stages of 2 r rows and their scales
+#define MBG_SMMA(DT, NW, SPW, RP, TW, PF, MINB, NAME)                                                     \
+    Variant{DT, (NW) * 32, 2 * (RP) * (TW), SPW, NW, XMODE_REG, NAME,                                    \
+            &launch_mmastage<DT, NW, SPW, RP, TW, PF, MINB>, &smem_limit_mmastage<DT, NW, SPW, RP, TW, PF, MINB>, \
+            KIND_SMMA, 0, &occupancy_mmastage<DT, NW, SPW, RP, TW, PF, MINB>, MATH_MIXED, ((PF) + 1) * (TW),  \
+            false, 2 * (RP), 0}
 
 #define MBG_VEC(DT, LPR, RPW, U, W, XM, NAME)                                              \
     Variant{DT, LPR, RPW, U, W, XM, NAME, &launch_vec<DT, LPR, RPW, U, W, XM>,              \

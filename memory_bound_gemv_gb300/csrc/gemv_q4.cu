@@ -34,6 +34,19 @@ static const Variant kTableQ4[] = {
     MBG_SBAND(DT_Q4, 448, 1, 2, 2, 2, 1, "sband_t448_c1_g2_w2_p2"),
     MBG_SBAND(DT_Q4, 224, 2, 2, 2, 2, 3, "sband_t224_c2_g2_w2_p2"),
     MBG_SBAND(DT_Q4, 224, 2, 1, 4, 2, 3, "sband_t224_c2_g1_w4_p2"),
+    // MMA row bands (products on the MMA unit), mma_w<warps>_s<steps per
+    // warp>_t<tiles in flight>_m<min blocks per SM>: rows of exactly warps *
+    // steps * 512 bytes (explicit choice: within noise of the bulk pipelines)
+    MBG_MMA(DT_Q4, 14, 1, 4, 1, "mma_w14_s1_t4_m1"),
+    MBG_MMA(DT_Q4, 4, 1, 4, 1, "mma_w4_s1_t4_m1"),
+    MBG_MMA(DT_Q4, 4, 1, 4, 4, "mma_w4_s1_t4_m4"),
+    MBG_MMA(DT_Q4, 14, 1, 2, 2, "mma_w14_s1_t2_m2"),
+    // staged MMA row bands, smma_w<warps>_s<steps per warp>_r<row pairs per
+    // tile>_t<tiles per window>_p<windows in flight>_m<min blocks per SM>:
+    // rows of exactly warps * steps * 512 bytes (explicit choice)
+    MBG_SMMA(DT_Q4, 4, 1, 4, 2, 1, 3, "smma_w4_s1_r4_t2_p1_m3"),
+    MBG_SMMA(DT_Q4, 14, 1, 2, 2, 1, 1, "smma_w14_s1_r2_t2_p1_m1"),
+    MBG_SMMA(DT_Q4, 7, 2, 2, 2, 1, 2, "smma_w7_s2_r2_t2_p1_m2"),
     // general variants (explicit choice, and the fallbacks of the automatic one)
     MBG_BULK(DT_Q4, 256, 1, 4, "bulk_t256_r1_s4"),
     MBG_BULK(DT_Q4, 256, 1, 3, "bulk_t256_r1_s3"),

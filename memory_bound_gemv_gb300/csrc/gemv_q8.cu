@@ -9,6 +9,11 @@ namespace mbg {
 static const Variant kTableQ8[] = {
     // the automatic choice takes, in table order, the first row band or
     // fixed-count bulk pipeline that covers the row exactly (measured best first)
+    // MMA row bands (products on the MMA unit), mma_w<warps>_s<steps per
+    // warp>_t<tiles in flight>_m<min blocks per SM>: rows of exactly warps *
+    // steps * 512 bytes (measured best of every design at 4096 and 14336 columns)
+    MBG_MMA(DT_Q8, 8, 1, 4, 2, "mma_w8_s1_t4_m2"),
+    MBG_MMA(DT_Q8, 28, 1, 2, 1, "mma_w28_s1_t2_m1"),
     MBG_BAND(DT_Q8, 256, 1, 2, 4, 2, "band_t256_c1_g2_w4"),
     // bulk-copy pipelines specialised for rows of exactly f * t chunks:
     // bulk_t<consumer threads>_r<rows per stage>_s<stages>_f<chunks per thread>
@@ -30,6 +35,15 @@ static const Variant kTableQ8[] = {
     MBG_SBAND(DT_Q8, 448, 2, 2, 2, 1, 1, "sband_t448_c2_g2_w2_p1"),
     MBG_SBAND(DT_Q8, 448, 2, 1, 2, 2, 1, "sband_t448_c2_g1_w2_p2"),
     MBG_SBAND(DT_Q8, 896, 1, 1, 2, 2, 1, "sband_t896_c1_g1_w2_p2"),
+    // other MMA row bands (explicit choice)
+    MBG_MMA(DT_Q8, 8, 1, 2, 4, "mma_w8_s1_t2_m4"),
+    MBG_MMA(DT_Q8, 4, 2, 2, 4, "mma_w4_s2_t2_m4"),
+    MBG_MMA(DT_Q8, 14, 2, 2, 2, "mma_w14_s2_t2_m2"),
+    // staged MMA row bands, smma_w<warps>_s<steps per warp>_r<row pairs per
+    // tile>_t<tiles per window>_p<windows in flight>_m<min blocks per SM>:
+    // rows of exactly warps * steps * 512 bytes (explicit choice)
+    MBG_SMMA(DT_Q8, 8, 1, 2, 2, 2, 2, "smma_w8_s1_r2_t2_p2_m2"),
+    MBG_SMMA(DT_Q8, 14, 2, 1, 2, 2, 1, "smma_w14_s2_r1_t2_p2_m1"),
     // general variants (explicit choice, and the fallbacks of the automatic one)
     // bulk-copy pipelines: bulk_t<consumer threads>_r<rows per stage>_s<stages>
     MBG_BULK(DT_Q8, 256, 1, 3, "bulk_t256_r1_s3"),

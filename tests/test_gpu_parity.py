@@ -296,18 +296,19 @@ def _timeout_then_recovery(run, check, mask):
 @pytest.mark.parametrize("dtype,M,N", [("q4", 300, 4096), ("q8", 300, 4096), ("q4", 37, 14336),
                                        ("f16", 300, 4096)])
 def test_bulk_pipeline_stage_wait_runs_out(dtype, M, N):
-    """Every bulk-pipeline and staged row-band variant: the first weight stage
-    of every block is armed but never copied.  Bulk pipeline: the consumers
-    give up, the producer gives up on the reduced-stage barrier, drains its
-    other stages and the block exits.  Staged row band: every thread gives up
-    on the stage, the block agrees at the window barrier, thread 0 drains the
-    other stages and the block exits."""
+    """Every bulk-pipeline, staged row-band and staged MMA row-band variant:
+    the first weight stage of every block is armed but never copied.  Bulk
+    pipeline: the consumers give up, the producer gives up on the
+    reduced-stage barrier, drains its other stages and the block exits.
+    Staged row bands (CUDA-core or MMA products): every thread gives up on the
+    stage, the block agrees at the window barrier, thread 0 drains the other
+    stages and the block exits."""
     inp = synth.make(synth.random_case(dtype, M, N, 515 + M))
     t = upload(dtype, inp)
     y_ref, den = reference(dtype, inp, M, N)
     ran = 0
     for v in mbg.variants(dtype):
-        if v["kind"] not in ("bulk", "sband"):
+        if v["kind"] not in ("bulk", "sband", "smma"):
             continue
         try:
             mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], t.get("scales"))
