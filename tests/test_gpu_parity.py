@@ -25,7 +25,7 @@ DTYPES = ("f32", "f16", "q8", "q4", "f16x32", "q8row")
 # and row pitches that are / are not multiples of 16 bytes.
 SHAPES = [(1, 1), (1, 8), (2, 3), (3, 7), (5, 32), (7, 33), (9, 64), (31, 65), (32, 126),
           (33, 128), (63, 130), (64, 254), (65, 256), (127, 258), (129, 512), (130, 1000),
-          (257, 1024), (64, 2056), (33, 4096), (300, 4160), (17, 8200)]
+          (257, 1024), (64, 2056), (33, 4096), (300, 4160), (17, 8200), (37, 14336)]
 
 
 def _shapes(dtype):
@@ -221,6 +221,52 @@ def test_identity_is_exact(dtype):
             continue
         torch.cuda.synchronize()
         assert np.array_equal(y.cpu().numpy().astype(np.float64), expect), v["name"]
+
+
+@pytest.mark.parametrize("dtype", ("q8", "q4"))
+def test_exact_cases_every_variant(dtype):
+    """Cases with exact answers, at a row length every quantised kernel family
+    serves (4096 columns, 37 rows: an odd last tile), for every variant:
+    - an identity (code 1 on the diagonal) with power-of-two scales that
+      differ per (row, group) times an x of binary16 subnormals and normals:
+      y_i = s_i x_i exactly (the MMA path multiplies binary16 operands, so a
+      flushed subnormal or a wrong group scale would show);
+    - rows of zero codes (with nonzero scales and x) come out exactly 0."""
+    M, N = 37, 4096
+    g = synth.n_groups(N)
+    # x: every fourth value a binary16 subnormal (2^-24 .. 2^-15), the rest normal
+    xv = synth.normal(404, 2, 0, N, 1.0)
+    sub = (synth.integers(404, 3, 0, N, 1, 1023) * 2.0 ** -24)
+    xv[::4] = sub[::4] * np.where(np.arange(N)[::4] % 8 == 0, 1.0, -1.0)
+    xb = synth.to_f16_bits(xv)
+    xd = xb.view(np.float16).astype(np.float64)
+    assert np.count_nonzero(np.abs(xd) < 2.0 ** -14) >= N // 4 - 8  # subnormals present
+    codes = np.zeros((M, N), dtype=np.int64)
+    cols = (np.arange(M) * 97 + 5) % N           # one code per row, spread over the groups
+    zero_rows = [3, 17, 36]
+    for i in range(M):
+        if i not in zero_rows:
+            codes[i, cols[i]] = 1 if i % 2 else -1
+    exps = synth.integers(404, 5, 0, M * g, -4, 4).reshape(M, g)
+    scales = synth.to_f16_bits(np.ldexp(1.0, exps))
+    A = codes.astype(np.int8) if dtype == "q8" else synth.pack_int4(codes)
+    t = upload(dtype, {"A": A, "x": xb, "scales": scales})
+    expect = np.zeros(M)
+    for i in range(M):
+        if i not in zero_rows:
+            expect[i] = codes[i, cols[i]] * np.ldexp(1.0, exps[i, cols[i] // 128]) * xd[cols[i]]
+    ran = set()
+    for v in mbg.variants(dtype):
+        try:
+            y = mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], t["scales"])
+        except mbg.GemvError as e:
+            assert e.status == mbg.ERR_UNSUPPORTED
+            continue
+        torch.cuda.synchronize()
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, expect), (v["name"], np.nonzero(got != expect)[0][:5])
+        ran.add(v["kind"])
+    assert {"mma", "smma", "bulk", "band"} <= ran or {"mma", "smma", "bulk"} <= ran, ran
 
 
 @pytest.mark.parametrize("dtype", ("q8", "q4"))
