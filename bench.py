@@ -849,6 +849,26 @@ def measure_configs(args, mbg, dev, l2, stream, timer, ceiling):
         del g_ov
         torch.cuda.empty_cache()
 
+    # the fixed cost of one launch in such a chain: the smallest GEMV (FP16,
+    # 2 x 512, 2 KB of weights, L2-resident), timed the same way; a matrix of
+    # B bytes cannot take less than about B / probe + this per launch
+    import numpy as np
+    wf = synth.random_case("f16", 2, 512, 7)
+    inf = synth.make(wf)
+    A_f = torch.from_numpy(inf["A"].view(np.float16)).to(dev)
+    x_f = torch.from_numpy(inf["x"].view(np.float16)).to(dev)
+    y_f = torch.empty(2, dtype=torch.float32, device=dev)
+    floor = {"shape": "f16 2x512 (2 KB of weights, L2-resident)"}
+    for key, ov in (("us", False), ("overlap_us", True)):
+        def launch(i, overlap):
+            mbg.gemv("f16", A_f, x_f, None, y=y_f, overlap=overlap)
+        plan = [(args.config_launches, 1)]
+        g = timer.capture(launch, plan, overlap=ov, copies=2)
+        timer.warm(g, plan, 1)
+        floor[key] = timer.timed(g, plan) / args.config_launches * 1e6
+        del g
+    out["launch_floor"] = floor
+
     for shape, names in INTERLEAVED.items():
         best = {n: float("inf") for n in names}
         for _ in range(args.interleave_rounds):
