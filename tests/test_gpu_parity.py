@@ -269,6 +269,41 @@ def test_exact_cases_every_variant(dtype):
     assert {"mma", "smma", "bulk", "band"} <= ran or {"mma", "smma", "bulk"} <= ran, ran
 
 
+@pytest.mark.parametrize("dtype,N", [("q8", 4096), ("q4", 4096), ("q4", 14336)])
+def test_scales_two_byte_aligned(dtype, N):
+    """Scales that start 2 bytes past an aligned address (legal for binary16):
+    every variant either computes the right result or refuses the call with
+    GEMV_ERR_UNSUPPORTED before launching (the INT4 MMA band reads two
+    neighbouring scales as one 4-byte word, the staged kernels copy whole
+    rows of scales in bulk); the automatic choice still works."""
+    M = 64
+    inp = synth.make(synth.random_case(dtype, M, N, 606 + N))
+    y_ref, den = reference(dtype, inp, M, N)
+    t = upload(dtype, inp)
+    sc = t["scales"].reshape(-1)
+    buf = torch.empty(sc.numel() + 8, dtype=sc.dtype, device="cuda")
+    buf[1:1 + sc.numel()].copy_(sc)
+    s_off = buf[1:1 + sc.numel()].view(t["scales"].shape)
+    assert s_off.data_ptr() % 4 == 2
+    y = mbg.gemv(dtype, t["A"], t["x"], s_off)
+    torch.cuda.synchronize()
+    assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} offset scales auto")
+    refused = set()
+    for v in mbg.variants(dtype):
+        try:
+            y = mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], s_off)
+        except mbg.GemvError as e:
+            assert e.status == mbg.ERR_UNSUPPORTED
+            refused.add(v["kind"])
+            continue
+        torch.cuda.synchronize()
+        assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} offset scales {v['name']}")
+    assert "smma" in refused
+    if dtype == "q4":
+        assert "mma" in refused
+    assert mbg.gemv_get_device_error() == mbg.OK
+
+
 @pytest.mark.parametrize("dtype", ("q8", "q4"))
 def test_dequant_bit_exact(dtype):
     orc = oracle.load()
