@@ -1118,9 +1118,9 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
 // keeps its chunks of the next TW tiles in flight in a rolling window of
 // registers (refilled in place, as in the row-band kernel).  Warp w takes the
 // steps w, w + NW, ..., so for every step index the block reads NW * 512
-// contiguous bytes of each row.  The four MMA pairs of a step go into two
-// accumulators whose first MMA starts from zero.  Rows must be exactly
-// NW * SPW * 512 bytes.
+// contiguous bytes of each row.  The MMAs of a step alternate between two
+// accumulators, each started from zero by its first MMA.  Rows must be
+// exactly NW * SPW * 512 bytes.
 __device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                  uint32_t a3, uint32_t b0, uint32_t b1)
 {
@@ -1604,15 +1604,16 @@ __global__ void __launch_bounds__(T, MINB) mbg_stageband_kernel(const GemvArgs p
 // bulk async copies (the staged row band's pipeline: thread 0 issues, every
 // wait bounded, the block barrier that closes a window of TW tiles frees its
 // stages).  The bytes in flight cost no registers, so the lookahead (PF
-// windows) can cover the memory latency while enough warps stay resident to
-// keep the MMA and unpacking pipes busy; the row pairs of a tile share the B
-// fragments and the per-tile bookkeeping.
+// windows) does not compete with the arithmetic for registers; the row pairs
+// of a tile share the B fragments and the per-tile bookkeeping.  (Measured
+// no faster than the register-resident band or the bulk pipeline on the
+// decode shapes: an explicit option.)
 //
 // Slots in a stage: lane (g, t) reads chunk t of slots k and 4 + k of row
 // g & 1 of each row pair, with k = (g >> 1) ^ (g & 1): the two rows of a
-// pair sit a multiple of 128 bytes apart, and flipping the slot order of the
-// odd row puts the eight lanes of every quarter-warp on 128 distinct bytes of
-// bank space (no bank conflicts).  B column 2k carries the x of slot k and
+// pair sit a multiple of 128 bytes apart, and the odd row's lanes taking the
+// neighbouring slot of their even-row partners puts the eight lanes of every
+// quarter-warp on 128 distinct bytes of bank space (no bank conflicts).  B column 2k carries the x of slot k and
 // column 2k + 1 that of slot 4 + k, so the results of A-rows g and g + 8 land
 // in lane (g, k), registers d[0] and d[3].
 template <int DT, int NW, int SPW, int RP, int TW, int PF, int MINB>
