@@ -70,7 +70,9 @@ KERNEL_NAMES = {"vec": "mbg_warprow_kernel", "tile": "mbg_rowtile_kernel", "bulk
 CONFIG_WORKLOADS = ["f32_1024", "f16_4096", "f16_up_14336x4096", "f16_down_4096x14336",
                     "sweep_f32_2048", "sweep_f32_4096", "sweep_f32_8192", "sweep_f32_16384",
                     "sweep_f16_2048", "sweep_f16_4096", "sweep_f16_8192", "sweep_f16_16384",
-                    "q8_4096x14336", "q8_14336x4096", "q4_4096x14336", "q4_14336x4096"]
+                    "q8_4096x14336", "q8_14336x4096", "q4_4096x14336", "q4_14336x4096",
+                    # format options: binary16 weights with an FP32 x, INT8 with one scale per row
+                    "f16x32_down_4096x14336", "q8row_4096x14336"]
 # FP16 / INT8 / INT4 at one shape, timed in interleaved rounds
 INTERLEAVED = {"4096x14336": ("f16_down_4096x14336", "q8_4096x14336", "q4_4096x14336"),
                "14336x4096": ("f16_up_14336x4096", "q8_14336x4096", "q4_14336x4096")}

@@ -287,7 +287,7 @@ int choose_variant(const DeviceState &d, int dtype, const void *A, const void *x
     if (!vec_ok) return find_variant(dtype, 32, XMODE_ELEM, KIND_ELEM);
     const int64_t chunks = rb / 16;
     const bool small_x = N * x_elem_bytes(dtype) <= kAutoSmemX;
-    if (dtype == DT_F32 || dtype == DT_F16) {
+    if (dtype == DT_F32 || dtype == DT_F16 || dtype == DT_F16X32) {
         for (int k = 0; k < n; ++k) {
             // a capped grid only for small matrices, where the next launch's
             // blocks starting beside it matter more than bytes in flight

@@ -6,6 +6,12 @@
 namespace mbg {
 
 static const Variant kTableF16X32[] = {
+    // row bands (x in registers) for rows they cover exactly, the FP16 row
+    // bands' shapes: band_t<threads>_c<chunks per thread>_g<rows per tile>_w<tiles in flight>
+    MBG_BAND(DT_F16X32, 896, 2, 2, 2, 1, "band_t896_c2_g2_w2"),
+    MBG_BAND(DT_F16X32, 256, 2, 2, 4, 2, "band_t256_c2_g2_w4"),
+    MBG_BAND(DT_F16X32, 512, 4, 2, 2, 1, "band_t512_c4_g2_w2"),
+    MBG_BAND(DT_F16X32, 448, 4, 2, 2, 1, "band_t448_c4_g2_w2"),
     MBG_TILE(DT_F16X32, 1, 8, 256, XMODE_BULK, "tile_g1_c8_t256_bulk"),
     MBG_TILE(DT_F16X32, 2, 8, 256, XMODE_BULK, "tile_g2_c8_t256_bulk"),
     MBG_TILE(DT_F16X32, 4, 8, 256, XMODE_BULK, "tile_g4_c8_t256_bulk"),

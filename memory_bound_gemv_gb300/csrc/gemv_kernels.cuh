@@ -784,7 +784,23 @@ template <int DT, bool PAIRED, int G>
 __device__ __forceinline__ void tile_chunk(const uint4 (&a)[G], const uint4 (&xv)[x_chunk_vecs<DT>()],
                                            float (&c0)[G], float (&c1)[G])
 {
-    if constexpr (DT == DT_F32) {
+    if constexpr (DT == DT_F16X32) {
+        // binary16 weights widened to FP32 (exact), FP32 x, FP32 FMAs: word q
+        // of a chunk holds columns 2q and 2q + 1, whose x sit in vector q / 2
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 &x = xv[q >> 1];
+            const float xa = __uint_as_float((q & 1) ? x.z : x.x);
+            const float xb = __uint_as_float((q & 1) ? x.w : x.y);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t w = q == 0 ? a[g].x : q == 1 ? a[g].y : q == 2 ? a[g].z : a[g].w;
+                const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+                c0[g] = fmaf(wf.x, xa, c0[g]);
+                c1[g] = fmaf(wf.y, xb, c1[g]);
+            }
+        }
+    } else if constexpr (DT == DT_F32) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             c0[g] = fmaf(__uint_as_float(a[g].x), __uint_as_float(xv[0].x), c0[g]);
@@ -922,7 +938,8 @@ __global__ void __launch_bounds__(T, MINB) mbg_rowband_kernel(const GemvArgs p)
     constexpr int ROWB = T * CPT * 16;  // bytes per row
     constexpr bool PAIRED = DT == DT_Q4;
     static_assert(T % 32 == 0 && NW <= 32, "block shape");
-    static_assert(F::XB == 2 || DT == DT_F32, "binary16 x (mixed-precision products) or FP32");
+    static_assert(F::XB == 2 || DT == DT_F32 || DT == DT_F16X32,
+                  "binary16 x (mixed-precision products), FP32, or binary16 weights with an FP32 x");
     static_assert((U & (U - 1)) == 0 && U <= 32, "rows in flight: a power of two up to 32");
 
     __shared__ float part[2][U][NW];
@@ -1994,8 +2011,8 @@ cudaError_t occupancy_band(int *blocks, size_t smem)
 #define MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, CAP, NAME)                                          \
     Variant{DT, T, (G) * (TW), CPT, T / 32, XMODE_REG, NAME, &launch_band<DT, T, CPT, G, TW, MINB>, \
             &smem_limit_band<DT, T, CPT, G, TW, MINB>, KIND_BAND, 0,                               \
-            &occupancy_band<DT, T, CPT, G, TW, MINB>, (DT) == DT_F32 ? MATH_F32 : MATH_MIXED, 0,   \
-            false, G, CAP}
+            &occupancy_band<DT, T, CPT, G, TW, MINB>,                                               \
+            ((DT) == DT_F32 || (DT) == DT_F16X32) ? MATH_F32 : MATH_MIXED, 0, false, G, CAP}
 #define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME) MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, 0, NAME)
 
 template <int DT, int NW, int SPW, int TW, int MINB>
