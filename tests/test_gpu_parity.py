@@ -269,6 +269,27 @@ def test_exact_cases_every_variant(dtype):
     assert {"mma", "smma", "bulk", "band"} <= ran or {"mma", "smma", "bulk"} <= ran, ran
 
 
+@pytest.mark.parametrize("dtype", ("q8", "q4", "f16", "f16x32"))
+def test_one_to_three_rows_every_variant(dtype):
+    """1, 2 and 3 rows at the decode row lengths: grids with more blocks than
+    tiles, a single tile whose second row does not exist, every variant
+    against the oracle."""
+    for N in (4096, 14336):
+        for M in (1, 2, 3):
+            inp = synth.make(synth.random_case(dtype, M, N, 700 + 10 * M + N))
+            y_ref, den = reference(dtype, inp, M, N)
+            t = upload(dtype, inp)
+            for v in mbg.variants(dtype):
+                try:
+                    y = mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], t.get("scales"))
+                except mbg.GemvError as e:
+                    assert e.status == mbg.ERR_UNSUPPORTED
+                    continue
+                torch.cuda.synchronize()
+                assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} {M}x{N} {v['name']}")
+    assert mbg.gemv_get_device_error() == mbg.OK
+
+
 @pytest.mark.parametrize("dtype,N", [("q8", 4096), ("q4", 4096), ("q4", 14336)])
 def test_scales_two_byte_aligned(dtype, N):
     """Scales that start 2 bytes past an aligned address (legal for binary16):
