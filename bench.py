@@ -1027,13 +1027,59 @@ def run_profile_softmax(args):
     return 0
 
 
+def run_profile_aux(args):
+    """The kernels off the GEMV and softmax paths, each launched once (for one ncu capture):
+    every read and copy probe pattern over 256 MiB (twice L2), the quantiser (INT8 per group,
+    INT8 per row, INT4) of the FP16 4096x14336 decode matrix and the dequantisation of its output,
+    one host-buffer call (x fetched by the copy kernel), the zero fill of an N = 0 call and the
+    softmax kernel for any layout (rows of 8191 values)."""
+    import numpy as np
+    import torch
+
+    import memory_bound_gemv_gb300 as mbg
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    words = (256 << 20) // 4
+    buf = torch.randint(-2 ** 31, 2 ** 31 - 1, (words,), dtype=torch.int32, generator=gen).to(dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    for v in range(len(mbg.probe_variants())):
+        mbg.gemv_probe_read(buf, sink, v)
+    dst = torch.empty_like(buf)
+    for v in range(len(mbg.copy_probe_variants())):
+        mbg.gemv_probe_copy(buf, dst, v)
+    torch.cuda.synchronize()
+    del buf, dst
+    w = synth.WORKLOADS[DEFAULT_WORKLOAD]
+    inp = synth.make(w)
+    W = torch.from_numpy(inp["A"].view(np.float16)).to(dev)
+    A8, S8 = mbg.quantize(W, "q8")
+    mbg.quantize(W, "q8row")
+    A4, S4 = mbg.quantize(W, "q4")
+    mbg.gemv_dequant_q8(A8, S8)
+    mbg.gemv_dequant_q4(A4, S4)
+    x_host = torch.from_numpy(inp["x"].view(np.float16)).pin_memory()
+    x_dev = torch.empty(w.N, dtype=torch.float16, device=dev)
+    y_host = mbg.gemv_host("f16", W, x_host, x_dev)
+    y0 = torch.full((w.M,), 7.0, device=dev)
+    _ = mbg.lib().gemv_f32(0, 0, y0.data_ptr(), w.M, 0, None)
+    xs = torch.randn(8192, 8191, generator=gen).to(torch.float16).to(dev)
+    ys = mbg.gemv_softmax_f16(xs)  # 8191 is no multiple of 8: the any-layout kernel
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": "aux", "y0": float(y_host[0].item()), "zero_fill": float(y0.abs().max().item()),
+                      "softmax_row_sum": float(ys[0].float().sum().item())}))
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--op", choices=("gemv", "softmax"), default="gemv")
+    p.add_argument("--op", choices=("gemv", "softmax", "aux"), default="gemv",
+                   help="aux (with --profile): the probes, quantiser, host copy and edge kernels once each")
     p.add_argument("--workload", default=None,
                    choices=sorted(synth.WORKLOADS) + sorted(synth.SOFTMAX_WORKLOADS))
     p.add_argument("--graph-max", type=int, default=GRAPH_MAX, help="launches per captured graph")
@@ -1060,6 +1106,10 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         p.error("--steps must be >= 1 and --warmup >= 0")
+    if args.op == "aux":
+        if not args.profile:
+            p.error("--op aux runs only with --profile")
+        return run_profile_aux(args)
     if args.workload is None:
         args.workload = "softmax_8192x8192" if args.op == "softmax" else DEFAULT_WORKLOAD
     if args.op == "softmax":

@@ -29,7 +29,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return v;
 }
 
-// 16-byte read-only load that may allocate in L1 (x, when it is not staged).
 // An ordinary 16-byte load cached in L2 only (not the read-only path).
 __device__ __forceinline__ uint4 ld_l2_16(const void *p)
 {
@@ -41,6 +40,7 @@ __device__ __forceinline__ uint4 ld_l2_16(const void *p)
     return v;
 }
 
+// 16-byte read-only load that may allocate in L1 (x, when it is not staged).
 __device__ __forceinline__ uint4 ld_cached16(const void *p)
 {
     uint4 v;

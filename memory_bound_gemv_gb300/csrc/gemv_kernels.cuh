@@ -1159,8 +1159,8 @@ __device__ __forceinline__ void mma_m16n8k16_f16_first(float (&d)[4], uint32_t a
 }
 
 // The code unpacking of q8_codes_h2 / q4_codes_h2 as volatile asm: kept in
-// program order between the (volatile) MMAs, so that a word's codes are
-// unpacked right before its MMAs and only one word's codes are live at a time.
+// program order between the (volatile) MMAs, so that a step's codes are
+// unpacked right before its MMAs and only one step's codes are live at a time.
 __device__ __forceinline__ uint32_t vlop3_sel_xor(uint32_t a, uint32_t b, uint32_t c)
 {
     uint32_t d;
@@ -1185,21 +1185,78 @@ __device__ __forceinline__ uint32_t vprmt(uint32_t a, uint32_t b, uint32_t sel)
     asm volatile("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
-__device__ __forceinline__ void q4_codes_h2_ordered(uint32_t w, uint32_t (&h)[4])
+// Two words of codes at once (the A fragments of one MMA step): all the
+// integer operations first, then the binary16 pair operations, so that no
+// pair operation issues right behind the integer operation it reads.
+__device__ __forceinline__ void q4_codes_h2_two(uint32_t wa, uint32_t wb, uint32_t (&ha)[4], uint32_t (&hb)[4])
 {
-    uint32_t v;
-    asm volatile("shr.b32 %0, %1, 8;" : "=r"(v) : "r"(w));
-    h[0] = vhsub2(vlop3_sel_xor(w, 0x64086408u, 0x000F000Fu), 0x64086408u);
-    h[1] = vhfma2(vlop3_sel_xor(w, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
-    h[2] = vhsub2(vlop3_sel_xor(v, 0x64086408u, 0x000F000Fu), 0x64086408u);
-    h[3] = vhfma2(vlop3_sel_xor(v, 0x64806480u, 0x00F000F0u), 0x2C002C00u, 0xD480D480u);
+    uint32_t va, vb;
+    asm volatile("shr.b32 %0, %1, 8;" : "=r"(va) : "r"(wa));
+    asm volatile("shr.b32 %0, %1, 8;" : "=r"(vb) : "r"(wb));
+    ha[0] = vlop3_sel_xor(wa, 0x64086408u, 0x000F000Fu);
+    hb[0] = vlop3_sel_xor(wb, 0x64086408u, 0x000F000Fu);
+    ha[1] = vlop3_sel_xor(wa, 0x64806480u, 0x00F000F0u);
+    hb[1] = vlop3_sel_xor(wb, 0x64806480u, 0x00F000F0u);
+    ha[2] = vlop3_sel_xor(va, 0x64086408u, 0x000F000Fu);
+    hb[2] = vlop3_sel_xor(vb, 0x64086408u, 0x000F000Fu);
+    ha[3] = vlop3_sel_xor(va, 0x64806480u, 0x00F000F0u);
+    hb[3] = vlop3_sel_xor(vb, 0x64806480u, 0x00F000F0u);
+    ha[0] = vhsub2(ha[0], 0x64086408u);
+    hb[0] = vhsub2(hb[0], 0x64086408u);
+    ha[1] = vhfma2(ha[1], 0x2C002C00u, 0xD480D480u);
+    hb[1] = vhfma2(hb[1], 0x2C002C00u, 0xD480D480u);
+    ha[2] = vhsub2(ha[2], 0x64086408u);
+    hb[2] = vhsub2(hb[2], 0x64086408u);
+    ha[3] = vhfma2(ha[3], 0x2C002C00u, 0xD480D480u);
+    hb[3] = vhfma2(hb[3], 0x2C002C00u, 0xD480D480u);
 }
-__device__ __forceinline__ void q8_codes_h2_ordered(uint32_t w, uint32_t (&h)[2])
+__device__ __forceinline__ void q8_codes_h2_two(uint32_t wa, uint32_t wb, uint32_t (&ha)[2], uint32_t (&hb)[2])
 {
-    uint32_t u;
-    asm volatile("xor.b32 %0, %1, 0x80808080;" : "=r"(u) : "r"(w));
-    h[0] = vhsub2(vprmt(u, 0x64646464u, 0x4140u), 0x64806480u);
-    h[1] = vhsub2(vprmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+    uint32_t ua, ub;
+    asm volatile("xor.b32 %0, %1, 0x80808080;" : "=r"(ua) : "r"(wa));
+    asm volatile("xor.b32 %0, %1, 0x80808080;" : "=r"(ub) : "r"(wb));
+    ha[0] = vprmt(ua, 0x64646464u, 0x4140u);
+    hb[0] = vprmt(ub, 0x64646464u, 0x4140u);
+    ha[1] = vprmt(ua, 0x64646464u, 0x4342u);
+    hb[1] = vprmt(ub, 0x64646464u, 0x4342u);
+    ha[0] = vhsub2(ha[0], 0x64806480u);
+    hb[0] = vhsub2(hb[0], 0x64806480u);
+    ha[1] = vhsub2(ha[1], 0x64806480u);
+    hb[1] = vhsub2(hb[1], 0x64806480u);
+}
+
+// A lane's two 16-byte chunks (one per slot) times its x fragments: eight
+// MMAs (INT4) or four (INT8) that alternate between two accumulators, each
+// started from zero by its first MMA, so that no MMA follows the one whose
+// result it adds to.  The slot sums are d[0][0] + d[1][0] (first slot) and
+// d[0][3] + d[1][3] (second slot) of a lane that holds results.
+template <int DT>
+__device__ __forceinline__ void mma_chunk_pair(const uint4 &c0, const uint4 &c1,
+                                               const uint4 (&x)[DT == DT_Q4 ? 4 : 2], float (&d)[2][4])
+{
+    const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w};
+    const uint32_t w1[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if constexpr (DT == DT_Q4) {
+            uint32_t h[4], h8[4];
+            q4_codes_h2_two(w0[k], w1[k], h, h8);
+            if (k == 0) {
+                mma_m16n8k16_f16_first(d[0], h[0], h8[0], h[1], h8[1], x[k].x, x[k].y);
+                mma_m16n8k16_f16_first(d[1], h[2], h8[2], h[3], h8[3], x[k].z, x[k].w);
+            } else {
+                mma_m16n8k16_f16(d[0], h[0], h8[0], h[1], h8[1], x[k].x, x[k].y);
+                mma_m16n8k16_f16(d[1], h[2], h8[2], h[3], h8[3], x[k].z, x[k].w);
+            }
+        } else {
+            uint32_t h[2], h8[2];
+            q8_codes_h2_two(w0[k], w1[k], h, h8);
+            const uint4 &xv = x[k >> 1];
+            const uint32_t b0 = (k & 1) ? xv.z : xv.x, b1 = (k & 1) ? xv.w : xv.y;
+            if (k < 2) mma_m16n8k16_f16_first(d[k & 1], h[0], h8[0], h[1], h8[1], b0, b1);
+            else mma_m16n8k16_f16(d[k & 1], h[0], h8[0], h[1], h8[1], b0, b1);
+        }
+    }
 }
 
 // Sums each of the TW values over the 16 lanes that share lane bit 2 (lanes
@@ -1371,34 +1428,14 @@ __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvAr
 #pragma unroll
         for (int s = 0; s < SPW; ++s) {
             float d[2][4];
-            const uint32_t w0[4] = {a[w][s][0].x, a[w][s][0].y, a[w][s][0].z, a[w][s][0].w};
-            const uint32_t w1[4] = {a[w][s][1].x, a[w][s][1].y, a[w][s][1].z, a[w][s][1].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float(&dk)[4] = d[k & 1];
-                if constexpr (DT == DT_Q4) {
-                    uint32_t h[4], h8[4];
-                    q4_codes_h2_ordered(w0[k], h);
-                    q4_codes_h2_ordered(w1[k], h8);
-                    if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], xr[s][k].x, xr[s][k].y);
-                    else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], xr[s][k].x, xr[s][k].y);
-                    mma_m16n8k16_f16(dk, h[2], h8[2], h[3], h8[3], xr[s][k].z, xr[s][k].w);
-                } else {
-                    uint32_t h[2], h8[2];
-                    q8_codes_h2_ordered(w0[k], h);
-                    q8_codes_h2_ordered(w1[k], h8);
-                    const uint4 &x = xr[s][k >> 1];
-                    const uint32_t b0 = (k & 1) ? x.z : x.x, b1 = (k & 1) ? x.w : x.y;
-                    if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], b0, b1);
-                    else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], b0, b1);
-                }
-            }
+            mma_chunk_pair<DT>(a[w][s][0], a[w][s][1], xr[s], d);
+            const float r0 = d[0][0] + d[1][0], r3 = d[0][3] + d[1][3];
             if constexpr (PAIR) {
                 const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc[w][s]));
-                acc = fmaf(sf.x, d[0][0] + d[1][0], acc);
-                acc = fmaf(sf.y, d[0][3] + d[1][3], acc);
+                acc = fmaf(sf.x, r0, acc);
+                acc = fmaf(sf.y, r3, acc);
             } else {
-                acc = fmaf(half_bits_to_float(sc[w][s]), (d[0][0] + d[1][0]) + (d[0][3] + d[1][3]), acc);
+                acc = fmaf(half_bits_to_float(sc[w][s]), r0 + r3, acc);
             }
         }
         return use ? acc : 0.f;
@@ -1746,31 +1783,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmastage_kernel(const GemvA
                     for (int r = 0; r < RP; ++r) {
                         const uint4 a0 = lds128(st + aoff[q] + r * pair_a);
                         const uint4 a1 = lds128(st + aoff[q] + r * pair_a + 256);
-                        const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w};
-                        const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w};
                         float d[2][4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            float(&dk)[4] = d[k & 1];
-                            if constexpr (DT == DT_Q4) {
-                                uint32_t h[4], h8[4];
-                                q4_codes_h2_ordered(w0[k], h);
-                                q4_codes_h2_ordered(w1[k], h8);
-                                if (k < 2)
-                                    mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], xr[q][k].x, xr[q][k].y);
-                                else
-                                    mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], xr[q][k].x, xr[q][k].y);
-                                mma_m16n8k16_f16(dk, h[2], h8[2], h[3], h8[3], xr[q][k].z, xr[q][k].w);
-                            } else {
-                                uint32_t h[2], h8[2];
-                                q8_codes_h2_ordered(w0[k], h);
-                                q8_codes_h2_ordered(w1[k], h8);
-                                const uint4 &x = xr[q][k >> 1];
-                                const uint32_t b0 = (k & 1) ? x.z : x.x, b1 = (k & 1) ? x.w : x.y;
-                                if (k < 2) mma_m16n8k16_f16_first(dk, h[0], h8[0], h[1], h8[1], b0, b1);
-                                else mma_m16n8k16_f16(dk, h[0], h8[0], h[1], h8[1], b0, b1);
-                            }
-                        }
+                        mma_chunk_pair<DT>(a0, a1, xr[q], d);
                         const uint32_t sp = st + r * pair_s;
                         float &av = acc[w * RP + r];
                         av = fmaf(lds_half_as_float(sp + soff[q][0]), d[0][0] + d[1][0], av);

@@ -115,3 +115,34 @@ def test_page_rmse_and_round_trip_at_decode_size():
     inp = {"A": A[rows].cpu().numpy(), "x": x_bits, "scales": S[rows].cpu().numpy().view(np.uint16).reshape(-1, 1)}
     y_ref, den = reference("q8row", inp, len(rows), N)
     assert_close("q8row", y.cpu().numpy()[rows], y_ref, den, "q8row after quantize")
+
+
+@pytest.mark.parametrize("f16", (False, True), ids=("fp32_in", "fp16_in"))
+@pytest.mark.parametrize("dtype", QDTYPES)
+def test_layout_paths_agree(dtype, f16):
+    """The same weights through the 16-byte path (aligned, whole groups) and through the general
+    path (the weights 2 or 4 bytes past a 16-byte boundary), each with and without the error sum:
+    codes and scales bit-exact with the oracle, the error sum within the reordering bound.  FP32
+    input adds a row of values around 1e9, whose residual w - s q is not exact in FP32 (the scale
+    saturates at 65504), so the error sum takes its double-precision branch."""
+    M, N = 48, 4096
+    W = _weights(M, N, 211, f16)
+    if not f16:
+        W[5, :] *= np.float32(1e9)
+    orc = oracle.load()
+    A_ref, S_ref, e_ref = orc.quantize(dtype, W.view(np.uint16) if f16 else W, M, N)
+    t = torch.from_numpy(np.ascontiguousarray(W)).cuda()
+    big = torch.empty(M * N + 8, dtype=t.dtype, device="cuda")
+    off = big[1:1 + M * N].view(M, N)
+    off.copy_(t)
+    assert off.data_ptr() % 16 != 0
+    for src in (t, off):
+        for want_err in (True, False):
+            err = torch.zeros(1, dtype=torch.float64, device="cuda") if want_err else None
+            A, S = mbg.quantize(src, dtype, sq_err=err)
+            torch.cuda.synchronize()
+            assert np.array_equal(A.cpu().numpy(), A_ref.reshape(A.shape)), (dtype, src is t, want_err)
+            assert np.array_equal(S.cpu().numpy().view(np.uint16).reshape(S_ref.shape), S_ref)
+            if want_err:
+                e = float(err.item())
+                assert abs(e - e_ref) <= M * N * 2.0 ** -52 * e_ref, (dtype, src is t, e, e_ref)
