@@ -323,7 +323,7 @@ gemv_status_t gemv_dequant_q4(const uint8_t *A, const uint16_t *scales, float *W
  * takes `unroll` steps of 512 bytes of each row (rows of exactly warps *
  * unroll * 512 bytes); the exact binary16 codes are multiplied by x and
  * summed in FP32 by the warp-level MMA instruction (mma.sync m16n8k16), x
- * held in registers; rows_per_group = rows in flight per thread;
+ * held in registers; rows_per_group = rows per window of tiles;
  * 7 = staged MMA row bands: the same arithmetic, with tiles of one or more
  * row pairs streamed into a ring of shared-memory stages by bulk async
  * copies (rows_per_group = rows per window of tiles).

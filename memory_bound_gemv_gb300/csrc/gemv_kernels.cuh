@@ -1320,7 +1320,7 @@ __device__ __forceinline__ void ld_u32_if(uint32_t &v, const void *p, bool pred)
                  : "l"(p), "r"(static_cast<int>(pred)));
 }
 
-template <int DT, int NW, int SPW, int TW, int MINB>
+template <int DT, int NW, int SPW, int TW, int MINB, bool RC>
 __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvArgs p)
 {
     static_assert(DT == DT_Q8 || DT == DT_Q4, "quantised weights only");
@@ -1328,16 +1328,23 @@ __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvAr
     constexpr int XV = DT == DT_Q4 ? 4 : 2;  // 16-byte x vectors per 16-byte chunk of codes
     constexpr int ROWB = NW * SPW * 512;     // bytes per row
     constexpr int U = 2 * TW;                // rows per window
-    // INT4: a lane's two slots are two neighbouring scale groups (one 4-byte
-    // load, groups a multiple of 8); INT8: both halves of one group, or the
-    // row's one scale
-    constexpr bool PAIR = DT == DT_Q4;
+    // Two lane layouts.  RC = false: lane (g, t) loads chunk t of the slots
+    // 2(g/2) and 2(g/2) + 1 of tile row g % 2 (A-rows g and g + 8; results in
+    // d[0] and d[3]); INT4: the two slots are neighbouring scale groups (one
+    // 4-byte load, groups a multiple of 8); INT8: both halves of one group, or
+    // the row's one scale.  RC = true: lane (g, t) loads chunk t of slot g of
+    // both tile rows, so each load instruction of a warp reads 512 contiguous
+    // bytes of one row (A-rows g and g + 8 are rows 0 and 1; results in
+    // d[g % 2] and d[2 + g % 2]); one scale per row, and one exchange across
+    // lane bit 2 per tile leaves each lane the sums of row g % 2 over the
+    // slots g and g ^ 1, as in the first layout.
+    constexpr bool PAIR = DT == DT_Q4 && !RC;
 
     __shared__ float part[2][U][NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int rsel = g & 1;          // tile row whose chunks this lane loads
+    const int rsel = g & 1;          // tile row whose sums this lane keeps
     const bool use = t == (g >> 1);  // this lane holds its A-rows' results
 
     const int64_t grid = gridDim.x;
@@ -1353,44 +1360,55 @@ __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvAr
     }
     if (!p.pdl) pdl_wait();
 
-    // byte offset of this lane's scale(s) of step s within the scales of its row
+    // byte offset of this lane's scale(s) of step s within the scales of a row
     int sidx[SPW];
 #pragma unroll
-    for (int s = 0; s < SPW; ++s) sidx[s] = (((((warp + s * NW) * 8 + 2 * (g >> 1)) * 4) >> p.scale_shift) * 2);
+    for (int s = 0; s < SPW; ++s)
+        sidx[s] = (((((warp + s * NW) * 8 + (RC ? g : 2 * (g >> 1))) * 4) >> p.scale_shift) * 2);
     const int64_t sgrp = p.groups;
 
     uint4 a[TW][SPW][2];
-    uint32_t sc[TW][SPW];  // binary16 scale bits (a pair, or one in the low half)
+    uint32_t sc[TW][SPW];           // binary16 scale bits (a pair, or one in the low half)
+    uint32_t sc1[RC ? TW : 1][SPW];  // RC: the scale of tile row 1
 #pragma unroll
     for (int w = 0; w < TW; ++w)
 #pragma unroll
         for (int s = 0; s < SPW; ++s) {
             a[w][s][0] = a[w][s][1] = make_uint4(0u, 0u, 0u, 0u);
             sc[w][s] = 0u;
+            if constexpr (RC) sc1[w][s] = 0u;
         }
     int in = 0;
-    const unsigned char *an = static_cast<const unsigned char *>(p.A) + (b * 2 + rsel) * ROWB + warp * 512 +
-                              (g >> 1) * 128 + t * 16;
+    // RC: tile row 0 (row 1 lies ROWB further); else this lane's tile row
+    const int64_t arow = RC ? 0 : rsel;
+    const unsigned char *an = static_cast<const unsigned char *>(p.A) + (b * 2 + arow) * ROWB + warp * 512 +
+                              (RC ? g * 64 : (g >> 1) * 128) + t * 16;
+    constexpr int SECOND = RC ? ROWB : 64;  // offset of the second load
     const int64_t astep = grid * 2 * ROWB;
-    const unsigned char *sn = reinterpret_cast<const unsigned char *>(p.scales + (b * 2 + rsel) * sgrp);
+    const unsigned char *sn = reinterpret_cast<const unsigned char *>(p.scales + (b * 2 + arow) * sgrp);
+    const int64_t srow = sgrp * 2;  // bytes of scales per row
     const int64_t sstep = grid * 2 * sgrp * 2;
     // FULL: the tile and both its rows exist (no predicates)
     auto load_tile = [&](int w, auto full) {
         constexpr bool FULL = decltype(full)::value;
-        const bool ok = FULL || (in < I && (b + static_cast<int64_t>(in) * grid) * 2 + rsel < p.M);
+        const int64_t row0 = (b + static_cast<int64_t>(in) * grid) * 2;
+        const bool ok0 = FULL || (in < I && row0 + arow < p.M);
+        const bool ok1 = FULL || (in < I && row0 + 1 < p.M);
 #pragma unroll
         for (int s = 0; s < SPW; ++s) {
             const unsigned char *q = an + s * NW * 512;
             if constexpr (FULL) {
                 ld_stream16_into(a[w][s][0], q);
-                ld_stream16_into(a[w][s][1], q + 64);
+                ld_stream16_into(a[w][s][1], q + SECOND);
                 if constexpr (PAIR) ld_u32_into(sc[w][s], sn + sidx[s]);
                 else ld_u16_into(sc[w][s], sn + sidx[s]);
+                if constexpr (RC) ld_u16_into(sc1[w][s], sn + srow + sidx[s]);
             } else {
-                ld_stream16_if(a[w][s][0], q, ok);
-                ld_stream16_if(a[w][s][1], q + 64, ok);
-                if constexpr (PAIR) ld_u32_if(sc[w][s], sn + sidx[s], ok);
-                else ld_u16_if(sc[w][s], sn + sidx[s], ok);
+                ld_stream16_if(a[w][s][0], q, ok0);
+                ld_stream16_if(a[w][s][1], q + SECOND, RC ? ok1 : ok0);
+                if constexpr (PAIR) ld_u32_if(sc[w][s], sn + sidx[s], ok0);
+                else ld_u16_if(sc[w][s], sn + sidx[s], ok0);
+                if constexpr (RC) ld_u16_if(sc1[w][s], sn + srow + sidx[s], ok1);
             }
         }
         asm volatile("add.s64 %0, %0, %1;" : "+l"(sn) : "l"(sstep));
@@ -1424,21 +1442,39 @@ __global__ void __launch_bounds__(NW * 32, MINB) mbg_mmaband_kernel(const GemvAr
     // its scales (no divergent branch); the lanes that hold no result (their
     // sums mix foreign slices) give 0 through one select per tile.
     auto tile_dot = [&](int w) -> float {
-        float acc = 0.f;
+        if constexpr (RC) {
+            float acc0 = 0.f, acc1 = 0.f;  // tile rows 0 and 1, slot g
 #pragma unroll
-        for (int s = 0; s < SPW; ++s) {
-            float d[2][4];
-            mma_chunk_pair<DT>(a[w][s][0], a[w][s][1], xr[s], d);
-            const float r0 = d[0][0] + d[1][0], r3 = d[0][3] + d[1][3];
-            if constexpr (PAIR) {
-                const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc[w][s]));
-                acc = fmaf(sf.x, r0, acc);
-                acc = fmaf(sf.y, r3, acc);
-            } else {
-                acc = fmaf(half_bits_to_float(sc[w][s]), r0 + r3, acc);
+            for (int s = 0; s < SPW; ++s) {
+                float d[2][4];
+                mma_chunk_pair<DT>(a[w][s][0], a[w][s][1], xr[s], d);
+                const float r0 = rsel ? d[0][1] + d[1][1] : d[0][0] + d[1][0];
+                const float r1 = rsel ? d[0][3] + d[1][3] : d[0][2] + d[1][2];
+                acc0 = fmaf(half_bits_to_float(sc[w][s]), r0, acc0);
+                acc1 = fmaf(half_bits_to_float(sc1[w][s]), r1, acc1);
             }
+            // keep row g % 2, hand the other row to lane bit 2's partner
+            // (slot g ^ 1, which keeps the other row)
+            const float keep = rsel ? acc1 : acc0, send = rsel ? acc0 : acc1;
+            const float acc = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            return use ? acc : 0.f;
+        } else {
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < SPW; ++s) {
+                float d[2][4];
+                mma_chunk_pair<DT>(a[w][s][0], a[w][s][1], xr[s], d);
+                const float r0 = d[0][0] + d[1][0], r3 = d[0][3] + d[1][3];
+                if constexpr (PAIR) {
+                    const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc[w][s]));
+                    acc = fmaf(sf.x, r0, acc);
+                    acc = fmaf(sf.y, r3, acc);
+                } else {
+                    acc = fmaf(half_bits_to_float(sc[w][s]), r0 + r3, acc);
+                }
+            }
+            return use ? acc : 0.f;
         }
-        return use ? acc : 0.f;
     };
 
     int half = 0;
@@ -2029,31 +2065,34 @@ cudaError_t occupancy_band(int *blocks, size_t smem)
             ((DT) == DT_F32 || (DT) == DT_F16X32) ? MATH_F32 : MATH_MIXED, 0, false, G, CAP}
 #define MBG_BAND(DT, T, CPT, G, TW, MINB, NAME) MBG_BAND_CAP(DT, T, CPT, G, TW, MINB, 0, NAME)
 
-template <int DT, int NW, int SPW, int TW, int MINB>
+template <int DT, int NW, int SPW, int TW, int MINB, bool RC>
 void launch_mmaband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)
 {
-    launch_maybe_pdl(mbg_mmaband_kernel<DT, NW, SPW, TW, MINB>, a, grid, NW * 32, smem, s, pdl);
+    launch_maybe_pdl(mbg_mmaband_kernel<DT, NW, SPW, TW, MINB, RC>, a, grid, NW * 32, smem, s, pdl);
 }
 
-template <int DT, int NW, int SPW, int TW, int MINB>
+template <int DT, int NW, int SPW, int TW, int MINB, bool RC>
 cudaError_t smem_limit_mmaband(int)
 {
     return cudaSuccess;  // static shared memory only
 }
 
-template <int DT, int NW, int SPW, int TW, int MINB>
+template <int DT, int NW, int SPW, int TW, int MINB, bool RC>
 cudaError_t occupancy_mmaband(int *blocks, size_t smem)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_mmaband_kernel<DT, NW, SPW, TW, MINB>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mbg_mmaband_kernel<DT, NW, SPW, TW, MINB, RC>,
                                                          NW * 32, smem);
 }
 
-// mma_w<warps>_s<steps per warp>_t<tiles in flight>_m<min blocks per SM>: rows
-// of exactly warps * steps * 512 bytes; x in registers; products on the MMA unit
-#define MBG_MMA(DT, NW, SPW, TW, MINB, NAME)                                                          \
-    Variant{DT, (NW) * 32, 2 * (TW), SPW, NW, XMODE_REG, NAME, &launch_mmaband<DT, NW, SPW, TW, MINB>, \
-            &smem_limit_mmaband<DT, NW, SPW, TW, MINB>, KIND_MMA, 0,                                   \
-            &occupancy_mmaband<DT, NW, SPW, TW, MINB>, MATH_MIXED, 0, false, 2, 0}
+// mma_w<warps>_s<steps per warp>_t<tiles in flight>_m<min blocks per SM>[_rc]:
+// rows of exactly warps * steps * 512 bytes; x in registers; products on the
+// MMA unit; _rc: each load instruction of a warp reads 512 contiguous bytes of
+// one row
+#define MBG_MMA_L(DT, NW, SPW, TW, MINB, RC, NAME)                                                         \
+    Variant{DT, (NW) * 32, 2 * (TW), SPW, NW, XMODE_REG, NAME, &launch_mmaband<DT, NW, SPW, TW, MINB, RC>, \
+            &smem_limit_mmaband<DT, NW, SPW, TW, MINB, RC>, KIND_MMA, 0,                                   \
+            &occupancy_mmaband<DT, NW, SPW, TW, MINB, RC>, MATH_MIXED, 0, false, 2, 0}
+#define MBG_MMA(DT, NW, SPW, TW, MINB, NAME) MBG_MMA_L(DT, NW, SPW, TW, MINB, false, NAME)
 
 template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>
 void launch_stageband(const GemvArgs &a, unsigned grid, size_t smem, cudaStream_t s, bool pdl)

@@ -39,6 +39,9 @@ static const Variant kTableQ8[] = {
     MBG_MMA(DT_Q8, 8, 1, 2, 4, "mma_w8_s1_t2_m4"),
     MBG_MMA(DT_Q8, 4, 2, 2, 4, "mma_w4_s2_t2_m4"),
     MBG_MMA(DT_Q8, 14, 2, 2, 2, "mma_w14_s2_t2_m2"),
+    // the same with row-contiguous loads
+    MBG_MMA_L(DT_Q8, 8, 1, 4, 2, true, "mma_w8_s1_t4_m2_rc"),
+    MBG_MMA_L(DT_Q8, 28, 1, 2, 1, true, "mma_w28_s1_t2_m1_rc"),
     // staged MMA row bands, smma_w<warps>_s<steps per warp>_r<row pairs per
     // tile>_t<tiles per window>_p<windows in flight>_m<min blocks per SM>:
     // rows of exactly warps * steps * 512 bytes (explicit choice)
