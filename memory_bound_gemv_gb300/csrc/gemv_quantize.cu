@@ -220,10 +220,11 @@ __device__ __forceinline__ void add_block_err(double err, double *sq_err)
 
 // Groups of exactly 128 columns (N a multiple of 128), 16-byte aligned W:
 // group k of the row-major sequence is W[128 k .. 128 k + 127], handled by
-// one half-warp whose lane l holds weights 8 l .. 8 l + 7 of it.  A warp
-// takes the groups 2 (UNROLL j + u) + h, u < UNROLL, of its j-th pass (all
-// loads first), so every pass of a warp reads 512 UNROLL contiguous bytes of
-// binary16 weights.
+// one half-warp whose lane l holds weights 8 l .. 8 l + 7 of it.  In each
+// pass a warp takes 2 UNROLL consecutive groups (group 2 u + h of its run to
+// half-warp h, u < UNROLL) and issues all their loads first; consecutive
+// warps take consecutive runs, so a pass of the grid reads one contiguous
+// span of W.
 template <int QMAX, bool F16IN, bool PACK4, bool ERR, int UNROLL>
 __global__ void __launch_bounds__(256) mbg_quantize_vec_kernel(const QuantArgs p)
 {
