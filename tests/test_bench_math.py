@@ -113,3 +113,13 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "3", "--warmup", "1"], capture_output=True, text=True,
                        timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_cli_rejects_aux_without_profile_and_bad_arguments():
+    """`--op aux` launches kernels for a profiler only; it and other bad argument sets are refused
+    by the argument parser (exit code 2) before anything touches a GPU."""
+    for argv in (["--op", "aux"], ["--steps", "0"], ["--warmup", "-1"],
+                 ["--op", "softmax", "--workload", "f16_4096"], ["--workload", "no_such_workload"]):
+        with pytest.raises(SystemExit) as e:
+            bench.main(argv)
+        assert e.value.code == 2, argv
