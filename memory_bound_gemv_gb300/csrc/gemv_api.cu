@@ -202,9 +202,10 @@ bool variant_fits(const Variant &v, const DeviceState &d, int dtype, const void 
         return rb / 16 == static_cast<int64_t>(v.lanes_per_row) * v.unroll;  // persistent grid
     }
     if (v.kind == KIND_MMA) {
-        // every warp takes exactly `unroll` steps of 512 bytes of each row; INT4
-        // reads the scales of two neighbouring groups as one 4-byte word
-        if (dtype == DT_Q4 && !aligned(scales, 4)) return false;
+        // every warp takes exactly `unroll` steps of 512 bytes of each row; the
+        // first INT4 layout reads the scales of two neighbouring groups as one
+        // 4-byte word
+        if (!aligned(scales, v.scale_align)) return false;
         return is_quant(dtype) && rb == static_cast<int64_t>(v.warps) * v.unroll * 512;  // persistent grid
     }
     if (v.kind == KIND_SMMA) {

@@ -92,6 +92,7 @@ struct Variant {
     int tile_rows = 1;   // row bands: consecutive rows per tile
     int max_blocks_per_sm = 0;  // cap on the persistent grid (0: as many as fit), leaving room
                                 // for the next launch's blocks to start alongside
+    int scale_align = 2;        // MMA row bands: alignment (bytes) the kernel needs of the scales
     bool supports_pdl() const
     {
         return kind == KIND_TILE || kind == KIND_BULK || kind == KIND_BAND || kind == KIND_SBAND ||

@@ -2091,7 +2091,8 @@ cudaError_t occupancy_mmaband(int *blocks, size_t smem)
 #define MBG_MMA_L(DT, NW, SPW, TW, MINB, RC, NAME)                                                         \
     Variant{DT, (NW) * 32, 2 * (TW), SPW, NW, XMODE_REG, NAME, &launch_mmaband<DT, NW, SPW, TW, MINB, RC>, \
             &smem_limit_mmaband<DT, NW, SPW, TW, MINB, RC>, KIND_MMA, 0,                                   \
-            &occupancy_mmaband<DT, NW, SPW, TW, MINB, RC>, MATH_MIXED, 0, false, 2, 0}
+            &occupancy_mmaband<DT, NW, SPW, TW, MINB, RC>, MATH_MIXED, 0, false, 2, 0,                  \
+            ((DT) == DT_Q4 && !(RC)) ? 4 : 2}
 #define MBG_MMA(DT, NW, SPW, TW, MINB, NAME) MBG_MMA_L(DT, NW, SPW, TW, MINB, false, NAME)
 
 template <int DT, int T, int CPT, int G, int TW, int PF, int MINB>

@@ -294,9 +294,10 @@ def test_one_to_three_rows_every_variant(dtype):
 def test_scales_two_byte_aligned(dtype, N):
     """Scales that start 2 bytes past an aligned address (legal for binary16):
     every variant either computes the right result or refuses the call with
-    GEMV_ERR_UNSUPPORTED before launching (the INT4 MMA band reads two
-    neighbouring scales as one 4-byte word, the staged kernels copy whole
-    rows of scales in bulk); the automatic choice still works."""
+    GEMV_ERR_UNSUPPORTED before launching (the first INT4 MMA band layout reads
+    two neighbouring scales as one 4-byte word, the staged kernels copy whole
+    rows of scales in bulk; the row-contiguous layout takes them); the
+    automatic choice still works."""
     M = 64
     inp = synth.make(synth.random_case(dtype, M, N, 606 + N))
     y_ref, den = reference(dtype, inp, M, N)
@@ -309,7 +310,7 @@ def test_scales_two_byte_aligned(dtype, N):
     y = mbg.gemv(dtype, t["A"], t["x"], s_off)
     torch.cuda.synchronize()
     assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} offset scales auto")
-    refused = set()
+    refused, ran = set(), set()
     for v in mbg.variants(dtype):
         try:
             y = mbg.gemv_run_variant(dtype, v["id"], t["A"], t["x"], s_off)
@@ -319,9 +320,12 @@ def test_scales_two_byte_aligned(dtype, N):
             continue
         torch.cuda.synchronize()
         assert_close(dtype, y.cpu().numpy(), y_ref, den, f"{dtype} offset scales {v['name']}")
+        ran.add(v["name"])
     assert "smma" in refused
     if dtype == "q4":
         assert "mma" in refused
+        # the row-contiguous layout loads one scale at a time
+        assert any(n.startswith("mma_") and n.endswith("_rc") for n in ran), sorted(ran)
     assert mbg.gemv_get_device_error() == mbg.OK
 
 
